@@ -1,0 +1,331 @@
+#!/usr/bin/env python
+"""Throughput of the fused IQL + HER train step on one GB300 (one JSON line).
+
+A step is one pass of the whole path over one batch: HER index sampling and
+relabel, V forward + expectile loss + policy + V backward, the primary
+gradient reduction with the per-source norms and budget coefficients, and
+Adam.  Inputs are synthetic (seeded, see synth/), resident in HBM before the
+timed region; per step a fresh Q [B, A] is read.  With --gpus N under
+torchrun every rank runs an independent replica (the step has no exchange).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "IQL+HER train steps/s and samples/s at B=16384; % tensor/HBM roofline"
+UNIT = "samples/s"
+SMS = 152
+FP32_LANES_PER_SM = 128
+PROFILE_NOTE = "profiles/ (ncu launch list and per-kernel summaries)"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=synth.PROD.name, choices=[w.name for w in synth.ALL])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="bounded oracle sample (CPU baseline)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}, \
+        "fallback"
+
+
+def algorithmic(w):
+    """Algorithmic work of one step, per phase: bytes moved and flops."""
+    b, s, a, p, n, g = w.batch, w.state_dim, w.num_actions, w.n_params, w.n_nets, w.goal_dim
+    nh = w.her_count
+    relabel = b * (2 * s * 4 + 12) * 2 + b * 8 + nh * 4 * g + (nh * 4 if w.strategy != "random" else 0)
+    vnet_bytes = b * s * 4 + b * 4 + b * a * 4 + n * (p * 4 + b * 4 * (2 + a) + p * 4)
+    flops = n * 2 * b * (2 * s * w.hidden + 3 * w.hidden ** 2 + 3 * w.hidden)
+    optim_bytes = n * 4 * p * (6 + 2 + 2 * w.n_aux)
+    return dict(relabel_bytes=relabel, vnet_bytes=vnet_bytes, vnet_flops=flops, optim_bytes=optim_bytes,
+                total_bytes=relabel + vnet_bytes + optim_bytes)
+
+
+class Clocks:
+    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_baseline(w, seconds):
+    """The oracle as it stands, on this host, on a bounded sample of the workload."""
+    from oracle import step as ostep
+    rep = synth.make_replay(w)
+    cfg = ostep.config_from_workload(w)
+    nets = [ostep.NetState.fresh(synth.make_params(w, k), w.taus[k]) for k in range(w.n_nets)]
+    k = 0
+    t0 = time.perf_counter()
+    while True:
+        q = synth.make_q(w, k)
+        aux = [synth.make_aux(w, k, n) for n in range(w.n_nets)] if w.n_aux else None
+        ostep.train_step(cfg, rep, k, q, nets, aux)
+        k += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or k >= 50:
+            break
+    return {"value": k * w.batch / el, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{k} full steps (B={w.batch}) of {w.name} in {el:.1f} s, numpy fp64 with its default "
+                      f"BLAS threading; index sampling in single-threaded Python"}
+
+
+def run_reference(args, w):
+    """--impl reference: the CPU oracle (the slow definition) timed on this host."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import step as ostep
+    sample_rows = 2048
+    ws = synth.scaled(w, batch=sample_rows)
+    rep = synth.make_replay(w)
+    cfg = ostep.config_from_workload(ws)
+    nets = [ostep.NetState.fresh(synth.make_params(w, k), w.taus[k]) for k in range(w.n_nets)]
+
+    def one(k):
+        q = synth.make_q(ws, k)
+        aux = [synth.make_aux(w, k, n) for n in range(w.n_nets)] if w.n_aux else None
+        ostep.train_step(cfg, rep, k, q, nets, aux)
+
+    for k in range(args.warmup):
+        one(k)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        one(args.warmup + k)
+    el = time.perf_counter() - t0
+    value = args.steps * sample_rows / el
+    sample = (f"each step: {sample_rows} rows of the {w.name} batch (full-size replay buffer and V network), "
+              f"numpy fp64 oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": sample_rows, "hidden": w.hidden, "state_dim": w.state_dim},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import offline_rl_step_gb300 as ofrl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    rep = synth.make_replay(w)
+    replay = ofrl.Replay(dev(rep["states"]), dev(rep["next_states"]), dev(rep["actions"]), dev(rep["rewards"]),
+                         dev(rep["dones"]), w.state_dim, w.goal_dim, dev(rep["episode_ends"]))
+    replay_bytes = sum(t.numel() * t.element_size() for t in (replay.states, replay.next_states))
+    del rep
+    her = ofrl.HerConfig(w.batch, w.her_count, w.strategy, w.goal_threshold, w.seed + rank)
+    ctx = ofrl.Context(w.state_dim, w.hidden, w.num_actions, w.prec, max_batch=w.batch, max_nets=w.n_nets)
+    nets = [ofrl.VNet.from_params(torch.from_numpy(synth.make_params(w, k)), w.taus[k]) for k in range(w.n_nets)]
+    opt = ofrl.Opt(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
+                   max_grad_norm=w.max_grad_norm, beta=w.beta, budget=w.budget)
+    batch = ofrl.Batch.empty(w.batch, w.state_stride)
+    n, b, a = w.n_nets, w.batch, w.num_actions
+    v_out = torch.empty(n, b, device="cuda")
+    pi_out = torch.empty(n, b, a, device="cuda")
+    am_out = torch.empty(n, b, dtype=torch.int32, device="cuda")
+    loss_out = torch.empty(n, device="cuda")
+    norms_out = torch.empty(n, 5, device="cuda")
+    total = args.warmup + args.steps
+    q_host = np.stack([synth.make_q(w, k) for k in range(total)])
+    q_dev = dev(q_host)
+    aux_dev = None
+    if w.n_aux:
+        aux_dev = [[dev(x) for x in synth.make_aux(w, k, 0)] for k in range(total)]
+    plan = ofrl.StepPlan(ctx, replay, her, batch, nets, opt, n_aux=w.n_aux, v_out=v_out, pi_out=pi_out,
+                         argmax_out=am_out, loss_out=loss_out, norms_out=norms_out)
+
+    def step(k):
+        plan.run(k, q_dev[k], [aux_dev[k]] if aux_dev is not None else None)
+
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, device time by CUDA events ----
+    clocks = Clocks(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for k in range(args.warmup, total):
+        step(k)
+    e1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * args.steps * w.batch / (ms / 1e3)
+
+    # ---- per-phase device time (CUDA events inside the step, same stream) ----
+    ofrl.profile_begin(ctx, args.steps)
+    for k in range(args.warmup, total):
+        step(k)
+    phase_ms, nprof = ofrl.profile_end(ctx)
+    phase_avg = {p: v / max(nprof, 1) for p, v in phase_ms.items()}
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        qh = torch.from_numpy(q_host).pin_memory()
+        q_stage = torch.empty_like(q_dev[0])
+        loss_h = torch.empty(n, pin_memory=True)
+        norms_h = torch.empty(n, 5, pin_memory=True)
+        torch.cuda.synchronize()
+        e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2.record()
+        for k in range(args.warmup, total):
+            q_stage.copy_(qh[k], non_blocking=True)
+            plan.run(k, q_stage, [aux_dev[k]] if aux_dev is not None else None)
+            loss_h.copy_(loss_out, non_blocking=True)
+            norms_h.copy_(norms_out, non_blocking=True)
+        e3.record()
+        torch.cuda.synchronize()
+        ems = e2.elapsed_time(e3)
+        if world > 1:
+            t = torch.tensor([ems], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * args.steps * w.batch / (ems / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(b * a * 4), "d2h_bytes_per_step": int(n * 4 + n * 5 * 4)}
+    plan.sync_t()
+    status = ctx.poll_status()
+
+    # ---- roofline of the dominant kernel ----
+    pk, pk_kind = peaks()
+    alg = algorithmic(w)
+    dominant = max(phase_avg, key=phase_avg.get)
+    dur_s = phase_avg[dominant] / 1e3
+    sm_mhz = pk.get("sm_max_mhz", 2070.0)
+    if dominant == "vnet":
+        fp32_peak = SMS * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+        ach = alg["vnet_flops"] / dur_s / 1e12
+        roof = {"kernel": "vnet_fwd_bwd", "bound": "alu", "achieved": ach, "peak": fp32_peak, "unit": "TFLOP/s",
+                "frac": ach / fp32_peak, "traffic": None,
+                "peak_source": f"fp32 FMA: {SMS} SMs x {FP32_LANES_PER_SM} lanes x 2 x {sm_mhz:.0f} MHz"}
+    else:
+        key = {"relabel": "relabel_bytes", "reduce": "optim_bytes", "adam": "optim_bytes"}[dominant]
+        ach = alg[key] / dur_s / 1e9
+        roof = {"kernel": dominant, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / pk["hbm_gbs"], "traffic": None, "peak_source": f"hbm_gbs ({pk_kind})"}
+    roof["phase_ms"] = {p: round(v, 5) for p, v in phase_avg.items()}
+    roof["relabel_hbm_frac"] = alg["relabel_bytes"] / (phase_avg["relabel"] / 1e3) / 1e9 / pk["hbm_gbs"]
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "steps_per_s": 1e3 / ms_per_step * world,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.prec == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "state_dim": w.state_dim, "hidden": w.hidden,
+                       "num_actions": w.num_actions, "n_nets": w.n_nets, "her": f"{w.strategy} {w.her_ratio}",
+                       "capacity": w.capacity, "parallelism": f"replicas{world}",
+                       "l2": f"inputs larger than L2: replay buffer {replay_bytes / 2**20:.0f} MiB read at "
+                             f"random rows every step"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 4 * args.steps, "clocks": clk, "status": status,
+        }
+        print(json.dumps(line))
+    ctx.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    w = synth.BY_NAME[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,305 @@
+"""GB300 (sm_103a) fused offline-RL train step: HER relabel + IQL value update.
+
+A thin Python binding over the C ABI of include/ofrl.h.  Every function
+marshals torch CUDA tensors into device pointers and calls the library on
+the current torch stream; all arithmetic runs in the library's CUDA kernels.
+There is no CPU path: if libofrl.so is missing, importing the binding's
+calls raises.
+
+Functions (same names as the C entry points, without the ofrl_ prefix):
+  Context(...)                  ofrl_create / ofrl_destroy / ofrl_poll_status
+  her_relabel(...)              HER index sampling + gather + relabel
+  iql_value_fwd_bwd(...)        V forward + expectile loss + V backward
+  expectile_loss(...)           expectile loss and dL/dV
+  adv_weighted_policy(...)      softmax(beta * clamp(Q - V, -10, 10)), argmax
+  budgeted_clip_saxpy(...)      budgeted per-source clip + SAXPY, norms
+  adam_step(...)                Adam with the safety clip
+  train_step(...)               the fused step composed of the above
+"""
+import ctypes as C
+from dataclasses import dataclass, field
+from typing import List, Optional, Sequence
+
+import torch
+
+from . import _abi
+from ._abi import (HER_FINAL, HER_FUTURE, HER_RANDOM, PREC_BF16, PREC_FP32,  # noqa: F401
+                   STAT_BAD_ACTION, STAT_BAD_INDEX, STAT_NONFINITE_GRAD, STAT_TIMEOUT, OfrlError)
+
+STRATEGY = {"final": HER_FINAL, "future": HER_FUTURE, "random": HER_RANDOM}
+PRECISION = {"fp32": PREC_FP32, "bf16": PREC_BF16}
+BUDGET = (0.70, 0.15, 0.10, 0.05)
+
+
+def n_params(state_dim: int, hidden: int) -> int:
+    return hidden * state_dim + hidden + hidden * hidden + hidden + hidden + 1
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+F32, I32 = torch.float32, torch.int32
+
+
+@dataclass
+class Replay:
+    """Replay buffer (device tensors): states/next_states [capacity, stride]."""
+    states: torch.Tensor
+    next_states: torch.Tensor
+    actions: torch.Tensor
+    rewards: torch.Tensor
+    dones: torch.Tensor
+    state_dim: int
+    goal_dim: int
+    episode_ends: Optional[torch.Tensor] = None
+
+    def c(self):
+        cap, stride = self.states.shape
+        ne = 0 if self.episode_ends is None else int(self.episode_ends.numel())
+        return _abi.Replay(_ptr(self.states, F32, "states"), _ptr(self.next_states, F32, "next_states"),
+                           _ptr(self.actions, I32, "actions"), _ptr(self.rewards, F32, "rewards"),
+                           _ptr(self.dones, F32, "dones"), _ptr(self.episode_ends, I32, "episode_ends"),
+                           cap, ne, self.state_dim, stride, self.goal_dim)
+
+
+@dataclass
+class HerConfig:
+    batch: int
+    her_count: int
+    strategy: str = "future"
+    goal_threshold: float = 0.01
+    seed: int = 0
+
+    def c(self):
+        return _abi.HerCfg(self.batch, self.her_count, STRATEGY[self.strategy], self.goal_threshold,
+                           self.seed & ((1 << 64) - 1))
+
+
+@dataclass
+class Batch:
+    """Relabelled batch (device tensors), written by her_relabel / train_step."""
+    states: torch.Tensor
+    next_states: torch.Tensor
+    actions: torch.Tensor
+    rewards: torch.Tensor
+    dones: torch.Tensor
+    src_idx: torch.Tensor
+    donor_idx: torch.Tensor
+
+    @classmethod
+    def empty(cls, batch: int, stride: int, device="cuda"):
+        f = dict(device=device, dtype=F32)
+        i = dict(device=device, dtype=I32)
+        return cls(torch.empty(batch, stride, **f), torch.empty(batch, stride, **f), torch.empty(batch, **i),
+                   torch.empty(batch, **f), torch.empty(batch, **f), torch.empty(batch, **i),
+                   torch.empty(batch, **i))
+
+    def c(self):
+        return _abi.Batch(_ptr(self.states, F32, "batch.states"), _ptr(self.next_states, F32, "batch.next_states"),
+                          _ptr(self.actions, I32, "batch.actions"), _ptr(self.rewards, F32, "batch.rewards"),
+                          _ptr(self.dones, F32, "batch.dones"), _ptr(self.src_idx, I32, "batch.src_idx"),
+                          _ptr(self.donor_idx, I32, "batch.donor_idx"), self.states.shape[1])
+
+
+@dataclass
+class VNet:
+    """One V network's trainable state: params, Adam moments m and v, step t."""
+    params: torch.Tensor
+    m: torch.Tensor
+    v: torch.Tensor
+    tau: float
+    t: int = 0
+
+    @classmethod
+    def from_params(cls, params: torch.Tensor, tau: float):
+        p = params.detach().to(device="cuda", dtype=F32).contiguous().clone()
+        return cls(p, torch.zeros_like(p), torch.zeros_like(p), float(tau), 0)
+
+
+@dataclass
+class Opt:
+    lr: float = 3e-4
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
+    weight_decay: float = 0.0
+    max_grad_norm: float = 1.0
+    beta: float = 3.0
+    budget: Sequence[float] = BUDGET
+    alpha: Sequence[float] = (1.0, 1.0, 1.0, 1.0)
+
+    def c(self):
+        b = (C.c_float * 4)(*[float(x) for x in (list(self.budget) + [0.0] * 4)[:4]])
+        a = (C.c_float * 4)(*[float(x) for x in (list(self.alpha) + [0.0] * 4)[:4]])
+        return _abi.Opt(self.lr, self.beta1, self.beta2, self.eps, self.weight_decay, self.max_grad_norm,
+                        self.beta, b, a)
+
+
+class Context:
+    """Device workspace for one V-network shape (ofrl_create); the only allocation."""
+
+    def __init__(self, state_dim: int, hidden: int, num_actions: int, prec: str = "fp32",
+                 max_batch: int = 16384, max_nets: int = 1):
+        self._lib = _abi.load()
+        self.shape = _abi.VShape(state_dim, hidden, num_actions, PRECISION[prec])
+        self.state_dim, self.hidden, self.num_actions, self.prec = state_dim, hidden, num_actions, prec
+        self.max_batch, self.max_nets = max_batch, max_nets
+        self.n_params = n_params(state_dim, hidden)
+        h = C.c_void_p()
+        _abi.check("ofrl_create", self._lib.ofrl_create(C.byref(self.shape), max_batch, max_nets, C.byref(h)))
+        self.handle = h
+
+    def close(self):
+        if self.handle is not None and self.handle.value:
+            _abi.check("ofrl_destroy", self._lib.ofrl_destroy(self.handle))
+        self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def poll_status(self, stream=None):
+        words = (C.c_int32 * _abi.STAT_WORDS)()
+        _abi.check("ofrl_poll_status", self._lib.ofrl_poll_status(self.handle, _stream(stream), words))
+        return {"nonfinite_grad": words[_abi.STAT_NONFINITE_GRAD], "bad_action": words[_abi.STAT_BAD_ACTION],
+                "bad_index": words[_abi.STAT_BAD_INDEX], "timeout": words[_abi.STAT_TIMEOUT]}
+
+    def workspace_bytes(self) -> int:
+        return int(self._lib.ofrl_workspace_bytes(C.byref(self.shape), self.max_batch, self.max_nets))
+
+
+def her_relabel(ctx: Context, replay: Replay, her: HerConfig, step: int, out: Batch, stream=None):
+    r, h, b = replay.c(), her.c(), out.c()
+    _abi.check("ofrl_her_relabel", ctx._lib.ofrl_her_relabel(ctx.handle, C.byref(r), C.byref(h), step,
+                                                              C.byref(b), _stream(stream)))
+
+
+def iql_value_fwd_bwd(ctx: Context, params, states, q_taken, tau: float, v_out, loss_out, grad_out,
+                      stream=None):
+    batch = int(q_taken.numel())
+    _abi.check("ofrl_iql_value_fwd_bwd", ctx._lib.ofrl_iql_value_fwd_bwd(
+        ctx.handle, _ptr(params, F32, "params"), _ptr(states, F32, "states"), states.shape[1], batch,
+        _ptr(q_taken, F32, "q_taken"), tau, _ptr(v_out, F32, "v_out"), _ptr(loss_out, F32, "loss_out"),
+        _ptr(grad_out, F32, "grad_out"), _stream(stream)))
+
+
+def expectile_loss(ctx: Context, q_taken, v, tau: float, loss_out, dv_out=None, stream=None):
+    _abi.check("ofrl_expectile_loss", ctx._lib.ofrl_expectile_loss(
+        ctx.handle, _ptr(q_taken, F32, "q_taken"), _ptr(v, F32, "v"), int(v.numel()), tau,
+        _ptr(loss_out, F32, "loss_out"), _ptr(dv_out, F32, "dv_out"), _stream(stream)))
+
+
+def adv_weighted_policy(ctx: Context, q, v, beta: float, pi_out, argmax_out=None, stream=None):
+    b, a = q.shape
+    _abi.check("ofrl_adv_weighted_policy", ctx._lib.ofrl_adv_weighted_policy(
+        ctx.handle, _ptr(q, F32, "q"), _ptr(v, F32, "v"), b, a, beta, _ptr(pi_out, F32, "pi_out"),
+        _ptr(argmax_out, I32, "argmax_out"), _stream(stream)))
+
+
+def budgeted_clip_saxpy(ctx: Context, sources: List[torch.Tensor], budget_frac, alpha, max_grad_norm: float,
+                        grad_out, norms_out=None, stream=None):
+    k = len(sources)
+    n = int(sources[0].numel())
+    ptrs = (C.c_void_p * k)(*[_ptr(s, F32, "source").value for s in sources])
+    bf = (C.c_float * k)(*[float(x) for x in budget_frac[:k]])
+    al = (C.c_float * k)(*[float(x) for x in alpha[:k]])
+    _abi.check("ofrl_budgeted_clip_saxpy", ctx._lib.ofrl_budgeted_clip_saxpy(
+        ctx.handle, ptrs, bf, al, k, n, max_grad_norm, _ptr(grad_out, F32, "grad_out"),
+        _ptr(norms_out, F32, "norms_out"), _stream(stream)))
+
+
+def adam_step(ctx: Context, p, g, m, v, t: int, opt: Opt, grad_norm=None, stream=None):
+    o = opt.c()
+    _abi.check("ofrl_adam_step", ctx._lib.ofrl_adam_step(
+        ctx.handle, _ptr(p, F32, "p"), _ptr(g, F32, "g"), _ptr(m, F32, "m"), _ptr(v, F32, "v"), int(p.numel()),
+        t, C.byref(o), _ptr(grad_norm, F32, "grad_norm"), _stream(stream)))
+
+
+def train_step(ctx: Context, replay: Replay, her: HerConfig, step: int, batch: Batch, q, nets: List[VNet],
+               opt: Opt, aux: Optional[List[List[torch.Tensor]]] = None, v_out=None, pi_out=None,
+               argmax_out=None, loss_out=None, norms_out=None, grad_out=None, stream=None):
+    """One fused step; increments every net's t."""
+    r, h, b, o = replay.c(), her.c(), batch.c(), opt.c()
+    n_nets = len(nets)
+    cn = (_abi.VNet * n_nets)(*[_abi.VNet(_ptr(x.params, F32, "params"), _ptr(x.m, F32, "m"),
+                                          _ptr(x.v, F32, "v"), x.t, x.tau) for x in nets])
+    n_aux = 0 if not aux else len(aux[0])
+    aux_arr = None
+    if n_aux:
+        flat = [_ptr(t, F32, "aux").value for per in aux for t in per]
+        aux_arr = (C.c_void_p * len(flat))(*flat)
+    _abi.check("ofrl_train_step", ctx._lib.ofrl_train_step(
+        ctx.handle, C.byref(r), C.byref(h), step, C.byref(b), _ptr(q, F32, "q"), cn, n_nets, C.byref(o),
+        aux_arr, n_aux, _ptr(v_out, F32, "v_out"), _ptr(pi_out, F32, "pi_out"),
+        _ptr(argmax_out, I32, "argmax_out"), _ptr(loss_out, F32, "loss_out"),
+        _ptr(norms_out, F32, "norms_out"), _ptr(grad_out, F32, "grad_out"), _stream(stream)))
+    for k in range(n_nets):
+        nets[k].t = cn[k].t
+
+
+class StepPlan:
+    """train_step with every argument marshalled once.
+
+    Per call only the step index, the Q pointer and the optional auxiliary
+    source pointers change; the networks' t counters live in the C array and
+    advance there.  Same semantics as train_step.
+    """
+
+    def __init__(self, ctx: Context, replay: Replay, her: HerConfig, batch: Batch, nets: List[VNet], opt: Opt,
+                 n_aux: int = 0, v_out=None, pi_out=None, argmax_out=None, loss_out=None, norms_out=None,
+                 grad_out=None):
+        self.ctx, self.nets = ctx, nets
+        self._keep = (replay, batch, nets, v_out, pi_out, argmax_out, loss_out, norms_out, grad_out)
+        self.r, self.h, self.b, self.o = replay.c(), her.c(), batch.c(), opt.c()
+        self.n_nets = len(nets)
+        self.cn = (_abi.VNet * self.n_nets)(*[_abi.VNet(_ptr(x.params, F32), _ptr(x.m, F32), _ptr(x.v, F32),
+                                                        x.t, x.tau) for x in nets])
+        self.n_aux = n_aux
+        self.aux_arr = (C.c_void_p * max(1, self.n_nets * n_aux))()
+        self.outs = [_ptr(v_out, F32), _ptr(pi_out, F32), _ptr(argmax_out, I32), _ptr(loss_out, F32),
+                     _ptr(norms_out, F32), _ptr(grad_out, F32)]
+        self.fn = ctx._lib.ofrl_train_step
+        self.rp, self.hp, self.bp, self.op = C.byref(self.r), C.byref(self.h), C.byref(self.b), C.byref(self.o)
+
+    def run(self, step: int, q: torch.Tensor, aux=None, stream=None):
+        if self.n_aux:
+            flat = [t.data_ptr() for per in aux for t in per]
+            for i, p in enumerate(flat):
+                self.aux_arr[i] = p
+        code = self.fn(self.ctx.handle, self.rp, self.hp, step, self.bp, C.c_void_p(q.data_ptr()), self.cn,
+                       self.n_nets, self.op, self.aux_arr if self.n_aux else None, self.n_aux, *self.outs,
+                       _stream(stream))
+        if code != _abi.OK:
+            _abi.check("ofrl_train_step", code)
+
+    def sync_t(self):
+        for k in range(self.n_nets):
+            self.nets[k].t = self.cn[k].t
+
+
+def profile_begin(ctx: Context, max_steps: int):
+    _abi.check("ofrl_profile_begin", ctx._lib.ofrl_profile_begin(ctx.handle, max_steps))
+
+
+def profile_end(ctx: Context):
+    """Per-phase device milliseconds summed over the profiled steps, and the step count."""
+    ms = (C.c_float * len(_abi.PHASES))()
+    n = C.c_int32()
+    _abi.check("ofrl_profile_end", ctx._lib.ofrl_profile_end(ctx.handle, ms, C.byref(n)))
+    return dict(zip(_abi.PHASES, list(ms))), int(n.value)

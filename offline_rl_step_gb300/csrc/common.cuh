@@ -1,0 +1,236 @@
+// Shared device helpers and the context layout of the ofrl library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/ofrl.h"
+
+namespace ofrl {
+
+constexpr int kMaxNets = 2;
+constexpr int kMaxSrc = 4;        // primary + up to three auxiliary sources
+constexpr int kGramPairs = 10;    // upper triangle of a 4x4 Gram matrix
+constexpr int kScalars = 32;      // per-network scalar slots (see Scalar)
+constexpr int kMaxActions = 16;
+constexpr int kMaxStateDim = 64;
+
+// Per-network scalar slots written by the reduction's last block.
+enum Scalar {
+    SC_NORM0 = 0,     // n_0 .. n_3 (pre-clip source norms)
+    SC_COEF0 = 4,     // alpha_k * s_k .. (4 slots)
+    SC_COMBINED = 8,  // ||G||
+    SC_LOSS = 9,      // mean expectile loss
+};
+
+// Upper-triangle index of the pair (j, k), j <= k < 4.
+__host__ __device__ constexpr int gram_index(int j, int k) {
+    return j * 4 - (j * (j - 1)) / 2 + (k - j);
+}
+
+struct Workspace {
+    float* partials;      // [max_nets][max_tiles][P] per-tile gradient partials
+    float* tile_loss;     // [max_nets][max_tiles] per-tile sum of w d^2
+    float* g0;            // [max_nets][P] primary gradient when the caller gives no buffer
+    float* gram_part;     // [max_nets][max_gram_blocks][kGramPairs]
+    float* scalars;       // [max_nets][kScalars]
+    unsigned int* counter;  // [max_nets] last-block tickets (reset by the last block)
+    int32_t* status;      // [OFRL_STAT_WORDS]
+};
+
+}  // namespace ofrl
+
+struct ofrl_ctx {
+    int device;
+    int num_sms;
+    ofrl_vshape shape;
+    int32_t max_batch;
+    int32_t max_nets;
+    int32_t max_tiles;
+    int32_t max_gram_blocks;
+    int64_t n_params;
+    void* base;           // the single cudaMalloc of the context
+    int64_t bytes;
+    ofrl::Workspace ws;
+    // measurement hooks: events[step][OFRL_PHASES + 1] while profiling
+    cudaEvent_t* prof_events;
+    int32_t prof_max;
+    int32_t prof_count;
+};
+
+namespace ofrl {
+
+// ---- counter-based RNG: SplitMix64 (Steele, Lea & Flood 2014) -----------
+__host__ __device__ __forceinline__ uint64_t sm64_mix(uint64_t z) {
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+// Output number (counter + 1) of SplitMix64 seeded with `seed`.
+__host__ __device__ __forceinline__ uint64_t sm64_at(uint64_t seed, uint64_t counter) {
+    return sm64_mix(seed + (counter + 1ull) * 0x9E3779B97F4A7C15ull);
+}
+// Lemire multiply-shift on the top 32 bits: uniform-ish in [0, n), n <= 2^32.
+__host__ __device__ __forceinline__ uint32_t below(uint64_t r, uint64_t n) {
+    return (uint32_t)(((r >> 32) * n) >> 32);
+}
+
+__device__ __forceinline__ float to_bf16_rn(float x) {
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ int warp_sum_int(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Clip scale of the pages' formula: (n > c && n > 0) ? c / n : 1.
+__device__ __forceinline__ float clip_scale(float n, float c) {
+    return (n > c && n > 0.0f) ? c / n : 1.0f;
+}
+
+inline int64_t n_params_of(int s, int h) {
+    return (int64_t)h * s + h + (int64_t)h * h + h + h + 1;
+}
+
+// Offsets of the six tensors inside the flat parameter / gradient buffer.
+struct Offsets {
+    int64_t w1, b1, w2, b2, w3, b3, total;
+};
+__host__ __device__ inline Offsets offsets_of(int s, int h) {
+    Offsets o;
+    o.w1 = 0;
+    o.b1 = o.w1 + (int64_t)h * s;
+    o.w2 = o.b1 + h;
+    o.b2 = o.w2 + (int64_t)h * h;
+    o.w3 = o.b2 + h;
+    o.b3 = o.w3 + h;
+    o.total = o.b3 + 1;
+    return o;
+}
+
+}  // namespace ofrl
+
+// Launch helpers (defined in the .cu files), called from api.cu.
+namespace ofrl {
+
+struct HerLaunch {
+    const float* states;
+    const float* next_states;
+    const int32_t* actions;
+    const float* rewards;
+    const float* dones;
+    const int32_t* episode_ends;
+    int32_t capacity;
+    int32_t num_episodes;
+    int32_t state_dim;
+    int32_t in_stride;
+    int32_t goal_dim;
+    int32_t batch;
+    int32_t first_her;
+    int32_t strategy;
+    float threshold;
+    uint64_t seed;
+    uint64_t step;
+    float* out_states;
+    float* out_next_states;
+    int32_t* out_actions;
+    float* out_rewards;
+    float* out_dones;
+    int32_t* out_src;
+    int32_t* out_donor;
+    int32_t out_stride;
+    int32_t copy_cols;      // columns copied per row (multiple of 4)
+    int32_t* status;
+};
+cudaError_t launch_her_relabel(const HerLaunch& a, cudaStream_t st);
+
+struct VnetLaunch {
+    const float* params[kMaxNets];
+    float tau[kMaxNets];
+    int n_nets;
+    int state_dim, hidden, num_actions, prec;
+    const float* states;
+    int32_t stride;
+    int32_t batch;
+    const float* q_taken;      // [B] (standalone) or null
+    const float* q;            // [B, A] (fused step) or null
+    const int32_t* actions;    // [B] with q
+    float beta;
+    float* v_out;              // [n_nets, B] or null
+    float* pi_out;             // [n_nets, B, A] or null
+    int32_t* argmax_out;       // [n_nets, B] or null
+    float* partials;           // [n_nets][n_tiles][P]
+    float* tile_loss;          // [n_nets][n_tiles]
+    int64_t net_partial_stride;  // floats between networks in partials
+    int32_t net_tile_stride;     // floats between networks in tile_loss
+    int32_t* status;
+};
+int vnet_tile_rows(int hidden);
+cudaError_t launch_vnet_fwd_bwd(const VnetLaunch& a, cudaStream_t st);
+
+struct ReduceLaunch {
+    int n_nets;
+    int64_t P;
+    int n_tiles;
+    const float* partials;       // [n_nets][n_tiles][P]; null: g0 is given in src[.][0]
+    int64_t net_partial_stride;
+    const float* tile_loss;      // [n_nets][n_tiles] or null
+    int32_t net_tile_stride;
+    float inv_batch;
+    float* g0_out[kMaxNets];     // where the reduced primary is written (if partials)
+    const float* src[kMaxNets][kMaxSrc];  // sources; src[n][0] ignored when partials != null
+    int n_src;
+    float budget[kMaxSrc];
+    float alpha[kMaxSrc];
+    float max_grad_norm;
+    float* gram_part;            // [n_nets][grid][kGramPairs]
+    float* scalars;              // [n_nets][kScalars]
+    unsigned int* counter;       // [n_nets]
+    float* norms_out;            // [n_nets][5] or null: n_0..n_3, combined
+    float* loss_out;             // [n_nets] or null
+};
+int reduce_grid(int64_t P);
+cudaError_t launch_reduce_gram(const ReduceLaunch& a, cudaStream_t st);
+
+struct AdamLaunch {
+    int n_nets;
+    int64_t n;
+    float* p[kMaxNets];
+    float* m[kMaxNets];
+    float* v[kMaxNets];
+    const float* src[kMaxNets][kMaxSrc];
+    int n_src;
+    const float* scalars;        // [n_nets][kScalars]: coefficients and the combined norm
+    const float* grad_norm;      // standalone: device scalar or null (then scalars[SC_COMBINED])
+    float lr[kMaxNets], bc1[kMaxNets], bc2[kMaxNets];
+    float beta1, beta2, eps, weight_decay, max_grad_norm;
+    int32_t* status;
+};
+cudaError_t launch_adam(const AdamLaunch& a, cudaStream_t st);
+
+struct CombineLaunch {
+    int64_t n;
+    const float* src[kMaxSrc];
+    int n_src;
+    const float* scalars;
+    float* out;
+    float* norms_out;            // [n_src + 1] or null
+};
+cudaError_t launch_combine(const CombineLaunch& a, cudaStream_t st);
+
+cudaError_t launch_expectile(const float* q_taken, const float* v, int batch, float tau,
+                             float* loss_out, float* dv_out, cudaStream_t st);
+cudaError_t launch_policy(const float* q, const float* v, int batch, int num_actions, float beta,
+                          float* pi_out, int32_t* argmax_out, int64_t net_stride_v,
+                          int n_nets, cudaStream_t st);
+
+}  // namespace ofrl

@@ -1,0 +1,280 @@
+// Gradient reduction, per-source norms, budgeted clipped SAXPY and Adam.
+//
+// Method: "Gradient Stability -- Multi-Task Gradient Isolation + Full
+// Spectral Norm", "Proper design" (each source clipped to its budget
+// fraction of max_grad_norm, then added; Adam's own clip at max_grad_norm)
+// and Task 1 Step 5 (norm of the source first, then the clipped SAXPY);
+// "DQN Backward-Path NaN Audit", Adam kernel findings (norm kept as a raw sum
+// of squares and square-rooted where used, the (n > c && n > 0) ? c / n : 1
+// clip, non-finite elements skipped, bias correction with t >= 1).
+//
+// The pages run one norm kernel and one SAXPY kernel per source and a
+// separate Adam launch, each a full pass over the parameters.  Here one pass
+// (reduce_gram) sums the per-tile gradient partials into the primary
+// gradient and accumulates the Gram matrix <g_j, g_k> of all sources; its
+// last block turns the Gram matrix into the source norms, the clip
+// coefficients and the norm of the combined gradient
+// ||sum_k c_k g_k||^2 = sum_jk c_j c_k <g_j, g_k>.  A second pass (adam)
+// forms the combined gradient element by element and applies Adam, so the
+// combined gradient is never stored.  Every reduction is in a fixed order.
+
+#include "common.cuh"
+
+namespace ofrl {
+namespace {
+
+constexpr int kRedThreads = 256;   // 32 elements x 8 tile lanes
+constexpr int kRedElems = 32;
+constexpr int kMaxGramBlocks = 2048;
+
+__global__ void __launch_bounds__(kRedThreads) reduce_gram_kernel(const ReduceLaunch a) {
+    __shared__ float sh[8][kRedElems + 1];
+    __shared__ unsigned int ticket;
+    __shared__ double dsh[kRedThreads / 32];
+    const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
+    const int net = blockIdx.y;
+    const int64_t P = a.P;
+    const int nsrc = a.n_src;
+
+    float gacc[kGramPairs];
+#pragma unroll
+    for (int p = 0; p < kGramPairs; ++p) gacc[p] = 0.0f;
+
+    for (int64_t base = (int64_t)blockIdx.x * kRedElems; base < P; base += (int64_t)gridDim.x * kRedElems) {
+        const int64_t i = base + tx;
+        float x[kMaxSrc] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (a.partials != nullptr) {
+            const float* pp = a.partials + (int64_t)net * a.net_partial_stride;
+            float s = 0.0f;
+            if (i < P)
+                for (int t = ty; t < a.n_tiles; t += 8) s += __ldcg(pp + (int64_t)t * P + i);
+            sh[ty][tx] = s;
+            __syncthreads();
+            if (ty == 0) {
+                float g = 0.0f;
+#pragma unroll
+                for (int y = 0; y < 8; ++y) g += sh[y][tx];
+                if (i < P) a.g0_out[net][i] = g;
+                x[0] = i < P ? g : 0.0f;
+            }
+            __syncthreads();
+        } else if (ty == 0 && i < P) {
+            x[0] = __ldg(a.src[net][0] + i);
+        }
+        if (ty == 0 && nsrc > 0) {
+            for (int k = 1; k < nsrc; ++k) x[k] = i < P ? __ldg(a.src[net][k] + i) : 0.0f;
+#pragma unroll
+            for (int j = 0; j < kMaxSrc; ++j)
+#pragma unroll
+                for (int k = j; k < kMaxSrc; ++k) gacc[gram_index(j, k)] = fmaf(x[j], x[k], gacc[gram_index(j, k)]);
+        }
+    }
+    float* gp = a.gram_part + ((int64_t)net * gridDim.x + blockIdx.x) * kGramPairs;
+    if (ty == 0) {
+#pragma unroll
+        for (int p = 0; p < kGramPairs; ++p) {
+            const float s = warp_sum(gacc[p]);
+            if (tx == 0) gp[p] = s;
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) ticket = atomicAdd(a.counter + net, 1u);
+    __syncthreads();
+    if (ticket != gridDim.x - 1) return;
+
+    // ---- last block: fixed-order totals, norms, clip coefficients ----
+    __threadfence();
+    double gram[kGramPairs];
+    const float* gall = a.gram_part + (int64_t)net * gridDim.x * kGramPairs;
+    for (int p = 0; p < kGramPairs; ++p) {
+        double s = 0.0;
+        for (int b = tid; b < (int)gridDim.x; b += kRedThreads) s += (double)__ldcg(gall + (int64_t)b * kGramPairs + p);
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (tx == 0) dsh[ty] = s;
+        __syncthreads();
+        double t = 0.0;
+        for (int y = 0; y < kRedThreads / 32; ++y) t += dsh[y];
+        gram[p] = t;
+        __syncthreads();
+    }
+    double loss = 0.0;
+    if (a.tile_loss != nullptr) {
+        const float* tl = a.tile_loss + (int64_t)net * a.net_tile_stride;
+        double s = 0.0;
+        for (int t = tid; t < a.n_tiles; t += kRedThreads) s += (double)__ldcg(tl + t);
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (tx == 0) dsh[ty] = s;
+        __syncthreads();
+        for (int y = 0; y < kRedThreads / 32; ++y) loss += dsh[y];
+    }
+    if (tid == 0) {
+        float* sc = a.scalars + (int64_t)net * kScalars;
+        double coef[kMaxSrc] = {0.0, 0.0, 0.0, 0.0};
+        for (int k = 0; k < kMaxSrc; ++k) {
+            const float nk = k < nsrc ? (float)sqrt(gram[gram_index(k, k)]) : 0.0f;
+            sc[SC_NORM0 + k] = nk;
+            if (k < nsrc) {
+                const float c = a.budget[k] * a.max_grad_norm;
+                coef[k] = (double)a.alpha[k] * (double)clip_scale(nk, c);
+            }
+            sc[SC_COEF0 + k] = (float)coef[k];
+        }
+        // IEEE arithmetic throughout: a NaN source norm gives coefficient 1
+        // and a NaN total; an infinite one gives coefficient 0 and 0 * inf =
+        // NaN, as the element-wise sum of the clipped sources would.
+        double c2 = 0.0;
+        for (int j = 0; j < nsrc; ++j)
+            for (int k = 0; k < nsrc; ++k) {
+                const int lo = j < k ? j : k, hi = j < k ? k : j;
+                c2 += coef[j] * coef[k] * gram[gram_index(lo, hi)];
+            }
+        const float cn = (float)(c2 < 0.0 ? 0.0 : sqrt(c2));
+        sc[SC_COMBINED] = cn;
+        const float lmean = (float)(loss * (double)a.inv_batch);
+        sc[SC_LOSS] = lmean;
+        if (a.norms_out != nullptr) {
+            for (int k = 0; k < kMaxSrc; ++k) a.norms_out[net * 5 + k] = sc[SC_NORM0 + k];
+            a.norms_out[net * 5 + 4] = cn;
+        }
+        if (a.loss_out != nullptr) a.loss_out[net] = lmean;
+        a.counter[net] = 0u;
+    }
+}
+
+__global__ void __launch_bounds__(256) adam_kernel(const AdamLaunch a) {
+    const int net = blockIdx.y;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    float coef[kMaxSrc] = {1.0f, 0.0f, 0.0f, 0.0f};
+    float gn;
+    if (a.scalars != nullptr) {
+        const float* sc = a.scalars + (int64_t)net * kScalars;
+#pragma unroll
+        for (int k = 0; k < kMaxSrc; ++k) coef[k] = sc[SC_COEF0 + k];
+        gn = a.grad_norm != nullptr ? __ldg(a.grad_norm) : sc[SC_COMBINED];
+    } else {
+        gn = __ldg(a.grad_norm);
+    }
+    const float s = clip_scale(gn, a.max_grad_norm);
+    bool bad = false;
+    if (i < a.n) {
+        float gsum = 0.0f;
+        for (int k = 0; k < a.n_src; ++k) gsum = fmaf(coef[k], __ldg(a.src[net][k] + i), gsum);
+        const float g = s * gsum;
+        if (!isfinite(g)) {
+            bad = true;
+        } else {
+            float m = a.m[net][i], v = a.v[net][i], p = a.p[net][i];
+            m = a.beta1 * m + (1.0f - a.beta1) * g;
+            v = a.beta2 * v + (1.0f - a.beta2) * g * g;
+            const float mhat = m / a.bc1[net];
+            const float vhat = v / a.bc2[net];
+            p = p - a.lr[net] * (mhat / (sqrtf(vhat) + a.eps) + a.weight_decay * p);
+            a.m[net][i] = m;
+            a.v[net][i] = v;
+            a.p[net][i] = p;
+        }
+    }
+    const unsigned ballot = __ballot_sync(0xffffffffu, bad);
+    if ((threadIdx.x & 31) == 0 && ballot != 0u) atomicAdd(a.status + OFRL_STAT_NONFINITE_GRAD, __popc(ballot));
+}
+
+__global__ void __launch_bounds__(256) combine_kernel(const CombineLaunch a) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < a.n) {
+        float g = 0.0f;
+        for (int k = 0; k < a.n_src; ++k) g = fmaf(a.scalars[SC_COEF0 + k], __ldg(a.src[k] + i), g);
+        a.out[i] = g;
+    }
+    if (blockIdx.x == 0 && a.norms_out != nullptr) {
+        if ((int)threadIdx.x < a.n_src) a.norms_out[threadIdx.x] = a.scalars[SC_NORM0 + threadIdx.x];
+        if ((int)threadIdx.x == a.n_src) a.norms_out[threadIdx.x] = a.scalars[SC_COMBINED];
+    }
+}
+
+constexpr int kLossThreads = 1024;
+
+__global__ void __launch_bounds__(kLossThreads) expectile_kernel(const float* __restrict__ q,
+                                                                 const float* __restrict__ v, int B,
+                                                                 float tau, float* loss_out,
+                                                                 float* dv_out) {
+    __shared__ float sh[kLossThreads / 32];
+    float s = 0.0f;
+    for (int i = threadIdx.x; i < B; i += kLossThreads) {
+        const float d = __ldg(q + i) - __ldg(v + i);
+        const float w = d >= 0.0f ? tau : 1.0f - tau;
+        s += w * d * d;
+        if (dv_out != nullptr) dv_out[i] = (-2.0f * w * d) / (float)B;
+    }
+    s = warp_sum(s);
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.0f;
+        for (int y = 0; y < kLossThreads / 32; ++y) t += sh[y];
+        *loss_out = t / (float)B;
+    }
+}
+
+__global__ void __launch_bounds__(256) policy_kernel(const float* __restrict__ q, const float* __restrict__ v,
+                                                     int B, int NA, float beta, float* pi_out,
+                                                     int32_t* argmax_out) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const float vb = __ldg(v + b);
+    const float* qr = q + (int64_t)b * NA;
+    float z[kMaxActions];
+    float zmax = -INFINITY, amax = -INFINITY;
+    int best = 0;
+    for (int k = 0; k < NA; ++k) {
+        const float adv = fminf(fmaxf(__ldg(qr + k) - vb, -10.0f), 10.0f);
+        if (adv > amax) { amax = adv; best = k; }
+        z[k] = beta * adv;
+        zmax = fmaxf(zmax, z[k]);
+    }
+    float sum = 0.0f;
+    for (int k = 0; k < NA; ++k) { z[k] = expf(z[k] - zmax); sum += z[k]; }
+    float* po = pi_out + (int64_t)b * NA;
+    for (int k = 0; k < NA; ++k) po[k] = z[k] / sum;
+    if (argmax_out != nullptr) argmax_out[b] = best;
+}
+
+}  // namespace
+
+int reduce_grid(int64_t P) {
+    const int64_t g = (P + kRedElems - 1) / kRedElems;
+    return (int)(g < kMaxGramBlocks ? (g < 1 ? 1 : g) : kMaxGramBlocks);
+}
+
+cudaError_t launch_reduce_gram(const ReduceLaunch& a, cudaStream_t st) {
+    const dim3 grid(reduce_grid(a.P), a.n_nets);
+    reduce_gram_kernel<<<grid, kRedThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_adam(const AdamLaunch& a, cudaStream_t st) {
+    if (a.n <= 0) return cudaSuccess;
+    const dim3 grid((unsigned)((a.n + 255) / 256), a.n_nets);
+    adam_kernel<<<grid, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const CombineLaunch& a, cudaStream_t st) {
+    const unsigned blocks = (unsigned)((a.n + 255) / 256);
+    combine_kernel<<<blocks < 1 ? 1 : blocks, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_expectile(const float* q_taken, const float* v, int batch, float tau,
+                             float* loss_out, float* dv_out, cudaStream_t st) {
+    expectile_kernel<<<1, kLossThreads, 0, st>>>(q_taken, v, batch, tau, loss_out, dv_out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_policy(const float* q, const float* v, int batch, int num_actions, float beta,
+                          float* pi_out, int32_t* argmax_out, int64_t, int, cudaStream_t st) {
+    policy_kernel<<<(batch + 255) / 256, 256, 0, st>>>(q, v, batch, num_actions, beta, pi_out, argmax_out);
+    return cudaGetLastError();
+}
+
+}  // namespace ofrl

@@ -102,6 +102,29 @@ def backward(flat, act: dict, dv, state_dim: int, hidden: int):
     return flatten(dw1, db1, dw2, db2, dw3, db3)
 
 
+def backward_abs(flat, act: dict, dv, state_dim: int, hidden: int):
+    """Per gradient element, the sum of |terms| of its expanded sum.
+
+    The backward of `backward` with every factor replaced by its absolute
+    value.  |grad_i| <= backward_abs_i, with equality when every term of
+    element i has one sign.  Rounding error of any summation order of
+    element i is bounded by a multiple of backward_abs_i, so elements with
+    |grad_i| far below it have a sign that finite precision does not fix.
+    """
+    w1, b1, w2, b2, w3, b3 = unflatten(flat, state_dim, hidden)
+    adv = np.abs(np.asarray(dv, dtype=np.float64))
+    x, z1, h1, z2, h2 = act["x"], act["z1"], act["h1"], act["z2"], act["h2"]
+    adz2 = adv[:, None] * np.abs(w3) * (z2 > 0.0)
+    adw3 = adv[None, :] @ np.abs(h2)
+    adb3 = np.array([adv.sum()])
+    adw2 = adz2.T @ np.abs(h1)
+    adb2 = adz2.sum(axis=0)
+    adz1 = (adz2 @ np.abs(w2)) * (z1 > 0.0)
+    adw1 = adz1.T @ np.abs(x)
+    adb1 = adz1.sum(axis=0)
+    return flatten(adw1, adb1, adw2, adb2, adw3, adb3)
+
+
 def value_fwd_bwd(flat, states, qt, tau: float, state_dim: int, hidden: int):
     """V forward + expectile loss + backward, as one call (fp64)."""
     v, act = forward(flat, states, state_dim, hidden)

@@ -81,17 +81,24 @@ def train_step(cfg: StepConfig, replay: dict, step: int, q, nets, aux=None):
     batch = her.relabel(replay, src, donor, cfg.goal_dim, cfg.goal_threshold)
     qt = iql.q_taken(q, batch["actions"])
     out = dict(batch=batch, v=[], loss=[], pi=[], argmax=[], grad=[], combined=[],
-               norms=[], skipped=[])
+               combined_abs=[], norms=[], skipped=[])
     for k, net in enumerate(nets):
         v, act = iql.forward(net.params, batch["states"], cfg.state_dim, cfg.hidden)
         loss, dv = iql.expectile_loss(qt, v, net.tau)
         pi, am = iql.policy(q, v, cfg.beta)
         g0 = iql.backward(net.params, act, dv, cfg.state_dim, cfg.hidden)
+        g0_abs = iql.backward_abs(net.params, act, dv, cfg.state_dim, cfg.hidden)
         sources = [g0]
         if aux is not None and aux[k] is not None:
             sources += [np.asarray(a, dtype=np.float64) for a in aux[k]]
         n = len(sources)
         g, norms = optim.budgeted_combine(sources, cfg.budget[:n], cfg.alpha[:n], cfg.max_grad_norm)
+        # magnitude scale of each combined element: |coef_0| * sum|terms of g0|
+        # plus |coef_k g_k| for the (exact) auxiliary inputs
+        g_abs = np.zeros_like(g)
+        for k, src in enumerate(sources):
+            c = abs(float(cfg.alpha[k]) * optim.clip_scale(norms[k], float(cfg.budget[k]) * cfg.max_grad_norm))
+            g_abs += c * (g0_abs if k == 0 else np.abs(src))
         net.t += 1
         net.params, net.m, net.v, skipped = optim.adam(
             net.params, g, net.m, net.v, net.t, cfg.lr, cfg.beta1, cfg.beta2, cfg.eps,
@@ -105,6 +112,7 @@ def train_step(cfg: StepConfig, replay: dict, step: int, q, nets, aux=None):
         out["argmax"].append(am)
         out["grad"].append(g0)
         out["combined"].append(g)
+        out["combined_abs"].append(g_abs)
         out["norms"].append(full)
         out["skipped"].append(skipped)
     return out

@@ -1,0 +1,156 @@
+"""Shared helpers of the GPU parity tests: inputs, oracle runs, comparisons.
+
+Tolerances (fp32 GEMM workloads): 1e-4 relative / 1e-5 absolute on V, the
+loss, the policy, gradients and post-Adam weights; bit-exact on HER indices,
+relabelled goals, rewards and the policy argmax.  bf16-GEMM workloads: 2e-2
+relative on the loss and the weights.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import her as oher
+from oracle import step as ostep
+
+RTOL, ATOL = 1e-4, 1e-5
+BF16_RTOL = 2e-2
+
+_REPLAYS = {}
+
+
+def f32(x):
+    """The fp32 value the library receives for a hyper-parameter."""
+    return float(np.float32(x))
+
+
+def need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import offline_rl_step_gb300 as ofrl  # noqa: F401
+    from offline_rl_step_gb300 import _abi
+    _abi.load()   # raises if the library is not built: no silent fallback
+
+
+def replay_np(w):
+    key = (w.seed, w.capacity, w.state_dim, w.goal_dim, w.ep_len, w.num_actions, w.anchor_frac)
+    if key not in _REPLAYS:
+        if len(_REPLAYS) >= 3:
+            _REPLAYS.clear()
+        _REPLAYS[key] = synth.make_replay(w)
+    return _REPLAYS[key]
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def replay_dev(w, rep):
+    import offline_rl_step_gb300 as ofrl
+    return ofrl.Replay(dev(rep["states"]), dev(rep["next_states"]), dev(rep["actions"]), dev(rep["rewards"]),
+                       dev(rep["dones"]), w.state_dim, w.goal_dim, dev(rep["episode_ends"]))
+
+
+def oracle_cfg(w):
+    """Oracle step config with the fp32-rounded constants the library gets."""
+    c = ostep.config_from_workload(w)
+    return dataclasses.replace(
+        c, goal_threshold=f32(w.goal_threshold), beta=f32(w.beta), lr=f32(w.lr), beta1=f32(w.beta1),
+        beta2=f32(w.beta2), eps=f32(w.eps), weight_decay=f32(w.weight_decay),
+        max_grad_norm=f32(w.max_grad_norm), budget=tuple(f32(b) for b in w.budget))
+
+
+def report(gpu, ref, rtol, atol):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err = np.abs(gpu - ref)
+    bad = ~(err <= atol + rtol * np.abs(ref))
+    rel = err / np.maximum(np.abs(ref), 1e-30)
+    return bad, float(err.max(initial=0.0)), float(rel.max(initial=0.0))
+
+
+def assert_close(gpu, ref, rtol=RTOL, atol=ATOL, what="value", allow=None):
+    """Element-wise |gpu - ref| <= atol + rtol |ref|; `allow` masks elements that may differ."""
+    bad, emax, rmax = report(gpu, ref, rtol, atol)
+    if allow is not None:
+        bad &= ~np.asarray(allow, dtype=bool)
+    n = int(bad.sum())
+    assert n == 0, f"{what}: {n} of {bad.size} elements out of tolerance (max abs {emax:.3g}, max rel {rmax:.3g})"
+
+
+def assert_bits(gpu, ref, what="value"):
+    g = np.ascontiguousarray(gpu)
+    r = np.ascontiguousarray(ref)
+    assert g.shape == r.shape, f"{what}: shape {g.shape} vs {r.shape}"
+    if g.dtype.kind == "f":
+        g, r = g.view(np.uint32 if g.itemsize == 4 else np.uint64), r.astype(g.dtype).view(
+            np.uint32 if g.itemsize == 4 else np.uint64)
+    n = int((g != r).sum())
+    assert n == 0, f"{what}: {n} of {g.size} elements differ"
+
+
+def argmax_ok(gpu_am, q, v_ref, beta, margin=1e-3):
+    """argmax equal to the oracle's, except on rows whose clamped advantages
+    tie within `margin` (only possible through the +-10 clamp), where any of
+    the tied maxima is accepted."""
+    adv = np.clip(np.asarray(q, np.float64) - np.asarray(v_ref, np.float64)[:, None], -10.0, 10.0)
+    top = adv.max(axis=1, keepdims=True)
+    near = adv >= top - margin
+    exact = near.sum(axis=1) == 1
+    want = np.argmax(adv, axis=1)
+    rows = np.arange(adv.shape[0])
+    assert (gpu_am[exact] == want[exact]).all(), "argmax differs on unambiguous rows"
+    assert near[rows, gpu_am].all(), "argmax is not among the maxima on ambiguous rows"
+    return int((~exact).sum())
+
+
+class GpuStep:
+    """The fused train step of one workload on the GPU, through the C ABI."""
+
+    def __init__(self, w):
+        import offline_rl_step_gb300 as ofrl
+        self.ofrl = ofrl
+        self.w = w
+        self.rep = replay_np(w)
+        self.replay = replay_dev(w, self.rep)
+        self.her = ofrl.HerConfig(w.batch, w.her_count, w.strategy, w.goal_threshold, w.seed)
+        self.ctx = ofrl.Context(w.state_dim, w.hidden, w.num_actions, w.prec, max_batch=w.batch,
+                                max_nets=w.n_nets)
+        self.params0 = [synth.make_params(w, k) for k in range(w.n_nets)]
+        self.nets = [ofrl.VNet.from_params(torch.from_numpy(p), w.taus[k]) for k, p in enumerate(self.params0)]
+        self.opt = ofrl.Opt(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
+                            max_grad_norm=w.max_grad_norm, beta=w.beta, budget=w.budget)
+        self.batch = ofrl.Batch.empty(w.batch, w.state_stride)
+        n, b, a, p = w.n_nets, w.batch, w.num_actions, w.n_params
+        self.v = torch.empty(n, b, device="cuda")
+        self.pi = torch.empty(n, b, a, device="cuda")
+        self.am = torch.empty(n, b, dtype=torch.int32, device="cuda")
+        self.loss = torch.empty(n, device="cuda")
+        self.norms = torch.empty(n, 5, device="cuda")
+        self.grad = torch.empty(n, p, device="cuda")
+
+    def step(self, k, q, aux=None):
+        aux_dev = None if aux is None else [[dev(a) for a in per] for per in aux]
+        self.ofrl.train_step(self.ctx, self.replay, self.her, k, self.batch, dev(q), self.nets, self.opt,
+                             aux=aux_dev, v_out=self.v, pi_out=self.pi, argmax_out=self.am,
+                             loss_out=self.loss, norms_out=self.norms, grad_out=self.grad)
+        torch.cuda.synchronize()
+        cpu = lambda t: t.cpu().numpy()
+        return dict(batch={k2: cpu(getattr(self.batch, k2)) for k2 in
+                           ("states", "next_states", "actions", "rewards", "dones", "src_idx", "donor_idx")},
+                    v=cpu(self.v), pi=cpu(self.pi), argmax=cpu(self.am), loss=cpu(self.loss),
+                    norms=cpu(self.norms), grad=cpu(self.grad),
+                    params=[cpu(n.params) for n in self.nets])
+
+    def close(self):
+        self.ctx.close()
+
+
+def oracle_nets(w):
+    return [ostep.NetState.fresh(synth.make_params(w, k), f32(w.taus[k])) for k in range(w.n_nets)]
+
+
+def her_rows(w):
+    return oher.her_count(w.batch, w.her_ratio)

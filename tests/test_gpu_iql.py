@@ -1,0 +1,89 @@
+"""GPU parity: V forward/backward, expectile loss and policy against the oracle."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from _gpu import (ATOL, BF16_RTOL, RTOL, argmax_ok, assert_close, dev, f32, need_gpu)
+from oracle import iql
+
+pytestmark = pytest.mark.gpu
+
+
+def _fwd_bwd(s, h, b, tau, prec="fp32", seed=0, stride=None):
+    import offline_rl_step_gb300 as ofrl
+    need_gpu()
+    w = dataclasses.replace(synth.PROD, state_dim=s, hidden=h, net_seeds=(seed + 7,))
+    params = synth.make_params(w)
+    rng = np.random.default_rng(seed)
+    st = stride or ((s + 7) & ~7)
+    x = np.zeros((b, st), dtype=np.float32)
+    x[:, :s] = rng.standard_normal((b, s))
+    qt = (rng.standard_normal(b) * 2).astype(np.float32)
+    ctx = ofrl.Context(s, h, 5, prec, max_batch=b)
+    v = torch.empty(b, device="cuda")
+    loss = torch.empty(1, device="cuda")
+    grad = torch.empty(w.n_params, device="cuda")
+    ofrl.iql_value_fwd_bwd(ctx, dev(params), dev(x), dev(qt), tau, v, loss, grad)
+    torch.cuda.synchronize()
+    rv, rloss, rgrad = iql.value_fwd_bwd(params, x, qt, f32(tau), s, h)
+    ctx.close()
+    return (v.cpu().numpy(), float(loss.cpu()[0]), grad.cpu().numpy()), (rv, rloss, rgrad)
+
+
+@pytest.mark.parametrize("s,h,b", [(48, 64, 256), (50, 128, 16384), (50, 128, 300), (50, 256, 200),
+                                   (50, 256, 16384), (7, 64, 1), (64, 128, 129)])
+def test_value_fwd_bwd_fp32(s, h, b):
+    (v, loss, g), (rv, rl, rg) = _fwd_bwd(s, h, b, 0.7, seed=s + h + b)
+    assert_close(v, rv, what="V")
+    assert_close(loss, rl, what="loss")
+    assert_close(g, rg, what="gradient")
+
+
+@pytest.mark.parametrize("h,b", [(128, 16384), (256, 333)])
+def test_value_fwd_bwd_bf16(h, b):
+    (v, loss, g), (rv, rl, rg) = _fwd_bwd(50, h, b, 0.9, prec="bf16", seed=h + b)
+    assert abs(loss - rl) <= BF16_RTOL * abs(rl)
+    assert_close(v, rv, rtol=BF16_RTOL, atol=BF16_RTOL * np.abs(rv).mean(), what="V (bf16)")
+    # gradient: bf16 operands, compared in norm
+    assert np.linalg.norm(g - rg) <= BF16_RTOL * np.linalg.norm(rg)
+
+
+@pytest.mark.parametrize("b", [1, 1000, 65536])
+@pytest.mark.parametrize("tau", [0.5, 0.7, 0.9])
+def test_expectile_loss(b, tau):
+    import offline_rl_step_gb300 as ofrl
+    need_gpu()
+    rng = np.random.default_rng(b)
+    q = (rng.standard_normal(b) * 2).astype(np.float32)
+    v = rng.standard_normal(b).astype(np.float32)
+    ctx = ofrl.Context(8, 64, 4, max_batch=1)
+    loss = torch.empty(1, device="cuda")
+    dv = torch.empty(b, device="cuda")
+    ofrl.expectile_loss(ctx, dev(q), dev(v), tau, loss, dv)
+    torch.cuda.synchronize()
+    rl, rdv = iql.expectile_loss(q, v, f32(tau))
+    assert_close(float(loss.cpu()[0]), rl, what="loss")
+    assert_close(dv.cpu().numpy(), rdv, what="dL/dV")
+    ctx.close()
+
+
+@pytest.mark.parametrize("b,a", [(1, 1), (777, 5), (16384, 9), (65536, 16)])
+def test_policy(b, a):
+    import offline_rl_step_gb300 as ofrl
+    need_gpu()
+    rng = np.random.default_rng(a * 100 + b)
+    q = (rng.standard_normal((b, a)) * 6).astype(np.float32)   # many advantages hit the clamp
+    v = (rng.standard_normal(b) * 3).astype(np.float32)
+    ctx = ofrl.Context(8, 64, 4, max_batch=1)
+    pi = torch.empty(b, a, device="cuda")
+    am = torch.empty(b, dtype=torch.int32, device="cuda")
+    ofrl.adv_weighted_policy(ctx, dev(q), dev(v), 3.0, pi, am)
+    torch.cuda.synchronize()
+    rpi, _ = iql.policy(q, v, f32(3.0))
+    assert_close(pi.cpu().numpy(), rpi, what="pi")
+    np.testing.assert_allclose(pi.cpu().numpy().sum(axis=1), 1.0, atol=1e-5)
+    argmax_ok(am.cpu().numpy(), q, v, 3.0)
+    ctx.close()

@@ -184,3 +184,24 @@ def test_policy_degenerate_cases():
     assert am[0] == 0 and am[1] == 0 and am[2] == 2
     pi0, _ = iql.policy(q, v, 0.0)
     np.testing.assert_allclose(pi0, 1 / 3, rtol=1e-15)
+
+
+def test_backward_abs_bounds_and_equality():
+    rng = np.random.default_rng(9)
+    s, h, b = 7, 6, 20
+    flat = _net(rng, s, h)
+    x = rng.standard_normal((b, s))
+    qt = rng.standard_normal(b) * 2
+    v, act = iql.forward(flat, x, s, h)
+    _, dv = iql.expectile_loss(qt, v, 0.7)
+    g = iql.backward(flat, act, dv, s, h)
+    ga = iql.backward_abs(flat, act, dv, s, h)
+    assert (np.abs(g) <= ga * (1 + 1e-12) + 1e-300).all()
+    # one-signed terms everywhere: positive inputs, weights and dv -> equality
+    flat = np.abs(flat) + 0.01
+    x = np.abs(x) + 0.01
+    v, act = iql.forward(flat, x, s, h)
+    dv = np.abs(rng.standard_normal(b)) + 0.01
+    g = iql.backward(flat, act, dv, s, h)
+    ga = iql.backward_abs(flat, act, dv, s, h)
+    np.testing.assert_allclose(np.abs(g), ga, rtol=1e-12)
