@@ -48,7 +48,7 @@ Layout layout_of(const ofrl_vshape* s, int32_t max_batch, int32_t max_nets) {
     L.max_tiles = (int32_t)((max_batch + tm - 1) / tm);
     int64_t o = 0;
     auto take = [&](int64_t bytes) { const int64_t at = o; o = round_up(o + bytes, 256); return at; };
-    L.off_partials = take((int64_t)max_nets * L.max_tiles * L.P * 4);
+    L.off_partials = take((int64_t)max_nets * L.max_tiles * part_stride_of(L.P) * 4);
     L.off_tile_loss = take((int64_t)max_nets * L.max_tiles * 4);
     L.off_g0 = take((int64_t)max_nets * L.P * 4);
     L.off_gram = take((int64_t)max_nets * kMaxGramBlocksWs * kGramPairs * 4);
@@ -74,6 +74,7 @@ ofrl_status check_replay(const ofrl_replay* r, const ofrl_her_cfg* h) {
     if (r->capacity < 1 || r->capacity > INT32_MAX) return OFRL_EINVAL;
     if (r->state_dim < 1 || r->state_stride < r->state_dim || (r->state_stride & 3)) return OFRL_EINVAL;
     if (r->goal_dim < 1 || r->goal_dim > r->state_dim) return OFRL_EINVAL;
+    if (r->state_dim > kMaxStateDim) return OFRL_EUNSUPPORTED;
     if (!aligned16(r->states) || !aligned16(r->next_states)) return OFRL_EINVAL;
     if (h->batch < 0 || h->her_count < 0 || h->her_count > h->batch) return OFRL_EINVAL;
     if (h->strategy != OFRL_HER_FINAL && h->strategy != OFRL_HER_FUTURE && h->strategy != OFRL_HER_RANDOM)
@@ -132,6 +133,9 @@ HerLaunch her_args(ofrl_ctx* ctx, const ofrl_replay* r, const ofrl_her_cfg* h, u
     a.out_donor = out->donor_idx;
     a.out_stride = out->stride;
     a.copy_cols = (r->state_dim + 3) & ~3;
+    int rounds = 0;
+    for (int64_t len = r->num_episodes; len > 16; len = (len + 15) / 16) ++rounds;
+    a.search_rounds = rounds;
     a.status = ctx->ws.status;
     return a;
 }
@@ -283,7 +287,8 @@ ofrl_status ofrl_iql_value_fwd_bwd(ofrl_ctx* ctx, const float* params, const flo
     v.v_out = v_out;
     v.partials = ctx->ws.partials;
     v.tile_loss = ctx->ws.tile_loss;
-    v.net_partial_stride = (int64_t)ctx->max_tiles * ctx->n_params;
+    v.part_stride = part_stride_of(ctx->n_params);
+    v.net_partial_stride = (int64_t)ctx->max_tiles * v.part_stride;
     v.net_tile_stride = ctx->max_tiles;
     v.status = ctx->ws.status;
     cudaError_t e = launch_vnet_fwd_bwd(v, st);
@@ -295,6 +300,7 @@ ofrl_status ofrl_iql_value_fwd_bwd(ofrl_ctx* ctx, const float* params, const flo
     r.P = ctx->n_params;
     r.n_tiles = n_tiles;
     r.partials = ctx->ws.partials;
+    r.part_stride = v.part_stride;
     r.net_partial_stride = v.net_partial_stride;
     r.tile_loss = ctx->ws.tile_loss;
     r.net_tile_stride = ctx->max_tiles;
@@ -475,7 +481,8 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
     v.argmax_out = pi_out != nullptr ? argmax_out : nullptr;
     v.partials = ctx->ws.partials;
     v.tile_loss = ctx->ws.tile_loss;
-    v.net_partial_stride = (int64_t)ctx->max_tiles * P;
+    v.part_stride = part_stride_of(P);
+    v.net_partial_stride = (int64_t)ctx->max_tiles * v.part_stride;
     v.net_tile_stride = ctx->max_tiles;
     v.status = ctx->ws.status;
     e = launch_vnet_fwd_bwd(v, st);
@@ -490,6 +497,7 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
     r.P = P;
     r.n_tiles = (B + tm - 1) / tm;
     r.partials = ctx->ws.partials;
+    r.part_stride = v.part_stride;
     r.net_partial_stride = v.net_partial_stride;
     r.tile_loss = ctx->ws.tile_loss;
     r.net_tile_stride = ctx->max_tiles;

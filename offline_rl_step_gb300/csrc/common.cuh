@@ -100,6 +100,9 @@ __device__ __forceinline__ float clip_scale(float n, float c) {
 inline int64_t n_params_of(int s, int h) {
     return (int64_t)h * s + h + (int64_t)h * h + h + h + 1;
 }
+// Per-tile stride of the gradient partials: P rounded up to 32 floats, so
+// every tile's slice starts on a 128-byte boundary.
+inline int64_t part_stride_of(int64_t p) { return (p + 31) / 32 * 32; }
 
 // Offsets of the six tensors inside the flat parameter / gradient buffer.
 struct Offsets {
@@ -148,7 +151,8 @@ struct HerLaunch {
     int32_t* out_src;
     int32_t* out_donor;
     int32_t out_stride;
-    int32_t copy_cols;      // columns copied per row (multiple of 4)
+    int32_t copy_cols;      // columns copied per row (multiple of 4, <= 64)
+    int32_t search_rounds;  // 16-ary search rounds that shrink num_episodes to <= 16
     int32_t* status;
 };
 cudaError_t launch_her_relabel(const HerLaunch& a, cudaStream_t st);
@@ -168,8 +172,9 @@ struct VnetLaunch {
     float* v_out;              // [n_nets, B] or null
     float* pi_out;             // [n_nets, B, A] or null
     int32_t* argmax_out;       // [n_nets, B] or null
-    float* partials;           // [n_nets][n_tiles][P]
+    float* partials;           // [n_nets][n_tiles][part_stride]
     float* tile_loss;          // [n_nets][n_tiles]
+    int64_t part_stride;       // floats between tiles in partials (P rounded up to 32)
     int64_t net_partial_stride;  // floats between networks in partials
     int32_t net_tile_stride;     // floats between networks in tile_loss
     int32_t* status;
@@ -181,7 +186,8 @@ struct ReduceLaunch {
     int n_nets;
     int64_t P;
     int n_tiles;
-    const float* partials;       // [n_nets][n_tiles][P]; null: g0 is given in src[.][0]
+    const float* partials;       // [n_nets][n_tiles][part_stride]; null: g0 is given in src[.][0]
+    int64_t part_stride;
     int64_t net_partial_stride;
     const float* tile_loss;      // [n_nets][n_tiles] or null
     int32_t net_tile_stride;

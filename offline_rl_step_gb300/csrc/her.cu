@@ -23,92 +23,125 @@ namespace {
 constexpr int kLanesPerRow = 16;
 constexpr int kRelabelThreads = 256;
 constexpr int kRowsPerBlock = kRelabelThreads / kLanesPerRow;
+constexpr unsigned kFull = 0xffffffffu;
 
-// First entry of `ends` above i (binary search); n if there is none.
-__device__ __forceinline__ int upper_bound_i32(const int32_t* __restrict__ ends, int n, int i) {
-    int lo = 0, hi = n;
-    while (lo < hi) {
-        int mid = (lo + hi) >> 1;
-        if (__ldg(ends + mid) > i) hi = mid; else lo = mid + 1;
+// First index k with ends[k] > i, found by the 16 lanes of a half-warp
+// together: each round probes the last entry of 16 equal segments of the
+// window and keeps the first segment that ends above i (a 16-ary search, so
+// log16(n) rounds instead of log2(n) dependent loads).  `rounds` is the same
+// for both half-warps, so every ballot is executed by the whole warp.
+// Returns n when no entry is above i.
+__device__ __forceinline__ int episode_search(const int32_t* __restrict__ ends, int n, int rounds, int i,
+                                              int sub) {
+    const int shift = threadIdx.x & 16;
+    int lo = 0, len = n;
+    for (int r = 0; r < rounds; ++r) {
+        const int step = (len + kLanesPerRow - 1) / kLanesPerRow;
+        const int p = lo + (sub + 1) * step - 1;
+        const bool gt = len > kLanesPerRow && p < lo + len ? __ldg(ends + p) > i : true;
+        const unsigned m = (__ballot_sync(kFull, gt) >> shift) & 0xFFFFu;
+        if (len > kLanesPerRow) {
+            const int f = __ffs(m) - 1;    // m != 0: the window's last segment always answers true
+            const int nlo = lo + f * step;
+            len = min(step, lo + len - nlo);
+            lo = nlo;
+        }
     }
-    return lo;
+    const bool gt = sub < len ? __ldg(ends + lo + sub) > i : true;
+    const unsigned m = (__ballot_sync(kFull, gt) >> shift) & 0xFFFFu;
+    const int f = __ffs(m) - 1;
+    return f < len ? lo + f : lo + len;
 }
 
 __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerLaunch a) {
-    const int lane = threadIdx.x & (kLanesPerRow - 1);
-    const int row = blockIdx.x * kRowsPerBlock + threadIdx.x / kLanesPerRow;
-    const bool live = row < a.batch;
+    const int sub = threadIdx.x & (kLanesPerRow - 1);
+    const int row_raw = blockIdx.x * kRowsPerBlock + threadIdx.x / kLanesPerRow;
+    const bool live = row_raw < a.batch;
+    const int row = live ? row_raw : a.batch - 1;   // dead half-warps shadow the last row, write nothing
+    const uint64_t ctr = (a.step << 32) | ((uint64_t)row << 1);
 
-    int src = 0, donor = -1, bad = 0;
-    if (lane == 0 && live) {
-        const uint64_t ctr = (a.step << 32) | ((uint64_t)row << 1);
-        src = (int)below(sm64_at(a.seed, ctr), (uint64_t)a.capacity);
-        if (row >= a.first_her) {
-            if (a.strategy == OFRL_HER_RANDOM) {
-                donor = (int)below(sm64_at(a.seed, ctr | 1ull), (uint64_t)a.capacity);
+    // 1. source index, then the source rows' loads go out at once
+    int src = 0;
+    if (sub == 0) src = (int)below(sm64_at(a.seed, ctr), (uint64_t)a.capacity);
+    src = __shfl_sync(kFull, src, 0, kLanesPerRow);
+    const int chunks = a.copy_cols >> 2;   // <= 16 (state_dim <= 64)
+    const bool has = sub < chunks;
+    float4 sv = make_float4(0.f, 0.f, 0.f, 0.f), nv = sv;
+    if (has) {
+        sv = __ldg(reinterpret_cast<const float4*>(a.states + (int64_t)src * a.in_stride) + sub);
+        nv = __ldg(reinterpret_cast<const float4*>(a.next_states + (int64_t)src * a.in_stride) + sub);
+    }
+    int act = 0;
+    float done = 0.0f, rew = 0.0f;
+    if (sub == 0) {
+        act = __ldg(a.actions + src);
+        done = __ldg(a.dones + src);
+        rew = __ldg(a.rewards + src);
+    }
+
+    // 2. donor (HER rows), overlapping the row loads
+    const bool her = row >= a.first_her;
+    int donor = -1, bad = 0;
+    if (a.strategy == OFRL_HER_RANDOM) {
+        if (sub == 0 && her) donor = (int)below(sm64_at(a.seed, ctr | 1ull), (uint64_t)a.capacity);
+    } else if (a.first_her < a.batch) {
+        const int k = episode_search(a.episode_ends, a.num_episodes, a.search_rounds, src, sub);
+        if (sub == 0 && her) {
+            int end = k < a.num_episodes ? __ldg(a.episode_ends + k) : a.capacity;
+            if (k >= a.num_episodes || end > a.capacity || end <= src) {
+                end = a.capacity;   // malformed boundaries: flagged; the donor stays inside the buffer
+                bad = 1;
+            }
+            if (a.strategy == OFRL_HER_FINAL) {
+                donor = end - 1;
             } else {
-                const int k = upper_bound_i32(a.episode_ends, a.num_episodes, src);
-                int end;
-                if (k < a.num_episodes) {
-                    end = __ldg(a.episode_ends + k);
-                } else {
-                    end = a.capacity;  // malformed boundaries: flagged, stay in the buffer
-                    bad = 1;
-                }
-                if (a.strategy == OFRL_HER_FINAL) {
-                    donor = end - 1;
-                } else {
-                    const int lo = src + 1;
-                    donor = lo < end ? lo + (int)below(sm64_at(a.seed, ctr | 1ull), (uint64_t)(end - lo))
-                                     : src;
-                }
+                const int lo = src + 1;
+                donor = lo < end ? lo + (int)below(sm64_at(a.seed, ctr | 1ull), (uint64_t)(end - lo)) : src;
             }
         }
     }
-    src = __shfl_sync(0xffffffffu, src, 0, kLanesPerRow);
-    donor = __shfl_sync(0xffffffffu, donor, 0, kLanesPerRow);
-    if (!live) return;
+    donor = __shfl_sync(kFull, donor, 0, kLanesPerRow);
 
-    const float4* s_in = reinterpret_cast<const float4*>(a.states + (int64_t)src * a.in_stride);
-    const float4* n_in = reinterpret_cast<const float4*>(a.next_states + (int64_t)src * a.in_stride);
-    const float4* d_in = reinterpret_cast<const float4*>(a.next_states + (int64_t)(donor < 0 ? 0 : donor) * a.in_stride);
-    float4* s_out = reinterpret_cast<float4*>(a.out_states + (int64_t)row * a.out_stride);
-    float4* n_out = reinterpret_cast<float4*>(a.out_next_states + (int64_t)row * a.out_stride);
-    const int chunks = a.copy_cols >> 2;
-    for (int c = lane; c < chunks; c += kLanesPerRow) {
-        float4 sv = __ldg(s_in + c);
-        float4 nv = __ldg(n_in + c);
-        if (donor >= 0 && 4 * c < a.goal_dim) {
-            const float4 gv = __ldg(d_in + c);
-            const int base = 4 * c;
-            if (base + 0 < a.goal_dim) { sv.x = gv.x; nv.x = gv.x; }
-            if (base + 1 < a.goal_dim) { sv.y = gv.y; nv.y = gv.y; }
-            if (base + 2 < a.goal_dim) { sv.z = gv.z; nv.z = gv.z; }
-            if (base + 3 < a.goal_dim) { sv.w = gv.w; nv.w = gv.w; }
-        }
-        s_out[c] = sv;
-        n_out[c] = nv;
-    }
-    if (lane == 0) {
-        float r;
-        if (donor >= 0) {
-            // fp32 distance as the pages' kernel: float accumulator in order,
-            // each product and sum rounded on its own (no FMA), IEEE sqrtf.
-            const float* ns = a.next_states + (int64_t)src * a.in_stride;
-            const float* nd = a.next_states + (int64_t)donor * a.in_stride;
-            float dsq = 0.0f;
-            for (int d = 0; d < a.goal_dim; ++d) {
-                const float diff = __fsub_rn(__ldg(ns + d), __ldg(nd + d));
+    // 3. goal slice from the donor's next state; reward from the fp32 distance.
+    // Every lane of the warp runs the shuffles (normal rows compare a row
+    // with itself and ignore the result).
+    const bool goal_lane = has && 4 * sub < a.goal_dim;
+    float4 gv = nv;
+    if (goal_lane && donor >= 0)
+        gv = __ldg(reinterpret_cast<const float4*>(a.next_states + (int64_t)donor * a.in_stride) + sub);
+    // distance as the pages' kernel: float accumulator in order d = 0..g-1,
+    // each product and sum rounded on its own (no FMA), IEEE sqrt
+    float dsq = 0.0f;
+    for (int c = 0; 4 * c < a.goal_dim; ++c) {
+        const float av[4] = {__shfl_sync(kFull, nv.x, c, kLanesPerRow), __shfl_sync(kFull, nv.y, c, kLanesPerRow),
+                             __shfl_sync(kFull, nv.z, c, kLanesPerRow), __shfl_sync(kFull, nv.w, c, kLanesPerRow)};
+        const float bv[4] = {__shfl_sync(kFull, gv.x, c, kLanesPerRow), __shfl_sync(kFull, gv.y, c, kLanesPerRow),
+                             __shfl_sync(kFull, gv.z, c, kLanesPerRow), __shfl_sync(kFull, gv.w, c, kLanesPerRow)};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (4 * c + e < a.goal_dim) {
+                const float diff = __fsub_rn(av[e], bv[e]);
                 dsq = __fadd_rn(dsq, __fmul_rn(diff, diff));
             }
-            const float dist = __fsqrt_rn(dsq);
-            r = dist < a.threshold ? 1.0f : -0.01f;
-        } else {
-            r = __ldg(a.rewards + src);
         }
-        a.out_actions[row] = __ldg(a.actions + src);
-        a.out_dones[row] = __ldg(a.dones + src);
-        a.out_rewards[row] = r;
+    }
+    const float r = __fsqrt_rn(dsq) < a.threshold ? 1.0f : -0.01f;
+    if (goal_lane && donor >= 0) {
+        const int base = 4 * sub;
+        if (base + 0 < a.goal_dim) { sv.x = gv.x; nv.x = gv.x; }
+        if (base + 1 < a.goal_dim) { sv.y = gv.y; nv.y = gv.y; }
+        if (base + 2 < a.goal_dim) { sv.z = gv.z; nv.z = gv.z; }
+        if (base + 3 < a.goal_dim) { sv.w = gv.w; nv.w = gv.w; }
+    }
+    if (!live) return;
+    if (has) {
+        reinterpret_cast<float4*>(a.out_states + (int64_t)row * a.out_stride)[sub] = sv;
+        reinterpret_cast<float4*>(a.out_next_states + (int64_t)row * a.out_stride)[sub] = nv;
+    }
+    if (sub == 0) {
+        a.out_actions[row] = act;
+        a.out_dones[row] = done;
+        a.out_rewards[row] = donor >= 0 ? r : rew;
         a.out_src[row] = src;
         a.out_donor[row] = donor;
         if (bad) atomicAdd(a.status + OFRL_STAT_BAD_INDEX, 1);

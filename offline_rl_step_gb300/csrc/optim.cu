@@ -23,15 +23,36 @@
 namespace ofrl {
 namespace {
 
-constexpr int kRedThreads = 256;   // 32 elements x 8 tile lanes
-constexpr int kRedElems = 32;
+constexpr int kRedThreads = 256;   // 8 element lanes (float4) x 32 tile lanes
+constexpr int kElemLanes = 8;
+constexpr int kTileLanes = kRedThreads / kElemLanes;
+constexpr int kRedElems = 4 * kElemLanes;   // elements per block per pass
 constexpr int kMaxGramBlocks = 2048;
 
+// Sum of the tile partials of element group i4..i4+3 over tiles ty, ty + 32,
+// ... (fixed order; independent 16-byte loads in flight).
+__device__ __forceinline__ float4 sum_tiles(const float* __restrict__ pp, int64_t stride, int n_tiles, int ty,
+                                            int64_t i4) {
+    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+    int t = ty;
+    for (; t + kTileLanes < n_tiles; t += 2 * kTileLanes) {
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(pp + (int64_t)t * stride + i4));
+        const float4 b = __ldcg(reinterpret_cast<const float4*>(pp + (int64_t)(t + kTileLanes) * stride + i4));
+        s0.x += a.x; s0.y += a.y; s0.z += a.z; s0.w += a.w;
+        s1.x += b.x; s1.y += b.y; s1.z += b.z; s1.w += b.w;
+    }
+    if (t < n_tiles) {
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(pp + (int64_t)t * stride + i4));
+        s0.x += a.x; s0.y += a.y; s0.z += a.z; s0.w += a.w;
+    }
+    return make_float4(s0.x + s1.x, s0.y + s1.y, s0.z + s1.z, s0.w + s1.w);
+}
+
 __global__ void __launch_bounds__(kRedThreads) reduce_gram_kernel(const ReduceLaunch a) {
-    __shared__ float sh[8][kRedElems + 1];
+    __shared__ float4 sh[kTileLanes][kElemLanes + 1];
     __shared__ unsigned int ticket;
-    __shared__ double dsh[kRedThreads / 32];
-    const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
+    const int tid = threadIdx.x, tx = tid % kElemLanes, ty = tid / kElemLanes;
+    const int lane = tid & 31, wid = tid >> 5;
     const int net = blockIdx.y;
     const int64_t P = a.P;
     const int nsrc = a.n_src;
@@ -41,40 +62,58 @@ __global__ void __launch_bounds__(kRedThreads) reduce_gram_kernel(const ReduceLa
     for (int p = 0; p < kGramPairs; ++p) gacc[p] = 0.0f;
 
     for (int64_t base = (int64_t)blockIdx.x * kRedElems; base < P; base += (int64_t)gridDim.x * kRedElems) {
-        const int64_t i = base + tx;
-        float x[kMaxSrc] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const int64_t i4 = base + 4 * tx;
+        float x[kMaxSrc][4];
+#pragma unroll
+        for (int k = 0; k < kMaxSrc; ++k)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[k][e] = 0.0f;
         if (a.partials != nullptr) {
+            // partial rows are padded to a multiple of 32 floats: the float4 at
+            // i4 < P stays inside the tile's slice
             const float* pp = a.partials + (int64_t)net * a.net_partial_stride;
-            float s = 0.0f;
-            if (i < P)
-                for (int t = ty; t < a.n_tiles; t += 8) s += __ldcg(pp + (int64_t)t * P + i);
-            sh[ty][tx] = s;
+            sh[ty][tx] = i4 < P ? sum_tiles(pp, a.part_stride, a.n_tiles, ty, i4) : make_float4(0.f, 0.f, 0.f, 0.f);
             __syncthreads();
             if (ty == 0) {
-                float g = 0.0f;
+                float g[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                for (int y = 0; y < kTileLanes; ++y) {
+                    const float4 v = sh[y][tx];
+                    g[0] += v.x; g[1] += v.y; g[2] += v.z; g[3] += v.w;
+                }
 #pragma unroll
-                for (int y = 0; y < 8; ++y) g += sh[y][tx];
-                if (i < P) a.g0_out[net][i] = g;
-                x[0] = i < P ? g : 0.0f;
+                for (int e = 0; e < 4; ++e) {
+                    if (i4 + e < P) {
+                        a.g0_out[net][i4 + e] = g[e];
+                        x[0][e] = g[e];
+                    }
+                }
             }
             __syncthreads();
-        } else if (ty == 0 && i < P) {
-            x[0] = __ldg(a.src[net][0] + i);
+        } else if (ty == 0) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (i4 + e < P) x[0][e] = __ldg(a.src[net][0] + i4 + e);
         }
         if (ty == 0 && nsrc > 0) {
-            for (int k = 1; k < nsrc; ++k) x[k] = i < P ? __ldg(a.src[net][k] + i) : 0.0f;
+            for (int k = 1; k < nsrc; ++k)
 #pragma unroll
-            for (int j = 0; j < kMaxSrc; ++j)
+                for (int e = 0; e < 4; ++e)
+                    if (i4 + e < P) x[k][e] = __ldg(a.src[net][k] + i4 + e);
 #pragma unroll
-                for (int k = j; k < kMaxSrc; ++k) gacc[gram_index(j, k)] = fmaf(x[j], x[k], gacc[gram_index(j, k)]);
+            for (int e = 0; e < 4; ++e)
+#pragma unroll
+                for (int j = 0; j < kMaxSrc; ++j)
+#pragma unroll
+                    for (int k = j; k < kMaxSrc; ++k)
+                        gacc[gram_index(j, k)] = fmaf(x[j][e], x[k][e], gacc[gram_index(j, k)]);
         }
     }
     float* gp = a.gram_part + ((int64_t)net * gridDim.x + blockIdx.x) * kGramPairs;
-    if (ty == 0) {
+    if (wid == 0) {   // the element lanes (ty == 0) are lanes 0..7 of warp 0; the rest hold zeros
 #pragma unroll
         for (int p = 0; p < kGramPairs; ++p) {
             const float s = warp_sum(gacc[p]);
-            if (tx == 0) gp[p] = s;
+            if (lane == 0) gp[p] = s;
         }
     }
     __threadfence();
@@ -84,54 +123,62 @@ __global__ void __launch_bounds__(kRedThreads) reduce_gram_kernel(const ReduceLa
     if (ticket != gridDim.x - 1) return;
 
     // ---- last block: fixed-order totals, norms, clip coefficients ----
+    // Every thread loads all ten Gram partials (and the loss partials) of its
+    // blocks at once, so the block pays one round of L2 latency, then one
+    // fixed-order tree over the block.  fp32 throughout: FP64 on this part is
+    // a small fraction of the fp32 rate and a chain of dependent FP64
+    // operations on one thread costs microseconds.
     __threadfence();
-    double gram[kGramPairs];
+    float acc[kGramPairs + 1];
+#pragma unroll
+    for (int p = 0; p <= kGramPairs; ++p) acc[p] = 0.0f;
     const float* gall = a.gram_part + (int64_t)net * gridDim.x * kGramPairs;
-    for (int p = 0; p < kGramPairs; ++p) {
-        double s = 0.0;
-        for (int b = tid; b < (int)gridDim.x; b += kRedThreads) s += (double)__ldcg(gall + (int64_t)b * kGramPairs + p);
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (tx == 0) dsh[ty] = s;
-        __syncthreads();
-        double t = 0.0;
-        for (int y = 0; y < kRedThreads / 32; ++y) t += dsh[y];
-        gram[p] = t;
-        __syncthreads();
+    for (int b = tid; b < (int)gridDim.x; b += kRedThreads) {
+        float v[kGramPairs];
+#pragma unroll
+        for (int p = 0; p < kGramPairs; ++p) v[p] = __ldcg(gall + (int64_t)b * kGramPairs + p);
+#pragma unroll
+        for (int p = 0; p < kGramPairs; ++p) acc[p] += v[p];
     }
-    double loss = 0.0;
     if (a.tile_loss != nullptr) {
         const float* tl = a.tile_loss + (int64_t)net * a.net_tile_stride;
-        double s = 0.0;
-        for (int t = tid; t < a.n_tiles; t += kRedThreads) s += (double)__ldcg(tl + t);
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (tx == 0) dsh[ty] = s;
-        __syncthreads();
-        for (int y = 0; y < kRedThreads / 32; ++y) loss += dsh[y];
+        for (int t = tid; t < a.n_tiles; t += kRedThreads) acc[kGramPairs] += __ldcg(tl + t);
     }
+    __shared__ float tot[kGramPairs + 1][kRedThreads / 32];
+#pragma unroll
+    for (int p = 0; p <= kGramPairs; ++p) {
+        const float s = warp_sum(acc[p]);
+        if (lane == 0) tot[p][wid] = s;
+    }
+    __syncthreads();
     if (tid == 0) {
+        float gram[kGramPairs];
+        float loss = 0.0f;
+        for (int p = 0; p <= kGramPairs; ++p) {
+            float s = 0.0f;
+            for (int y = 0; y < kRedThreads / 32; ++y) s += tot[p][y];
+            if (p < kGramPairs) gram[p] = s; else loss = s;
+        }
         float* sc = a.scalars + (int64_t)net * kScalars;
-        double coef[kMaxSrc] = {0.0, 0.0, 0.0, 0.0};
+        float coef[kMaxSrc] = {0.0f, 0.0f, 0.0f, 0.0f};
         for (int k = 0; k < kMaxSrc; ++k) {
-            const float nk = k < nsrc ? (float)sqrt(gram[gram_index(k, k)]) : 0.0f;
+            const float nk = k < nsrc ? sqrtf(gram[gram_index(k, k)]) : 0.0f;
             sc[SC_NORM0 + k] = nk;
-            if (k < nsrc) {
-                const float c = a.budget[k] * a.max_grad_norm;
-                coef[k] = (double)a.alpha[k] * (double)clip_scale(nk, c);
-            }
-            sc[SC_COEF0 + k] = (float)coef[k];
+            if (k < nsrc) coef[k] = a.alpha[k] * clip_scale(nk, a.budget[k] * a.max_grad_norm);
+            sc[SC_COEF0 + k] = coef[k];
         }
         // IEEE arithmetic throughout: a NaN source norm gives coefficient 1
         // and a NaN total; an infinite one gives coefficient 0 and 0 * inf =
         // NaN, as the element-wise sum of the clipped sources would.
-        double c2 = 0.0;
+        float c2 = 0.0f;
         for (int j = 0; j < nsrc; ++j)
             for (int k = 0; k < nsrc; ++k) {
                 const int lo = j < k ? j : k, hi = j < k ? k : j;
                 c2 += coef[j] * coef[k] * gram[gram_index(lo, hi)];
             }
-        const float cn = (float)(c2 < 0.0 ? 0.0 : sqrt(c2));
+        const float cn = c2 < 0.0f ? 0.0f : sqrtf(c2);
         sc[SC_COMBINED] = cn;
-        const float lmean = (float)(loss * (double)a.inv_batch);
+        const float lmean = loss * a.inv_batch;
         sc[SC_LOSS] = lmean;
         if (a.norms_out != nullptr) {
             for (int k = 0; k < kMaxSrc; ++k) a.norms_out[net * 5 + k] = sc[SC_NORM0 + k];

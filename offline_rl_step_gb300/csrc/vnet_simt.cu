@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_fwd_bwd_kernel(const VnetLau
     const float* __restrict__ prm = a.params[net];
     const float tau = a.tau[net];
     const int row0 = tile * TM;
-    float* part = a.partials + (int64_t)net * a.net_partial_stride + (int64_t)tile * off.total;
+    float* part = a.partials + (int64_t)net * a.net_partial_stride + (int64_t)tile * a.part_stride;
 
     // ---- state tile (zero rows past the batch, zero columns past S) ----
     for (int e = tid; e < TM * kXStride; e += kThreads) {

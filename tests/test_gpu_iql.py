@@ -6,6 +6,7 @@ import pytest
 import torch
 
 import synth
+from _errmodel import grad_ok, value_uncertainty, within
 from _gpu import (ATOL, BF16_RTOL, RTOL, argmax_ok, assert_close, dev, f32, need_gpu)
 from oracle import iql
 
@@ -28,23 +29,25 @@ def _fwd_bwd(s, h, b, tau, prec="fp32", seed=0, stride=None):
     grad = torch.empty(w.n_params, device="cuda")
     ofrl.iql_value_fwd_bwd(ctx, dev(params), dev(x), dev(qt), tau, v, loss, grad)
     torch.cuda.synchronize()
-    rv, rloss, rgrad = iql.value_fwd_bwd(params, x, qt, f32(tau), s, h)
+    rv, rgrad, vu, gu = value_uncertainty(params.astype(np.float64), x, qt, f32(tau), s, h)
+    rloss = iql.value_fwd_bwd(params, x, qt, f32(tau), s, h)[1]
     ctx.close()
-    return (v.cpu().numpy(), float(loss.cpu()[0]), grad.cpu().numpy()), (rv, rloss, rgrad)
+    return (v.cpu().numpy(), float(loss.cpu()[0]), grad.cpu().numpy()), (rv, rloss, rgrad, vu, gu)
 
 
 @pytest.mark.parametrize("s,h,b", [(48, 64, 256), (50, 128, 16384), (50, 128, 300), (50, 256, 200),
                                    (50, 256, 16384), (7, 64, 1), (64, 128, 129)])
 def test_value_fwd_bwd_fp32(s, h, b):
-    (v, loss, g), (rv, rl, rg) = _fwd_bwd(s, h, b, 0.7, seed=s + h + b)
-    assert_close(v, rv, what="V")
+    (v, loss, g), (rv, rl, rg, vu, gu) = _fwd_bwd(s, h, b, 0.7, seed=s + h + b)
+    assert within(v, rv, vu, RTOL, ATOL).all(), "V outside tolerance and fp32 bound"
     assert_close(loss, rl, what="loss")
-    assert_close(g, rg, what="gradient")
+    ok, n_bound, rel = grad_ok(g, rg, gu)
+    assert ok, f"gradient outside tolerance and fp32 bound (norm rel {rel:.3g}, {n_bound} by bound)"
 
 
 @pytest.mark.parametrize("h,b", [(128, 16384), (256, 333)])
 def test_value_fwd_bwd_bf16(h, b):
-    (v, loss, g), (rv, rl, rg) = _fwd_bwd(50, h, b, 0.9, prec="bf16", seed=h + b)
+    (v, loss, g), (rv, rl, rg, _, _) = _fwd_bwd(50, h, b, 0.9, prec="bf16", seed=h + b)
     assert abs(loss - rl) <= BF16_RTOL * abs(rl)
     assert_close(v, rv, rtol=BF16_RTOL, atol=BF16_RTOL * np.abs(rv).mean(), what="V (bf16)")
     # gradient: bf16 operands, compared in norm
