@@ -255,6 +255,38 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
                             float* v_out, float* pi_out, int32_t* argmax_out, float* loss_out,
                             float* norms_out, float* grad_out, void* stream);
 
+/* ---- allocation-free variant (no counterpart in the method's pages) ---- */
+
+/* Some callers may not allocate device memory: code whose GPU memory is
+ * handed out by a host application's or framework's own pool (direct
+ * cudaMalloc forbidden), code recorded into a CUDA graph under the global
+ * capture mode (cudaMalloc is refused there), and latency-critical loops that
+ * cannot take cudaMalloc's implicit device synchronisation.  ofrl_create
+ * allocates, so they call the entry point below instead.
+ *
+ * Its scratch is one file-scope device array of OFRL_NOALLOC_SCRATCH_BYTES,
+ * reserved in every GPU that loads this library until the library is
+ * unloaded.  The first call made with a given device current looks up the
+ * array's device address (cudaGetSymbolAddress) and keeps it; make that first
+ * call before any stream capture.  All calls share the one array: two calls
+ * whose kernels overlap on the GPU (different streams, or different host
+ * threads) race and give wrong results, so serialise them (one stream). */
+#define OFRL_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* Largest batch ofrl_iql_value_fwd_bwd_noalloc accepts for `shape` (what the
+ * scratch array holds), or -1 for an unsupported shape. */
+int64_t ofrl_noalloc_max_batch(const ofrl_vshape* shape);
+
+/* Same computation, arguments and results as ofrl_iql_value_fwd_bwd (V
+ * forward, expectile loss, V backward into grad_out), with `shape` in place
+ * of a context.  Allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library call.  A batch above ofrl_noalloc_max_batch(shape) returns
+ * OFRL_EINVAL before anything is launched; H outside {64, 128, 256} returns
+ * OFRL_EUNSUPPORTED.  Asynchronous on `stream`. */
+ofrl_status ofrl_iql_value_fwd_bwd_noalloc(const ofrl_vshape* shape, const float* params, const float* states,
+                                           int32_t state_stride, int32_t batch, const float* q_taken, float tau,
+                                           float* v_out, float* loss_out, float* grad_out, void* stream);
+
 /* ---- measurement hooks (not part of the method) ----------------------- */
 
 /* Phases of ofrl_train_step, in launch order. */

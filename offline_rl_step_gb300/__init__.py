@@ -199,6 +199,29 @@ def iql_value_fwd_bwd(ctx: Context, params, states, q_taken, tau: float, v_out, 
         _ptr(grad_out, F32, "grad_out"), _stream(stream)))
 
 
+def noalloc_max_batch(state_dim: int, hidden: int, num_actions: int, prec: str = "fp32") -> int:
+    """Largest batch iql_value_fwd_bwd_noalloc accepts for this shape."""
+    shape = _abi.VShape(state_dim, hidden, num_actions, PRECISION[prec])
+    return int(_abi.load().ofrl_noalloc_max_batch(C.byref(shape)))
+
+
+def iql_value_fwd_bwd_noalloc(state_dim: int, hidden: int, num_actions: int, params, states, q_taken,
+                              tau: float, v_out, loss_out, grad_out, prec: str = "fp32", stream=None):
+    """iql_value_fwd_bwd for callers that may not allocate device memory.
+
+    No Context: the library's own fixed scratch array is used (see the C
+    header), so nothing is allocated.  Calls that overlap on the GPU share
+    that scratch and race: issue them on one stream.
+    """
+    lib = _abi.load()
+    shape = _abi.VShape(state_dim, hidden, num_actions, PRECISION[prec])
+    batch = int(q_taken.numel())
+    _abi.check("ofrl_iql_value_fwd_bwd_noalloc", lib.ofrl_iql_value_fwd_bwd_noalloc(
+        C.byref(shape), _ptr(params, F32, "params"), _ptr(states, F32, "states"), states.shape[1], batch,
+        _ptr(q_taken, F32, "q_taken"), tau, _ptr(v_out, F32, "v_out"), _ptr(loss_out, F32, "loss_out"),
+        _ptr(grad_out, F32, "grad_out"), _stream(stream)))
+
+
 def expectile_loss(ctx: Context, q_taken, v, tau: float, loss_out, dv_out=None, stream=None):
     _abi.check("ofrl_expectile_loss", ctx._lib.ofrl_expectile_loss(
         ctx.handle, _ptr(q_taken, F32, "q_taken"), _ptr(v, F32, "v"), int(v.numel()), tau,
