@@ -64,6 +64,8 @@ SIGNATURES = {
     "ofrl_noalloc_max_batch": (C.c_int64, [C.POINTER(VShape)]),
     "ofrl_iql_value_fwd_bwd_noalloc": (C.c_int32, [C.POINTER(VShape), vp, vp, C.c_int32, C.c_int32, vp, C.c_float,
                                                    vp, vp, vp, vp]),
+    "ofrl_selftest_umma": (C.c_int32, [vp, vp, vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
+                                       C.c_int32, vp, vp]),
     "ofrl_profile_begin": (C.c_int32, [vp, C.c_int32]),
     "ofrl_profile_end": (C.c_int32, [vp, C.POINTER(C.c_float), C.POINTER(C.c_int32)]),
 }

@@ -36,7 +36,7 @@ bool shape_ok(const ofrl_vshape* s) {
 bool hidden_supported(int h) { return h == 64 || h == 128 || h == 256; }
 
 struct Layout {
-    int64_t off_partials, off_tile_loss, off_g0, off_gram, off_scalars, off_counter, off_status, total;
+    int64_t off_partials, off_tile_loss, off_g0, off_gram, off_scalars, off_counter, off_status, off_img, total;
     int32_t max_tiles;
     int64_t P;
 };
@@ -55,6 +55,7 @@ Layout layout_of(const ofrl_vshape* s, int32_t max_batch, int32_t max_nets) {
     L.off_scalars = take((int64_t)max_nets * kScalars * 4);
     L.off_counter = take((int64_t)max_nets * 4);
     L.off_status = take((int64_t)OFRL_STAT_WORDS * 4);
+    L.off_img = take(s->hidden == 128 ? (int64_t)max_nets * vnet_tc_image_bytes() : 0);
     L.total = o;
     return L;
 }
@@ -155,6 +156,13 @@ void prof_release(ofrl_ctx* ctx) {
     ctx->prof_max = ctx->prof_count = 0;
 }
 
+// V forward/backward: the tensor-core kernel where it applies (hidden 128,
+// 16-byte rows), else the CUDA-core kernel; both write the same partials.
+cudaError_t launch_vnet(ofrl_ctx* ctx, const VnetLaunch& v, cudaStream_t st) {
+    if (vnet_tc_supported(v)) return launch_vnet_tc(v, ctx->ws.img, st);
+    return launch_vnet_fwd_bwd(v, st);
+}
+
 void bias_corrections(float beta1, float beta2, int32_t t, float* bc1, float* bc2) {
     *bc1 = (float)(1.0 - std::pow((double)beta1, (double)t));
     *bc2 = (float)(1.0 - std::pow((double)beta2, (double)t));
@@ -205,6 +213,7 @@ ofrl_status ofrl_create(const ofrl_vshape* shape, int32_t max_batch, int32_t max
     ctx->ws.scalars = reinterpret_cast<float*>(b + L.off_scalars);
     ctx->ws.counter = reinterpret_cast<unsigned int*>(b + L.off_counter);
     ctx->ws.status = reinterpret_cast<int32_t*>(b + L.off_status);
+    ctx->ws.img = reinterpret_cast<uint8_t*>(b + L.off_img);
     if (cudaMemset(ctx->base, 0, (size_t)L.total) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
         cudaFree(ctx->base);
         delete ctx;
@@ -291,7 +300,7 @@ ofrl_status ofrl_iql_value_fwd_bwd(ofrl_ctx* ctx, const float* params, const flo
     v.net_partial_stride = (int64_t)ctx->max_tiles * v.part_stride;
     v.net_tile_stride = ctx->max_tiles;
     v.status = ctx->ws.status;
-    cudaError_t e = launch_vnet_fwd_bwd(v, st);
+    cudaError_t e = launch_vnet(ctx, v, st);
     if (e != cudaSuccess) return OFRL_ECUDA;
 
     ReduceLaunch r;
@@ -485,7 +494,7 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
     v.net_partial_stride = (int64_t)ctx->max_tiles * v.part_stride;
     v.net_tile_stride = ctx->max_tiles;
     v.status = ctx->ws.status;
-    e = launch_vnet_fwd_bwd(v, st);
+    e = launch_vnet(ctx, v, st);
     if (e != cudaSuccess) return OFRL_ECUDA;
     prof_mark(ctx, 2, st);
 

@@ -37,6 +37,7 @@ struct Workspace {
     float* scalars;       // [max_nets][kScalars]
     unsigned int* counter;  // [max_nets] last-block tickets (reset by the last block)
     int32_t* status;      // [OFRL_STAT_WORDS]
+    uint8_t* img;         // [max_nets] packed bf16 weight images for the tensor-core kernel
 };
 
 }  // namespace ofrl
@@ -181,6 +182,10 @@ struct VnetLaunch {
 };
 int vnet_tile_rows(int hidden);
 cudaError_t launch_vnet_fwd_bwd(const VnetLaunch& a, cudaStream_t st);
+// tensor-core kernel (hidden 128): packed weight images per network
+int64_t vnet_tc_image_bytes();
+bool vnet_tc_supported(const VnetLaunch& a);
+cudaError_t launch_vnet_tc(const VnetLaunch& a, uint8_t* img, cudaStream_t st);
 
 struct ReduceLaunch {
     int n_nets;

@@ -20,9 +20,12 @@ steps are not an element-wise-stable map (a ReLU kink decided the other way
 in fp32 moves a few weights by up to 2 lr, Adam's update is insensitive to
 gradient scale, and the difference spreads), so past that horizon (the
 100-step production run) the test checks the trajectory: batches bit-exact,
-the loss within 1e-4, V and the weights within 1e-4 in norm, under 10% of
+the loss within 1e-4, V and the weights within 1e-3 in norm, under 25% of
 the weights outside the element tolerance (the count is logged), and every weight within 2 lr per step
-of the oracle's.
+of the oracle's.  At steps 25, 50, 75 and 99 the GPU networks are re-loaded
+with the oracle's state (weights, Adam moments and t, rounded to fp32) and
+that step is checked element-wise again, so late steps, with Adam state
+built up, are held to the strict checks too.
 """
 import dataclasses
 import json
@@ -30,6 +33,7 @@ import os
 
 import numpy as np
 import pytest
+import torch
 
 import synth
 from _errmodel import grad_ok, value_uncertainty, within
@@ -42,6 +46,8 @@ pytestmark = pytest.mark.gpu
 
 FULL = os.environ.get("OFRL_FULL_STEPS", "0") == "1"
 STRICT = 10
+TRAJ_RTOL = 1e-3   # norm-wise V and weight agreement past the strict horizon
+RESYNC = (25, 50, 75, 99)   # steps checked strictly from the oracle's state
 LOG = os.environ.get("OFRL_PARITY_LOG")
 
 
@@ -63,10 +69,10 @@ def _check_trajectory(w, k, got, ref, nets):
         p, rp = got["params"][n].astype(np.float64), nets[n].params
         dp = np.abs(p - rp)
         assert abs(got["loss"][n] - ref["loss"][n]) <= RTOL * abs(ref["loss"][n]), f"step {k} loss"
-        assert np.linalg.norm(got["v"][n] - ref["v"][n]) <= RTOL * np.linalg.norm(ref["v"][n]), f"step {k} V"
-        assert np.linalg.norm(dp) <= RTOL * np.linalg.norm(rp), f"step {k} weights (norm)"
+        assert np.linalg.norm(got["v"][n] - ref["v"][n]) <= TRAJ_RTOL * np.linalg.norm(ref["v"][n]), f"step {k} V"
+        assert np.linalg.norm(dp) <= TRAJ_RTOL * np.linalg.norm(rp), f"step {k} weights (norm)"
         off = dp > ATOL + RTOL * np.abs(rp)
-        assert off.mean() < 0.10, f"step {k}: {int(off.sum())} weights outside tolerance"
+        assert off.mean() < 0.25, f"step {k}: {int(off.sum())} weights outside tolerance"
         assert (dp <= 2 * lr * (k + 1) + ATOL).all(), f"step {k}: a weight left the Adam envelope"
         assert abs(got["norms"][n][0] - ref["norms"][n][0]) <= 1e-3 * ref["norms"][n][0], f"step {k} norm"
         _log(dict(workload=w.name, step=k, net=n, phase="trajectory", weights_off_tolerance=int(off.sum()),
@@ -75,7 +81,7 @@ def _check_trajectory(w, k, got, ref, nets):
                   loss_rel=float(abs(got["loss"][n] / ref["loss"][n] - 1))))
 
 
-def _check_step(w, k, got, ref, flagged, nets, p_before, gpu_before, q):
+def _check_step(w, k, got, ref, flagged, nets, p_before, gpu_before, q, strict=False):
     s = w.state_dim
     bt, rb = got["batch"], ref["batch"]
     for key in ("src_idx", "donor_idx", "actions", "rewards", "dones"):
@@ -83,7 +89,7 @@ def _check_step(w, k, got, ref, flagged, nets, p_before, gpu_before, q):
     assert_bits(bt["states"][:, :s], rb["states"][:, :s], f"step {k} states")
     assert_bits(bt["next_states"][:, :s], rb["next_states"][:, :s], f"step {k} next_states")
     lr = w.lr
-    if k >= STRICT and w.prec != "bf16":
+    if k >= STRICT and not strict and w.prec != "bf16":
         _check_trajectory(w, k, got, ref, nets)
         return
     for n in range(w.n_nets):
@@ -136,10 +142,20 @@ def test_train_step_matches_oracle(w):
         for k in range(_steps(w)):
             q = synth.make_q(w, k)
             aux = [synth.make_aux(w, k, n) for n in range(w.n_nets)] if w.n_aux else None
+            resync = k in RESYNC and k >= STRICT and w.prec != "bf16"
+            if resync:
+                # load the oracle's state into the GPU networks (fp32)
+                for n, net in enumerate(nets):
+                    g.nets[n].params.copy_(torch.from_numpy(net.params.astype(np.float32)))
+                    g.nets[n].m.copy_(torch.from_numpy(net.m.astype(np.float32)))
+                    g.nets[n].v.copy_(torch.from_numpy(net.v.astype(np.float32)))
+                    g.nets[n].t = net.t
+                gpu_params = [net.params.astype(np.float32) for net in nets]
+                flagged = [np.zeros(w.n_params, dtype=bool) for _ in range(w.n_nets)]
             got = g.step(k, q, aux)
             p_before = [n.params.copy() for n in nets]
             ref = ostep.train_step(cfg, rep, k, q, nets, aux)
-            _check_step(w, k, got, ref, flagged, nets, p_before, gpu_params, q)
+            _check_step(w, k, got, ref, flagged, nets, p_before, gpu_params, q, strict=resync)
             gpu_params = got["params"]
             if w.n_aux:
                 # the combined norm never exceeds the budget sum
