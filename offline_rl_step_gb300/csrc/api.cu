@@ -15,6 +15,7 @@
 #include <new>
 
 #include "common.cuh"
+#include "tc_image.cuh"
 
 using namespace ofrl;
 
@@ -36,7 +37,8 @@ bool shape_ok(const ofrl_vshape* s) {
 bool hidden_supported(int h) { return h == 64 || h == 128 || h == 256; }
 
 struct Layout {
-    int64_t off_partials, off_tile_loss, off_g0, off_gram, off_scalars, off_counter, off_status, off_img, total;
+    int64_t off_partials, off_tile_loss, off_g0, off_gram, off_scalars, off_counter, off_status, off_img, off_ximg,
+        total;
     int32_t max_tiles;
     int64_t P;
 };
@@ -56,6 +58,7 @@ Layout layout_of(const ofrl_vshape* s, int32_t max_batch, int32_t max_nets) {
     L.off_counter = take((int64_t)max_nets * 4);
     L.off_status = take((int64_t)OFRL_STAT_WORDS * 4);
     L.off_img = take(s->hidden == 128 ? (int64_t)max_nets * vnet_tc_image_bytes() : 0);
+    L.off_ximg = take(s->hidden == 128 ? (int64_t)L.max_tiles * tc::x_tile_bytes() : 0);
     L.total = o;
     return L;
 }
@@ -158,8 +161,15 @@ void prof_release(ofrl_ctx* ctx) {
 
 // V forward/backward: the tensor-core kernel where it applies (hidden 128,
 // 16-byte rows), else the CUDA-core kernel; both write the same partials.
-cudaError_t launch_vnet(ofrl_ctx* ctx, const VnetLaunch& v, cudaStream_t st) {
-    if (vnet_tc_supported(v)) return launch_vnet_tc(v, ctx->ws.img, st);
+// `packed`: the weight images (and v.ximg, if set) were already written.
+cudaError_t launch_vnet(ofrl_ctx* ctx, const VnetLaunch& v, bool packed, cudaStream_t st) {
+    if (vnet_tc_supported(v)) {
+        if (!packed) {
+            const cudaError_t e = launch_vnet_tc_pack(v, ctx->ws.img, st);
+            if (e != cudaSuccess) return e;
+        }
+        return launch_vnet_tc(v, ctx->ws.img, st);
+    }
     return launch_vnet_fwd_bwd(v, st);
 }
 
@@ -214,6 +224,7 @@ ofrl_status ofrl_create(const ofrl_vshape* shape, int32_t max_batch, int32_t max
     ctx->ws.counter = reinterpret_cast<unsigned int*>(b + L.off_counter);
     ctx->ws.status = reinterpret_cast<int32_t*>(b + L.off_status);
     ctx->ws.img = reinterpret_cast<uint8_t*>(b + L.off_img);
+    ctx->ws.ximg = reinterpret_cast<uint8_t*>(b + L.off_ximg);
     if (cudaMemset(ctx->base, 0, (size_t)L.total) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
         cudaFree(ctx->base);
         delete ctx;
@@ -300,7 +311,7 @@ ofrl_status ofrl_iql_value_fwd_bwd(ofrl_ctx* ctx, const float* params, const flo
     v.net_partial_stride = (int64_t)ctx->max_tiles * v.part_stride;
     v.net_tile_stride = ctx->max_tiles;
     v.status = ctx->ws.status;
-    cudaError_t e = launch_vnet(ctx, v, st);
+    cudaError_t e = launch_vnet(ctx, v, false, st);
     if (e != cudaSuccess) return OFRL_ECUDA;
 
     ReduceLaunch r;
@@ -460,14 +471,8 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
     const int64_t P = ctx->n_params;
     const int B = her->batch;
 
-    // 1. HER relabel
-    prof_mark(ctx, 0, st);
-    const HerLaunch ha = her_args(ctx, replay, her, step, batch);
-    cudaError_t e = launch_her_relabel(ha, st);
-    if (e != cudaSuccess) return OFRL_ECUDA;
-    prof_mark(ctx, 1, st);
-
-    // 2. V forward / loss / policy / backward partials, all networks in one grid
+    // 2's arguments first: whether the tensor-core kernel runs decides what
+    // the relabel launch also produces
     VnetLaunch v;
     std::memset(&v, 0, sizeof(v));
     for (int k = 0; k < n_nets; ++k) {
@@ -494,7 +499,26 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
     v.net_partial_stride = (int64_t)ctx->max_tiles * v.part_stride;
     v.net_tile_stride = ctx->max_tiles;
     v.status = ctx->ws.status;
-    e = launch_vnet(ctx, v, st);
+    const bool tc_path = vnet_tc_supported(v);
+
+    // 1. HER relabel (+ state-tile images and packed weights for the tensor-core kernel)
+    prof_mark(ctx, 0, st);
+    HerLaunch ha = her_args(ctx, replay, her, step, batch);
+    if (tc_path) {
+        ha.ximg = ctx->ws.ximg;
+        ha.img_planes = sh.prec == OFRL_PREC_BF16 ? 1 : 3;
+        ha.img_rows = (B + tc::TM - 1) / tc::TM * tc::TM;
+        ha.wimg = ctx->ws.img;
+        ha.pack_nets = n_nets;
+        for (int k = 0; k < n_nets; ++k) ha.pack_params[k] = nets[k].params;
+        v.ximg = ctx->ws.ximg;
+    }
+    cudaError_t e = launch_her_relabel(ha, st);
+    if (e != cudaSuccess) return OFRL_ECUDA;
+    prof_mark(ctx, 1, st);
+
+    // 2. V forward / loss / policy / backward partials, all networks in one grid
+    e = launch_vnet(ctx, v, true, st);
     if (e != cudaSuccess) return OFRL_ECUDA;
     prof_mark(ctx, 2, st);
 

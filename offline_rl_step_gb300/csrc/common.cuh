@@ -38,6 +38,7 @@ struct Workspace {
     unsigned int* counter;  // [max_nets] last-block tickets (reset by the last block)
     int32_t* status;      // [OFRL_STAT_WORDS]
     uint8_t* img;         // [max_nets] packed bf16 weight images for the tensor-core kernel
+    uint8_t* ximg;        // [max_tiles] bf16 images of the relabelled state tiles
 };
 
 }  // namespace ofrl
@@ -155,6 +156,17 @@ struct HerLaunch {
     int32_t copy_cols;      // columns copied per row (multiple of 4, <= 64)
     int32_t search_rounds;  // 16-ary search rounds that shrink num_episodes to <= 16
     int32_t* status;
+    // optional: bf16 images of the relabelled states per 128-row tile, for
+    // the tensor-core V kernel (rows past the batch are zero), and packed
+    // weight images made by extra blocks of the same grid
+    uint8_t* ximg;          // null: no images
+    int32_t img_planes;     // 3 (fp32 workloads) or 1 (bf16)
+    int32_t img_rows;       // batch rounded up to a whole tile
+    int32_t relabel_blocks; // blocks doing rows; the rest pack weights
+    int32_t pack_blocks;
+    int32_t pack_nets;
+    const float* pack_params[kMaxNets];
+    uint8_t* wimg;          // per network: W1 image then W2 image
 };
 cudaError_t launch_her_relabel(const HerLaunch& a, cudaStream_t st);
 
@@ -175,6 +187,7 @@ struct VnetLaunch {
     int32_t* argmax_out;       // [n_nets, B] or null
     float* partials;           // [n_nets][n_tiles][part_stride]
     float* tile_loss;          // [n_nets][n_tiles]
+    const uint8_t* ximg;       // tensor-core kernel: state tile images from the relabel (or null)
     int64_t part_stride;       // floats between tiles in partials (P rounded up to 32)
     int64_t net_partial_stride;  // floats between networks in partials
     int32_t net_tile_stride;     // floats between networks in tile_loss
@@ -185,7 +198,8 @@ cudaError_t launch_vnet_fwd_bwd(const VnetLaunch& a, cudaStream_t st);
 // tensor-core kernel (hidden 128): packed weight images per network
 int64_t vnet_tc_image_bytes();
 bool vnet_tc_supported(const VnetLaunch& a);
-cudaError_t launch_vnet_tc(const VnetLaunch& a, uint8_t* img, cudaStream_t st);
+cudaError_t launch_vnet_tc_pack(const VnetLaunch& a, uint8_t* img, cudaStream_t st);
+cudaError_t launch_vnet_tc(const VnetLaunch& a, const uint8_t* img, cudaStream_t st);
 
 struct ReduceLaunch {
     int n_nets;

@@ -16,6 +16,7 @@
 // when the row stride is a multiple of 8 floats.
 
 #include "common.cuh"
+#include "tc_image.cuh"
 
 namespace ofrl {
 namespace {
@@ -53,10 +54,48 @@ __device__ __forceinline__ int episode_search(const int32_t* __restrict__ ends, 
     return f < len ? lo + f : lo + len;
 }
 
+// Extra blocks of the relabel grid: W1 [H][S] -> [128 x 64] image and
+// W2 [H][H] -> [128 x 128] image of every network, img_planes planes.
+__device__ void pack_weights(const HerLaunch& a) {
+    const int S = a.state_dim, H = tc::HH, np = a.img_planes;
+    const Offsets off = offsets_of(S, H);
+    const int n1 = H * (tc::KX / 4), n2 = H * (H / 4);      // groups of 4 columns
+    const int total = a.pack_nets * (n1 + n2);
+    for (int e = (blockIdx.x - a.relabel_blocks) * blockDim.x + threadIdx.x; e < total;
+         e += a.pack_blocks * blockDim.x) {
+        const int net = e / (n1 + n2), f = e % (n1 + n2);
+        const float* prm = a.pack_params[net];
+        uint8_t* w1i = a.wimg + (int64_t)net * tc::weight_image_bytes();
+        uint8_t* w2i = w1i + 3 * tc::kPlaneX;
+        float x[4];
+        if (f < n1) {
+            const int r = f / (tc::KX / 4), c = 4 * (f % (tc::KX / 4));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) x[j] = c + j < S ? __ldg(prm + off.w1 + (int64_t)r * S + c + j) : 0.0f;
+            tc::put4(w1i, tc::kPlaneX, np, tc::KX, r, c, x);
+        } else {
+            const int g = f - n1, r = g / (H / 4), c = 4 * (g % (H / 4));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) x[j] = __ldg(prm + off.w2 + (int64_t)r * H + c + j);
+            tc::put4(w2i, tc::kPlaneH, np, H, r, c, x);
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerLaunch a) {
+    if ((int)blockIdx.x >= a.relabel_blocks) {
+        pack_weights(a);
+        return;
+    }
     const int sub = threadIdx.x & (kLanesPerRow - 1);
     const int row_raw = blockIdx.x * kRowsPerBlock + threadIdx.x / kLanesPerRow;
     const bool live = row_raw < a.batch;
+    if (a.ximg != nullptr && row_raw >= a.batch && row_raw < a.img_rows) {
+        // the last tile's rows past the batch: zero image rows
+        const float z[4] = {0.f, 0.f, 0.f, 0.f};
+        tc::put4(a.ximg + (int64_t)(row_raw / tc::TM) * a.img_planes * tc::kPlaneX, tc::kPlaneX, a.img_planes,
+                 tc::KX, row_raw % tc::TM, 4 * sub, z);
+    }
     const int row = live ? row_raw : a.batch - 1;   // dead half-warps shadow the last row, write nothing
     const uint64_t ctr = (a.step << 32) | ((uint64_t)row << 1);
 
@@ -134,6 +173,15 @@ __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerL
         if (base + 3 < a.goal_dim) { sv.w = gv.w; nv.w = gv.w; }
     }
     if (!live) return;
+    if (a.ximg != nullptr) {
+        // the relabelled state, columns 4 sub .. 4 sub + 3, into this row's tile image
+        float x[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (!has || 4 * sub + j >= a.state_dim) x[j] = 0.0f;
+        tc::put4(a.ximg + (int64_t)(row / tc::TM) * a.img_planes * tc::kPlaneX, tc::kPlaneX, a.img_planes, tc::KX,
+                 row % tc::TM, 4 * sub, x);
+    }
     if (has) {
         reinterpret_cast<float4*>(a.out_states + (int64_t)row * a.out_stride)[sub] = sv;
         reinterpret_cast<float4*>(a.out_next_states + (int64_t)row * a.out_stride)[sub] = nv;
@@ -150,10 +198,13 @@ __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerL
 
 }  // namespace
 
-cudaError_t launch_her_relabel(const HerLaunch& a, cudaStream_t st) {
-    if (a.batch <= 0) return cudaSuccess;
-    const int blocks = (a.batch + kRowsPerBlock - 1) / kRowsPerBlock;
-    her_relabel_kernel<<<blocks, kRelabelThreads, 0, st>>>(a);
+cudaError_t launch_her_relabel(const HerLaunch& a_in, cudaStream_t st) {
+    if (a_in.batch <= 0) return cudaSuccess;
+    HerLaunch a = a_in;
+    const int rows = a.ximg != nullptr ? a.img_rows : a.batch;
+    a.relabel_blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+    a.pack_blocks = a.wimg != nullptr ? 48 : 0;
+    her_relabel_kernel<<<a.relabel_blocks + a.pack_blocks, kRelabelThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 

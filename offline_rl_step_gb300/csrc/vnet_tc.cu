@@ -12,44 +12,44 @@
 //   G3  dW2 [H x H]     = dz2^T . h1     (A: dz2 MN-major, B: h1 MN-major)
 //   G4  dh1 [rows x H]  = dz2 . W2       (A: dz2 K-major,  B: W2 MN-major)
 //   G5  dW1 [H x 64]    = dz1^T . X      (A: dz1 MN-major, B: X  MN-major)
-// Every operand lives in shared memory as an "image": bf16 core matrices of
-// 8 rows x 8 elements (16 bytes), chunk-major inside 8-row groups.  The same
-// image of an activation tile is the K-major operand of one GEMM and the
-// MN-major operand of another, so nothing is transposed.
+// Operands are bf16 images in shared memory (tc_image.cuh): core matrices of
+// 8 rows x 8 elements, so an activation tile written once is the K-major
+// operand of one GEMM and the MN-major operand of another.
 //
-// Precision: for fp32 results each fp32 operand is split into three bf16
-// terms x = x0 + x1 + x2 (24 significand bits) and each K-step issues the six
-// products whose size reaches 2^-16 of the leading one (x2 y0, x1 y1, x0 y2,
-// x1 y0, x0 y1, x0 y0); the dropped ones are below fp32 rounding.  For the
-// bf16 workload the operands are bf16 and one product is issued.
+// Precision: for fp32 results every operand is split into three bf16 terms
+// x = x0 + x1 + x2 (24 significand bits) and each K-step issues the six
+// products down to 2^-16 of the leading one (x2 y0, x1 y1, x0 y2, x1 y0,
+// x0 y1, x0 y0); the rest lie below fp32 rounding.  The bf16 workload has one
+// term and one product.
 //
 // Shared memory: two 96 KB regions reused through the step:
 //   R0: X image -> h1 -> W2 image (for G4) -> dz1
 //   R1: W1 image -> W2 image (for G2) -> dz2 -> X image (for G5)
-// Weight images come from the pack kernel in global memory (one bulk async
-// copy each); X images are built by the CTA's threads from the fp32 batch.
+// Images arrive by bulk asynchronous copies (cp.async.bulk) on an mbarrier:
+// the weights from the per-step pack, the state tiles from the relabel
+// kernel (or, without those, are built here from the fp32 batch).
+// 16 warps: warp w reads TMEM lane quarter w % 4 (tile rows, or hidden units
+// for the weight gradients) and column group w / 4 (32 columns).
 
 #include "common.cuh"
+#include "tc_image.cuh"
 #include "umma.cuh"
 
 namespace ofrl {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int TM = 128;     // batch rows per tile (MMA M)
-constexpr int HH = 128;     // hidden width of this kernel
-constexpr int KX = 64;      // state columns, padded (K of G1, N of G5)
+using tc::HH;
+using tc::KX;
+using tc::kPlaneH;
+using tc::kPlaneX;
+using tc::TM;
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_Z1 = 0, TM_Z2 = 128, TM_DW2 = 256, TM_DW1 = 384;   // TM_Z1 also holds dh1
-constexpr uint32_t kPlaneH = TM * HH * 2;    // one bf16 plane of a [128 x 128] image
-constexpr uint32_t kPlaneX = TM * KX * 2;    // one bf16 plane of a [128 x 64] image
 constexpr uint32_t kRegion = 3 * kPlaneH;    // 96 KB
 constexpr uint64_t kWaitNs = 1000000000ull;  // bounded waits: 1 s
-
-// Byte offset of element (r, c) inside one plane of an image with C columns.
-__device__ __forceinline__ uint32_t img_off(int r, int c, int C) {
-    return (uint32_t)((r >> 3) * (C >> 3) * 128 + (c >> 3) * 128 + (r & 7) * 16 + (c & 7) * 2);
-}
 
 // Descriptor of K-step ks (16 elements of K) of an image with C columns:
 // K-major (rows = M/N, columns = K): LBO = 128 (next chunk along K),
@@ -69,17 +69,15 @@ template <int NP>
 __device__ __forceinline__ void gemm(uint32_t d_tmem, const uint8_t* a, uint32_t a_plane, int a_cols, bool a_mn,
                                      const uint8_t* b, uint32_t b_plane, int b_cols, bool b_mn, int ksteps, int n) {
     const uint32_t idesc = umma::instr_desc(umma::kTypeBF16, a_mn, b_mn, TM, n);
-    // (a term, b term): smallest products first
-    constexpr int na = NP == 3 ? 6 : 1;
-    const int ta[6] = {2, 1, 0, 1, 0, 0};
-    const int tb[6] = {0, 1, 2, 0, 1, 0};
+    constexpr int nt = NP == 3 ? 6 : 1;
+    constexpr int ta[6] = {2, 1, 0, 1, 0, 0};   // smallest products first
+    constexpr int tb[6] = {0, 1, 2, 0, 1, 0};
     uint32_t acc = 0;
     for (int ks = 0; ks < ksteps; ++ks) {
 #pragma unroll
-        for (int t = 0; t < na; ++t) {
-            const int pa = NP == 3 ? ta[t] : 0, pb = NP == 3 ? tb[t] : 0;
-            const uint8_t* ap = a + (uint32_t)pa * a_plane;
-            const uint8_t* bp = b + (uint32_t)pb * b_plane;
+        for (int t = 0; t < nt; ++t) {
+            const uint8_t* ap = a + (uint32_t)(NP == 3 ? ta[t] : 0) * a_plane;
+            const uint8_t* bp = b + (uint32_t)(NP == 3 ? tb[t] : 0) * b_plane;
             const uint64_t ad = a_mn ? desc_mn(ap, a_cols, ks) : desc_k(ap, a_cols, ks);
             const uint64_t bd = b_mn ? desc_mn(bp, b_cols, ks) : desc_k(bp, b_cols, ks);
             umma::mma_f16(d_tmem, ad, bd, idesc, acc);
@@ -88,45 +86,37 @@ __device__ __forceinline__ void gemm(uint32_t d_tmem, const uint8_t* a, uint32_t
     }
 }
 
-// Store 16 fp32 values of row r, columns c0..c0+15 (c0 a multiple of 16) into
-// an image with C columns, as NP bf16 planes.
+// Store 16 fp32 values of row r, columns c0..c0+15 into a [128 x 128] image.
 template <int NP>
-__device__ __forceinline__ void store16(uint8_t* img, uint32_t plane, int C, int r, int c0, const float (&v)[16]) {
-    __nv_bfloat16 t[3][16];
+__device__ __forceinline__ void store16(uint8_t* img, int r, int c0, const float (&v)[16]) {
+    __nv_bfloat16 t[NP][16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-        if (NP == 3) umma::split_bf16x3(v[j], t[0][j], t[1][j], t[2][j]);
+        if constexpr (NP == 3) tc::split3(v[j], t[0][j], t[1][j], t[2][j]);
         else t[0][j] = __float2bfloat16_rn(v[j]);
     }
+    const uint32_t o0 = tc::img_off(r, c0, HH), o1 = tc::img_off(r, c0 + 8, HH);
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
-        uint8_t* base = img + (uint32_t)p * plane;
-        *reinterpret_cast<uint4*>(base + img_off(r, c0, C)) = *reinterpret_cast<const uint4*>(&t[p][0]);
-        *reinterpret_cast<uint4*>(base + img_off(r, c0 + 8, C)) = *reinterpret_cast<const uint4*>(&t[p][8]);
+        *reinterpret_cast<uint4*>(img + (uint32_t)p * kPlaneH + o0) = *reinterpret_cast<const uint4*>(&t[p][0]);
+        *reinterpret_cast<uint4*>(img + (uint32_t)p * kPlaneH + o1) = *reinterpret_cast<const uint4*>(&t[p][8]);
     }
 }
 
-// Build the X image ([128 x 64], NP planes) of this tile from the fp32 batch:
-// rows past the batch and columns past S are zero.
-template <int NP>
-__device__ __forceinline__ void build_x(uint8_t* img, const float* __restrict__ states, int stride, int row0, int B,
-                                        int S) {
+// Build the X image ([128 x 64]) of a tile from the fp32 batch (used when the
+// relabel kernel did not write images): rows past the batch, columns past S
+// are zero.
+__device__ __forceinline__ void build_x(uint8_t* img, int np, const float* __restrict__ states, int stride, int row0,
+                                        int B, int S) {
     for (int e = threadIdx.x; e < TM * (KX / 4); e += kThreads) {
         const int r = e / (KX / 4), c = 4 * (e % (KX / 4));
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (row0 + r < B && c < S) v = __ldg(reinterpret_cast<const float4*>(states + (int64_t)(row0 + r) * stride + c));
         float x[4] = {v.x, v.y, v.z, v.w};
-        __nv_bfloat16 t[3][4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 4; ++j)
             if (c + j >= S) x[j] = 0.0f;
-            if (NP == 3) umma::split_bf16x3(x[j], t[0][j], t[1][j], t[2][j]);
-            else t[0][j] = __float2bfloat16_rn(x[j]);
-        }
-#pragma unroll
-        for (int p = 0; p < NP; ++p)
-            *reinterpret_cast<uint2*>(img + (uint32_t)p * kPlaneX + img_off(r, c, KX)) =
-                *reinterpret_cast<const uint2*>(&t[p][0]);
+        tc::put4(img, kPlaneX, np, KX, r, c, x);
     }
 }
 
@@ -151,21 +141,20 @@ struct TcSmem {
     uint8_t r0[kRegion];
     uint8_t r1[kRegion];
     float b1[HH], b2[HH], w3[HH];
-    float vsum[2][TM];
-    float red[3][8][64];    // per warp column sums: dW3, db2, db1
-    float lred[2][8];       // per warp: loss, db3
+    float vsum[4][TM];
+    float red[3][kWarps][32];   // per warp column sums: dW3, db2, db1
+    float lred[2][4];           // per lane-quarter warp of column group 0: loss, db3
     uint64_t bar_mma, bar_load;
     uint32_t tmem_slot;
 };
 
 template <int NP>
-__global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a, const uint8_t* __restrict__ w1img,
-                                                              const uint8_t* __restrict__ w2img, int64_t img_stride) {
+__global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a, const uint8_t* __restrict__ wimg) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     TcSmem& sm = *reinterpret_cast<TcSmem*>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q = warp & 3, hh = warp >> 2;      // TMEM lane quarter, column half
-    const int row = 32 * q + lane;               // this thread's tile row (accumulator lane)
+    const int q = warp & 3, cg = warp >> 2;     // TMEM lane quarter, column group (32 columns)
+    const int row = 32 * q + lane;              // tile row / accumulator lane of this thread
     const int tile = blockIdx.x, net = blockIdx.y;
     const int S = a.state_dim, B = a.batch, NA = a.num_actions;
     const int row0 = tile * TM;
@@ -173,10 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     const float* __restrict__ prm = a.params[net];
     const float tau = a.tau[net];
     float* part = a.partials + (int64_t)net * a.net_partial_stride + (int64_t)tile * a.part_stride;
-    const uint8_t* w1i = w1img + (int64_t)net * img_stride;
-    const uint8_t* w2i = w1i + (uint32_t)NP * kPlaneX;
-    (void)w2img;
-    constexpr uint32_t kW1Bytes = (uint32_t)NP * kPlaneX, kW2Bytes = (uint32_t)NP * kPlaneH;
+    const uint8_t* w1i = wimg + (int64_t)net * tc::weight_image_bytes();
+    const uint8_t* w2i = w1i + 3 * kPlaneX;
+    const uint8_t* xi = a.ximg != nullptr ? a.ximg + (int64_t)tile * NP * kPlaneX : nullptr;
+    constexpr uint32_t kXBytes = (uint32_t)NP * kPlaneX, kW2Bytes = (uint32_t)NP * kPlaneH;
 
     if (tid == 0) {
         umma::mbar_init(&sm.bar_mma, 1);
@@ -207,12 +196,13 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         ph_load ^= 1u;
     };
 
-    // ---- stage 1: W1 image -> R1 (bulk copy), X image -> R0 (threads) ----
+    // ---- stage 1: X image -> R0, W1 image -> R1 ----
     if (tid == 0) {
-        umma::mbar_expect_tx(&sm.bar_load, kW1Bytes);
-        umma::bulk_g2s(sm.r1, w1i, kW1Bytes, &sm.bar_load);
+        umma::mbar_expect_tx(&sm.bar_load, (xi ? kXBytes : 0u) + kXBytes);
+        if (xi) umma::bulk_g2s(sm.r0, xi, kXBytes, &sm.bar_load);
+        umma::bulk_g2s(sm.r1, w1i, kXBytes, &sm.bar_load);
     }
-    build_x<NP>(sm.r0, a.states, a.stride, row0, B, S);
+    if (!xi) build_x(sm.r0, NP, a.states, a.stride, row0, B, S);
     umma::fence_smem_to_async();
     __syncthreads();
     wait_load();
@@ -223,12 +213,17 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         umma::commit(&sm.bar_mma);
     }
     wait_mma();
+    // W1 is no longer read: the W2 image streams into R1 during epilogue 1
+    if (tid == 0) {
+        umma::mbar_expect_tx(&sm.bar_load, kW2Bytes);
+        umma::bulk_g2s(sm.r1, w2i, kW2Bytes, &sm.bar_load);
+    }
 
     // ---- epilogue 1: h1 = relu(z1 + b1) -> R0; ReLU mask bits kept ----
-    uint64_t mask1 = 0;
+    uint32_t mask1 = 0;
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-        const int c0 = hh * 64 + cc * 16;
+    for (int cc = 0; cc < 2; ++cc) {
+        const int c0 = cg * 32 + cc * 16;
         float v[16];
         umma::tmem_ld16(tq + TM_Z1 + (uint32_t)c0, v);
         umma::tmem_ld_wait();
@@ -236,18 +231,13 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         for (int j = 0; j < 16; ++j) {
             const float z = v[j] + sm.b1[c0 + j];
             v[j] = z < 0.0f ? 0.0f : z;
-            if (v[j] > 0.0f) mask1 |= 1ull << (cc * 16 + j);
+            if (v[j] > 0.0f) mask1 |= 1u << (cc * 16 + j);
         }
-        store16<NP>(sm.r0, kPlaneH, HH, row, c0, v);
+        store16<NP>(sm.r0, row, c0, v);
     }
     umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
-    // ---- stage 2: W2 image -> R1 ----
-    if (tid == 0) {
-        umma::mbar_expect_tx(&sm.bar_load, kW2Bytes);
-        umma::bulk_g2s(sm.r1, w2i, kW2Bytes, &sm.bar_load);
-    }
     wait_load();
     // ---- G2: z2 = h1 . W2^T ----
     if (tid == 0) {
@@ -258,26 +248,23 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     wait_mma();
 
     // ---- epilogue 2: V, loss, dV, policy, dz2 -> R1, dW3 / db2 / db3 ----
-    float z2[64];
+    float z2[32];
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
+    for (int cc = 0; cc < 2; ++cc) {
         float v[16];
-        umma::tmem_ld16(tq + TM_Z2 + (uint32_t)(hh * 64 + cc * 16), v);
+        umma::tmem_ld16(tq + TM_Z2 + (uint32_t)(cg * 32 + cc * 16), v);
         umma::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) z2[cc * 16 + j] = v[j] + sm.b2[hh * 64 + cc * 16 + j];
+        for (int j = 0; j < 16; ++j) z2[cc * 16 + j] = v[j] + sm.b2[cg * 32 + cc * 16 + j];
     }
     {
         float vp = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-            const float h = z2[j] < 0.0f ? 0.0f : z2[j];
-            vp = fmaf(h, sm.w3[hh * 64 + j], vp);
-        }
-        sm.vsum[hh][row] = vp;
+        for (int j = 0; j < 32; ++j) vp = fmaf(z2[j] < 0.0f ? 0.0f : z2[j], sm.w3[cg * 32 + j], vp);
+        sm.vsum[cg][row] = vp;
     }
     __syncthreads();
-    const float V = (sm.vsum[0][row] + sm.vsum[1][row]) + b3;
+    const float V = ((sm.vsum[0][row] + sm.vsum[1][row]) + (sm.vsum[2][row] + sm.vsum[3][row])) + b3;
     const int b = row0 + row;
     float dv = 0.0f, lossp = 0.0f;
     if (b < B) {
@@ -285,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         if (a.q != nullptr) {
             int act = __ldg(a.actions + b);
             if (act < 0 || act >= NA) {
-                if (hh == 0) atomicAdd(a.status + OFRL_STAT_BAD_ACTION, 1);
+                if (cg == 0) atomicAdd(a.status + OFRL_STAT_BAD_ACTION, 1);
                 act = 0;
             }
             qv = __ldg(a.q + (int64_t)b * NA + act);
@@ -296,8 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         const float w = d >= 0.0f ? tau : 1.0f - tau;
         lossp = w * d * d;
         dv = (-2.0f * w * d) / (float)B;
-        if (hh == 0 && a.v_out != nullptr) a.v_out[(int64_t)net * B + b] = V;
-        if (hh == 1 && a.pi_out != nullptr) {
+        if (cg == 0 && a.v_out != nullptr) a.v_out[(int64_t)net * B + b] = V;
+        if (cg == 1 && a.pi_out != nullptr) {
             const float* qr = a.q + (int64_t)b * NA;
             float zz[kMaxActions];
             float zmax = -INFINITY, amax = -INFINITY;
@@ -315,14 +302,13 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
             if (a.argmax_out != nullptr) a.argmax_out[(int64_t)net * B + b] = best;
         }
     }
-    {
-        const float ls = warp_sum(hh == 0 ? lossp : 0.0f);
-        const float ds = warp_sum(hh == 0 ? dv : 0.0f);
-        if (lane == 0) { sm.lred[0][warp] = ls; sm.lred[1][warp] = ds; }
+    if (cg == 0) {
+        const float ls = warp_sum(lossp), ds = warp_sum(dv);
+        if (lane == 0) { sm.lred[0][q] = ls; sm.lred[1][q] = ds; }
     }
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-        const int c0 = hh * 64 + cc * 16;
+    for (int cc = 0; cc < 2; ++cc) {
+        const int c0 = cg * 32 + cc * 16;
         float g[16], hw[16], gs[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -331,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
             hw[j] = dv * (z < 0.0f ? 0.0f : z);
             gs[j] = g[j];
         }
-        store16<NP>(sm.r1, kPlaneH, HH, row, c0, g);
+        store16<NP>(sm.r1, row, c0, g);
         const float s3 = colsum16(hw);
         const float s2 = colsum16(gs);
         if ((lane & 1) == 0) {
@@ -350,15 +336,15 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     }
     // dW3, db2, db3 and the loss partial of the tile (fixed order over warps)
     for (int c = tid; c < HH; c += kThreads) {
-        const int h2 = c >> 6, cl = c & 63;
+        const int g = c >> 5, cl = c & 31;
         float s3 = 0.0f, s2 = 0.0f;
-        for (int qq = 0; qq < 4; ++qq) { s3 += sm.red[0][h2 * 4 + qq][cl]; s2 += sm.red[1][h2 * 4 + qq][cl]; }
+        for (int qq = 0; qq < 4; ++qq) { s3 += sm.red[0][g * 4 + qq][cl]; s2 += sm.red[1][g * 4 + qq][cl]; }
         part[off.w3 + c] = s3;
         part[off.b2 + c] = s2;
     }
     if (tid == 0) {
-        float l = 0.0f, d3 = 0.0f;
-        for (int w = 0; w < 4; ++w) { l += sm.lred[0][w]; d3 += sm.lred[1][w]; }
+        const float l = (sm.lred[0][0] + sm.lred[0][1]) + (sm.lred[0][2] + sm.lred[0][3]);
+        const float d3 = (sm.lred[1][0] + sm.lred[1][1]) + (sm.lred[1][2] + sm.lred[1][3]);
         a.tile_loss[(int64_t)net * a.net_tile_stride + tile] = l;
         part[off.b3] = d3;
     }
@@ -376,28 +362,33 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         umma::commit(&sm.bar_mma);
     }
     wait_mma();
+    // dz2 is no longer read: the X image streams into R1 during epilogue 4
+    if (tid == 0 && xi) {
+        umma::mbar_expect_tx(&sm.bar_load, kXBytes);
+        umma::bulk_g2s(sm.r1, xi, kXBytes, &sm.bar_load);
+    }
 
     // ---- epilogue 4: dz1 = dh1 * 1[z1 > 0] -> R0; db1 ----
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-        const int c0 = hh * 64 + cc * 16;
+    for (int cc = 0; cc < 2; ++cc) {
+        const int c0 = cg * 32 + cc * 16;
         float v[16];
         umma::tmem_ld16(tq + TM_Z1 + (uint32_t)c0, v);
         umma::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = ((mask1 >> (cc * 16 + j)) & 1ull) ? v[j] : 0.0f;
-        store16<NP>(sm.r0, kPlaneH, HH, row, c0, v);
+        for (int j = 0; j < 16; ++j) v[j] = ((mask1 >> (cc * 16 + j)) & 1u) ? v[j] : 0.0f;
+        store16<NP>(sm.r0, row, c0, v);
         float vs[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) vs[j] = v[j];
         const float s1 = colsum16(vs);
         if ((lane & 1) == 0) sm.red[2][warp][cc * 16 + ((lane >> 1) & 15)] = s1;
     }
-    // ---- stage 4: X image -> R1 (dz2 is no longer read) ----
-    build_x<NP>(sm.r1, a.states, a.stride, row0, B, S);
+    if (!xi) build_x(sm.r1, NP, a.states, a.stride, row0, B, S);
     umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
+    if (xi) wait_load();
     // ---- G5: dW1 = dz1^T . X ----
     if (tid == 0) {
         umma::fence_after_sync();
@@ -405,36 +396,33 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         umma::commit(&sm.bar_mma);
     }
     for (int c = tid; c < HH; c += kThreads) {
-        const int h2 = c >> 6, cl = c & 63;
+        const int g = c >> 5, cl = c & 31;
         float s1 = 0.0f;
-        for (int qq = 0; qq < 4; ++qq) s1 += sm.red[2][h2 * 4 + qq][cl];
+        for (int qq = 0; qq < 4; ++qq) s1 += sm.red[2][g * 4 + qq][cl];
         part[off.b1 + c] = s1;
     }
     wait_mma();
 
     // ---- dW2 (lane = output unit, 128 columns) and dW1 (lane = unit, 64 columns) ----
     {
-        float* dst = part + off.w2 + (int64_t)row * HH + hh * 64;
+        float* dst = part + off.w2 + (int64_t)row * HH + cg * 32;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
             float v[16];
-            umma::tmem_ld16(tq + TM_DW2 + (uint32_t)(hh * 64 + cc * 16), v);
+            umma::tmem_ld16(tq + TM_DW2 + (uint32_t)(cg * 32 + cc * 16), v);
             umma::tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 16; j += 4)
                 *reinterpret_cast<float4*>(dst + cc * 16 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
         }
+        const int c0 = cg * 16;
+        float v[16];
+        umma::tmem_ld16(tq + TM_DW1 + (uint32_t)c0, v);
+        umma::tmem_ld_wait();
         float* d1 = part + off.w1 + (int64_t)row * S;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            const int c0 = hh * 32 + cc * 16;
-            float v[16];
-            umma::tmem_ld16(tq + TM_DW1 + (uint32_t)c0, v);
-            umma::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                if (c0 + j < S) d1[c0 + j] = v[j];
-        }
+        for (int j = 0; j < 16; ++j)
+            if (c0 + j < S) d1[c0 + j] = v[j];
     }
     if (!ok && tid == 0) atomicAdd(a.status + OFRL_STAT_TIMEOUT, 1);
     umma::fence_before_sync();
@@ -443,71 +431,64 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
 }
 
 // Pack W1 ([H][S] -> [128 x 64] image) and W2 ([H][H] -> [128 x 128] image)
-// of every network into NP bf16 planes each, for the tensor-core kernel.
-template <int NP>
-__global__ void pack_weights_kernel(const VnetLaunch a, uint8_t* __restrict__ img, int64_t img_stride) {
+// of every network into NP bf16 planes each (standalone V forward/backward;
+// the fused step packs inside the relabel launch).
+__global__ void pack_weights_kernel(const VnetLaunch a, uint8_t* __restrict__ img, int np) {
     const int net = blockIdx.y;
     const int S = a.state_dim;
     const Offsets off = offsets_of(S, HH);
     const float* __restrict__ prm = a.params[net];
-    uint8_t* w1i = img + (int64_t)net * img_stride;
-    uint8_t* w2i = w1i + (uint32_t)NP * kPlaneX;
-    const int n1 = HH * KX, n2 = HH * HH;
+    uint8_t* w1i = img + (int64_t)net * tc::weight_image_bytes();
+    uint8_t* w2i = w1i + 3 * kPlaneX;
+    const int n1 = HH * (KX / 4), n2 = HH * (HH / 4);
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n1 + n2; e += gridDim.x * blockDim.x) {
-        float x;
-        uint8_t* base;
-        uint32_t plane, o;
+        float x[4];
         if (e < n1) {
-            const int r = e / KX, c = e % KX;
-            x = c < S ? __ldg(prm + off.w1 + (int64_t)r * S + c) : 0.0f;
-            base = w1i; plane = kPlaneX; o = img_off(r, c, KX);
+            const int r = e / (KX / 4), c = 4 * (e % (KX / 4));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) x[j] = c + j < S ? __ldg(prm + off.w1 + (int64_t)r * S + c + j) : 0.0f;
+            tc::put4(w1i, kPlaneX, np, KX, r, c, x);
         } else {
-            const int f = e - n1, r = f / HH, c = f % HH;
-            x = __ldg(prm + off.w2 + (int64_t)r * HH + c);
-            base = w2i; plane = kPlaneH; o = img_off(r, c, HH);
-        }
-        __nv_bfloat16 t0, t1, t2;
-        if (NP == 3) umma::split_bf16x3(x, t0, t1, t2);
-        else t0 = __float2bfloat16_rn(x);
-        *reinterpret_cast<__nv_bfloat16*>(base + o) = t0;
-        if (NP == 3) {
-            *reinterpret_cast<__nv_bfloat16*>(base + plane + o) = t1;
-            *reinterpret_cast<__nv_bfloat16*>(base + 2 * plane + o) = t2;
+            const int f = e - n1, r = f / (HH / 4), c = 4 * (f % (HH / 4));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) x[j] = __ldg(prm + off.w2 + (int64_t)r * HH + c + j);
+            tc::put4(w2i, kPlaneH, np, HH, r, c, x);
         }
     }
 }
 
 template <int NP>
-cudaError_t launch_np(const VnetLaunch& a, uint8_t* img, int64_t img_stride, cudaStream_t st) {
-    pack_weights_kernel<NP><<<dim3(48, a.n_nets), 256, 0, st>>>(a, img, img_stride);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+cudaError_t launch_np(const VnetLaunch& a, const uint8_t* wimg, cudaStream_t st) {
     auto kern = vnet_tc_kernel<NP>;
-    const size_t smem = sizeof(TcSmem) + 1024;
+    const size_t smem = sizeof(TcSmem);
     static bool configured = false;
     if (!configured) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
     const dim3 grid((a.batch + TM - 1) / TM, a.n_nets);
-    kern<<<grid, kThreads, smem, st>>>(a, img, img, img_stride);
+    kern<<<grid, kThreads, smem, st>>>(a, wimg);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-int64_t vnet_tc_image_bytes() { return 3 * (int64_t)(kPlaneX + kPlaneH); }
+int64_t vnet_tc_image_bytes() { return tc::weight_image_bytes(); }
 
 bool vnet_tc_supported(const VnetLaunch& a) {
     return a.hidden == HH && a.state_dim <= KX && (a.stride & 3) == 0 &&
            (reinterpret_cast<uintptr_t>(a.states) & 15) == 0;
 }
 
-cudaError_t launch_vnet_tc(const VnetLaunch& a, uint8_t* img, cudaStream_t st) {
+cudaError_t launch_vnet_tc_pack(const VnetLaunch& a, uint8_t* img, cudaStream_t st) {
+    pack_weights_kernel<<<dim3(32, a.n_nets), 256, 0, st>>>(a, img, a.prec == OFRL_PREC_BF16 ? 1 : 3);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_vnet_tc(const VnetLaunch& a, const uint8_t* img, cudaStream_t st) {
     if (a.batch <= 0) return cudaSuccess;
-    const int64_t stride = vnet_tc_image_bytes();
-    return a.prec == OFRL_PREC_BF16 ? launch_np<1>(a, img, stride, st) : launch_np<3>(a, img, stride, st);
+    return a.prec == OFRL_PREC_BF16 ? launch_np<1>(a, img, st) : launch_np<3>(a, img, st);
 }
 
 }  // namespace ofrl
