@@ -99,6 +99,54 @@ __device__ __forceinline__ float clip_scale(float n, float c) {
     return (n > c && n > 0.0f) ? c / n : 1.0f;
 }
 
+// Programmatic dependent launch: a kernel launched with launch_pdl may start
+// while the previous kernel in the stream finishes; pdl_wait() blocks until
+// that kernel has completed and its writes are visible (a no-op when there is
+// no such kernel), so everything that reads or writes global memory comes
+// after it.  pdl_trigger() lets the next kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Every kernel of the library asks for the largest shared-memory carveout,
+// so consecutive kernels never make an SM reconfigure its L1 / shared split
+// (the tensor-core kernel needs ~200 KB of shared memory).
+template <typename K>
+inline cudaError_t set_max_shared_carveout(K kernel) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                (int)cudaSharedmemCarveoutMaxShared);
+}
+
+template <typename Arg>
+inline cudaError_t launch_pdl(void (*kernel)(Arg), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Arg arg) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, arg);
+}
+
+template <typename Arg0, typename Arg1>
+inline cudaError_t launch_pdl(void (*kernel)(Arg0, Arg1), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Arg0 a0, Arg1 a1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a0, a1);
+}
+
 inline int64_t n_params_of(int s, int h) {
     return (int64_t)h * s + h + (int64_t)h * h + h + h + 1;
 }

@@ -83,6 +83,8 @@ __device__ void pack_weights(const HerLaunch& a) {
 }
 
 __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerLaunch a) {
+    pdl_trigger();
+    pdl_wait();
     if ((int)blockIdx.x >= a.relabel_blocks) {
         pack_weights(a);
         return;
@@ -123,7 +125,7 @@ __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerL
     int donor = -1, bad = 0;
     if (a.strategy == OFRL_HER_RANDOM) {
         if (sub == 0 && her) donor = (int)below(sm64_at(a.seed, ctr | 1ull), (uint64_t)a.capacity);
-    } else if (a.first_her < a.batch) {
+    } else if (__any_sync(kFull, live && her)) {   // warp-uniform: only warps holding a HER row search
         const int k = episode_search(a.episode_ends, a.num_episodes, a.search_rounds, src, sub);
         if (sub == 0 && her) {
             int end = k < a.num_episodes ? __ldg(a.episode_ends + k) : a.capacity;
@@ -142,8 +144,8 @@ __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerL
     donor = __shfl_sync(kFull, donor, 0, kLanesPerRow);
 
     // 3. goal slice from the donor's next state; reward from the fp32 distance.
-    // Every lane of the warp runs the shuffles (normal rows compare a row
-    // with itself and ignore the result).
+    // Every lane of a warp holding a HER row runs the shuffles (a normal row
+    // beside it compares a row with itself and ignores the result).
     const bool goal_lane = has && 4 * sub < a.goal_dim;
     float4 gv = nv;
     if (goal_lane && donor >= 0)
@@ -151,7 +153,8 @@ __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerL
     // distance as the pages' kernel: float accumulator in order d = 0..g-1,
     // each product and sum rounded on its own (no FMA), IEEE sqrt
     float dsq = 0.0f;
-    for (int c = 0; 4 * c < a.goal_dim; ++c) {
+    const bool any_her = __any_sync(kFull, donor >= 0);
+    for (int c = 0; any_her && 4 * c < a.goal_dim; ++c) {
         const float av[4] = {__shfl_sync(kFull, nv.x, c, kLanesPerRow), __shfl_sync(kFull, nv.y, c, kLanesPerRow),
                              __shfl_sync(kFull, nv.z, c, kLanesPerRow), __shfl_sync(kFull, nv.w, c, kLanesPerRow)};
         const float bv[4] = {__shfl_sync(kFull, gv.x, c, kLanesPerRow), __shfl_sync(kFull, gv.y, c, kLanesPerRow),
@@ -204,8 +207,13 @@ cudaError_t launch_her_relabel(const HerLaunch& a_in, cudaStream_t st) {
     const int rows = a.ximg != nullptr ? a.img_rows : a.batch;
     a.relabel_blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
     a.pack_blocks = a.wimg != nullptr ? 48 : 0;
-    her_relabel_kernel<<<a.relabel_blocks + a.pack_blocks, kRelabelThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    static bool configured = false;
+    if (!configured) {
+        const cudaError_t e = set_max_shared_carveout(her_relabel_kernel);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    return launch_pdl(her_relabel_kernel, dim3(a.relabel_blocks + a.pack_blocks), dim3(kRelabelThreads), 0, st, a);
 }
 
 }  // namespace ofrl

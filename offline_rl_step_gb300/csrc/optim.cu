@@ -48,7 +48,7 @@ __device__ __forceinline__ float4 sum_tiles(const float* __restrict__ pp, int64_
     return make_float4(s0.x + s1.x, s0.y + s1.y, s0.z + s1.z, s0.w + s1.w);
 }
 
-__global__ void __launch_bounds__(kRedThreads) reduce_gram_kernel(const ReduceLaunch a) {
+__global__ void __launch_bounds__(kRedThreads, 8) reduce_gram_kernel(const ReduceLaunch a) {
     __shared__ float4 sh[kTileLanes][kElemLanes + 1];
     __shared__ unsigned int ticket;
     const int tid = threadIdx.x, tx = tid % kElemLanes, ty = tid / kElemLanes;
@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(kRedThreads) reduce_gram_kernel(const ReduceLa
     const int net = blockIdx.y;
     const int64_t P = a.P;
     const int nsrc = a.n_src;
+    pdl_trigger();
+    pdl_wait();
 
     float gacc[kGramPairs];
 #pragma unroll
@@ -109,16 +111,20 @@ __global__ void __launch_bounds__(kRedThreads) reduce_gram_kernel(const ReduceLa
         }
     }
     float* gp = a.gram_part + ((int64_t)net * gridDim.x + blockIdx.x) * kGramPairs;
-    if (wid == 0) {   // the element lanes (ty == 0) are lanes 0..7 of warp 0; the rest hold zeros
+    // the element lanes (ty == 0) are lanes 0..7 of warp 0; the rest hold zeros.
+    // Lane 0 writes the block's Gram partial and alone fences before taking a
+    // ticket: the last block reads nothing else written in this launch.
+    if (wid == 0) {
 #pragma unroll
         for (int p = 0; p < kGramPairs; ++p) {
             const float s = warp_sum(gacc[p]);
             if (lane == 0) gp[p] = s;
         }
+        if (lane == 0) {
+            __threadfence();
+            ticket = atomicAdd(a.counter + net, 1u);
+        }
     }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) ticket = atomicAdd(a.counter + net, 1u);
     __syncthreads();
     if (ticket != gridDim.x - 1) return;
 
@@ -190,6 +196,8 @@ __global__ void __launch_bounds__(kRedThreads) reduce_gram_kernel(const ReduceLa
 }
 
 __global__ void __launch_bounds__(256) adam_kernel(const AdamLaunch a) {
+    pdl_trigger();
+    pdl_wait();
     const int net = blockIdx.y;
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     float coef[kMaxSrc] = {1.0f, 0.0f, 0.0f, 0.0f};
@@ -295,15 +303,25 @@ int reduce_grid(int64_t P) {
 
 cudaError_t launch_reduce_gram(const ReduceLaunch& a, cudaStream_t st) {
     const dim3 grid(reduce_grid(a.P), a.n_nets);
-    reduce_gram_kernel<<<grid, kRedThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    static bool configured = false;
+    if (!configured) {
+        const cudaError_t e = set_max_shared_carveout(reduce_gram_kernel);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    return launch_pdl(reduce_gram_kernel, grid, dim3(kRedThreads), 0, st, a);
 }
 
 cudaError_t launch_adam(const AdamLaunch& a, cudaStream_t st) {
     if (a.n <= 0) return cudaSuccess;
     const dim3 grid((unsigned)((a.n + 255) / 256), a.n_nets);
-    adam_kernel<<<grid, 256, 0, st>>>(a);
-    return cudaGetLastError();
+    static bool configured = false;
+    if (!configured) {
+        const cudaError_t e = set_max_shared_carveout(adam_kernel);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    return launch_pdl(adam_kernel, grid, dim3(256), 0, st, a);
 }
 
 cudaError_t launch_combine(const CombineLaunch& a, cudaStream_t st) {

@@ -151,6 +151,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
         : "memory");
 }
 
+// Bulk asynchronous copy shared -> global (16-byte aligned, size a multiple
+// of 16), tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void bulk_s2g(void* dst_gmem, const void* src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst_gmem),
+                 "r"(smem_u32(src_smem)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk copy of this thread has finished reading its
+// shared-memory source (the writes complete before the grid does).
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 // fp32 -> three bf16 terms x = b0 + b1 + b2 (each the nearest bf16 of what is
 // left); the sum carries 24 significand bits, the whole fp32 significand.
 __device__ __forceinline__ void split_bf16x3(float x, __nv_bfloat16& b0, __nv_bfloat16& b1, __nv_bfloat16& b2) {

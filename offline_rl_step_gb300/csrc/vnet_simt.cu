@@ -143,6 +143,8 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_fwd_bwd_kernel(const VnetLau
     const float tau = a.tau[net];
     const int row0 = tile * TM;
     float* part = a.partials + (int64_t)net * a.net_partial_stride + (int64_t)tile * a.part_stride;
+    pdl_trigger();
+    pdl_wait();
 
     // ---- state tile (zero rows past the batch, zero columns past S) ----
     for (int e = tid; e < TM * kXStride; e += kThreads) {
@@ -329,8 +331,7 @@ cudaError_t launch_h(const VnetLaunch& a, cudaStream_t st) {
         configured = true;
     }
     const dim3 grid((a.batch + TM - 1) / TM, a.n_nets);
-    kern<<<grid, kThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(kThreads), smem, st, a);
 }
 
 }  // namespace

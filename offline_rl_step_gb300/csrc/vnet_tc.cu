@@ -173,6 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         umma::fence_mbar_init();
     }
     if (warp == 0) umma::tmem_alloc(&sm.tmem_slot, kTmemCols);
+    pdl_trigger();
+    pdl_wait();
     for (int i = tid; i < HH; i += kThreads) {
         sm.b1[i] = __ldg(prm + off.b1 + i);
         sm.b2[i] = __ldg(prm + off.b2 + i);
@@ -404,25 +406,43 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     wait_mma();
 
     // ---- dW2 (lane = output unit, 128 columns) and dW1 (lane = unit, 64 columns) ----
+    // Staged in shared memory in their global layout (R0, R1 are free now),
+    // then written by two bulk copies.  A lane writes its 8 float4s in an
+    // order rotated by the lane, so each 8-lane store phase covers all banks.
     {
-        float* dst = part + off.w2 + (int64_t)row * HH + cg * 32;
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            float v[16];
-            umma::tmem_ld16(tq + TM_DW2 + (uint32_t)(cg * 32 + cc * 16), v);
+        float* st2 = reinterpret_cast<float*>(sm.r0);            // [HH][HH]
+        float* st1 = reinterpret_cast<float*>(sm.r1);            // [HH][S]
+        {
+            float w[32];
+            umma::tmem_ld16(tq + TM_DW2 + (uint32_t)(cg * 32), *reinterpret_cast<float(*)[16]>(w));
+            umma::tmem_ld16(tq + TM_DW2 + (uint32_t)(cg * 32 + 16), *reinterpret_cast<float(*)[16]>(w + 16));
             umma::tmem_ld_wait();
+            float4* dst = reinterpret_cast<float4*>(st2 + row * HH + cg * 32);
 #pragma unroll
-            for (int j = 0; j < 16; j += 4)
-                *reinterpret_cast<float4*>(dst + cc * 16 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            for (int i = 0; i < 8; ++i) {
+                // select float4 number f = (i + lane) & 7 without dynamic register indexing
+                float4 t = make_float4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+                for (int f = 1; f < 8; ++f)
+                    if (((i + lane) & 7) == f) t = make_float4(w[4 * f], w[4 * f + 1], w[4 * f + 2], w[4 * f + 3]);
+                dst[(i + lane) & 7] = t;
+            }
         }
         const int c0 = cg * 16;
         float v[16];
         umma::tmem_ld16(tq + TM_DW1 + (uint32_t)c0, v);
         umma::tmem_ld_wait();
-        float* d1 = part + off.w1 + (int64_t)row * S;
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-            if (c0 + j < S) d1[c0 + j] = v[j];
+            if (c0 + j < S) st1[row * S + c0 + j] = v[j];
+        umma::fence_smem_to_async();
+        __syncthreads();
+        if (tid == 0) {
+            umma::bulk_s2g(part + off.w2, st2, (uint32_t)(HH * HH * 4));
+            umma::bulk_s2g(part + off.w1, st1, (uint32_t)(HH * S * 4));
+            umma::bulk_commit();
+            umma::bulk_wait_read();
+        }
     }
     if (!ok && tid == 0) atomicAdd(a.status + OFRL_STAT_TIMEOUT, 1);
     umma::fence_before_sync();
@@ -463,13 +483,13 @@ cudaError_t launch_np(const VnetLaunch& a, const uint8_t* wimg, cudaStream_t st)
     const size_t smem = sizeof(TcSmem);
     static bool configured = false;
     if (!configured) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess) e = set_max_shared_carveout(kern);
         if (e != cudaSuccess) return e;
         configured = true;
     }
     const dim3 grid((a.batch + TM - 1) / TM, a.n_nets);
-    kern<<<grid, kThreads, smem, st>>>(a, wimg);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(kThreads), smem, st, a, wimg);
 }
 
 }  // namespace
