@@ -31,25 +31,42 @@ __host__ __device__ constexpr int64_t weight_image_bytes() { return 3 * (int64_t
 // Bytes of one state-tile image (3 planes).
 __host__ __device__ constexpr int64_t x_tile_bytes() { return 3 * (int64_t)kPlaneX; }
 
-__device__ __forceinline__ void split3(float x, __nv_bfloat16& b0, __nv_bfloat16& b1, __nv_bfloat16& b2) {
-    b0 = __float2bfloat16_rn(x);
-    const float r1 = x - __bfloat162float(b0);
-    b1 = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(b1);
-    b2 = __float2bfloat16_rn(r2);
+// Two fp32 values to a bf16 pair in one register (round to nearest even):
+// lo in bits 0-15 (the lower address in memory), hi in bits 16-31.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+__device__ __forceinline__ float bf16_lo(uint32_t p) { return __uint_as_float(p << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t p) { return __uint_as_float(p & 0xFFFF0000u); }
+
+// Split a pair of fp32 values into three bf16 pairs, x = x0 + x1 + x2, each
+// term the nearest bf16 of what the previous terms leave.
+__device__ __forceinline__ void split3x2(float a, float b, uint32_t& p0, uint32_t& p1, uint32_t& p2) {
+    p0 = pack_bf16x2(a, b);
+    a -= bf16_lo(p0);
+    b -= bf16_hi(p0);
+    p1 = pack_bf16x2(a, b);
+    a -= bf16_lo(p1);
+    b -= bf16_hi(p1);
+    p2 = pack_bf16x2(a, b);
 }
 
 // Write 4 consecutive values of row r, columns c..c+3 (c a multiple of 4)
 // into an image with C columns and np planes of `plane` bytes.
 __device__ __forceinline__ void put4(uint8_t* img, uint32_t plane, int np, int C, int r, int c, const float (&x)[4]) {
-    __nv_bfloat16 t[3][4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        if (np == 3) split3(x[j], t[0][j], t[1][j], t[2][j]);
-        else t[0][j] = __float2bfloat16_rn(x[j]);
-    }
     const uint32_t o = img_off(r, c, C);
-    for (int p = 0; p < np; ++p) *reinterpret_cast<uint2*>(img + (uint32_t)p * plane + o) = *reinterpret_cast<const uint2*>(&t[p][0]);
+    if (np == 3) {
+        uint32_t a0, a1, a2, b0, b1, b2;
+        split3x2(x[0], x[1], a0, a1, a2);
+        split3x2(x[2], x[3], b0, b1, b2);
+        *reinterpret_cast<uint2*>(img + o) = make_uint2(a0, b0);
+        *reinterpret_cast<uint2*>(img + plane + o) = make_uint2(a1, b1);
+        *reinterpret_cast<uint2*>(img + 2 * plane + o) = make_uint2(a2, b2);
+    } else {
+        *reinterpret_cast<uint2*>(img + o) = make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+    }
 }
 
 }  // namespace tc

@@ -89,17 +89,17 @@ __device__ __forceinline__ void gemm(uint32_t d_tmem, const uint8_t* a, uint32_t
 // Store 16 fp32 values of row r, columns c0..c0+15 into a [128 x 128] image.
 template <int NP>
 __device__ __forceinline__ void store16(uint8_t* img, int r, int c0, const float (&v)[16]) {
-    __nv_bfloat16 t[NP][16];
+    uint32_t t[NP][8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        if constexpr (NP == 3) tc::split3(v[j], t[0][j], t[1][j], t[2][j]);
-        else t[0][j] = __float2bfloat16_rn(v[j]);
+    for (int j = 0; j < 8; ++j) {
+        if constexpr (NP == 3) tc::split3x2(v[2 * j], v[2 * j + 1], t[0][j], t[1][j], t[2][j]);
+        else t[0][j] = tc::pack_bf16x2(v[2 * j], v[2 * j + 1]);
     }
     const uint32_t o0 = tc::img_off(r, c0, HH), o1 = tc::img_off(r, c0 + 8, HH);
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
-        *reinterpret_cast<uint4*>(img + (uint32_t)p * kPlaneH + o0) = *reinterpret_cast<const uint4*>(&t[p][0]);
-        *reinterpret_cast<uint4*>(img + (uint32_t)p * kPlaneH + o1) = *reinterpret_cast<const uint4*>(&t[p][8]);
+        *reinterpret_cast<uint4*>(img + (uint32_t)p * kPlaneH + o0) = make_uint4(t[p][0], t[p][1], t[p][2], t[p][3]);
+        *reinterpret_cast<uint4*>(img + (uint32_t)p * kPlaneH + o1) = make_uint4(t[p][4], t[p][5], t[p][6], t[p][7]);
     }
 }
 
@@ -250,19 +250,22 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     wait_mma();
 
     // ---- epilogue 2: V, loss, dV, policy, dz2 -> R1, dW3 / db2 / db3 ----
-    float z2[32];
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-        float v[16];
-        umma::tmem_ld16(tq + TM_Z2 + (uint32_t)(cg * 32 + cc * 16), v);
-        umma::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) z2[cc * 16 + j] = v[j] + sm.b2[cg * 32 + cc * 16 + j];
-    }
+    // z2 is read from TMEM twice (for V, then for dz2) instead of being kept
+    // in registers across the row reduction.
     {
         float vp = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) vp = fmaf(z2[j] < 0.0f ? 0.0f : z2[j], sm.w3[cg * 32 + j], vp);
+        for (int cc = 0; cc < 2; ++cc) {
+            const int c0 = cg * 32 + cc * 16;
+            float v[16];
+            umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, v);
+            umma::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float z = v[j] + sm.b2[c0 + j];
+                vp = fmaf(z < 0.0f ? 0.0f : z, sm.w3[c0 + j], vp);
+            }
+        }
         sm.vsum[cg][row] = vp;
     }
     __syncthreads();
@@ -287,20 +290,20 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         dv = (-2.0f * w * d) / (float)B;
         if (cg == 0 && a.v_out != nullptr) a.v_out[(int64_t)net * B + b] = V;
         if (cg == 1 && a.pi_out != nullptr) {
+            // three passes over the row of Q: max / argmax, sum of exps, outputs
             const float* qr = a.q + (int64_t)b * NA;
-            float zz[kMaxActions];
             float zmax = -INFINITY, amax = -INFINITY;
             int best = 0;
             for (int k = 0; k < NA; ++k) {
                 const float adv = fminf(fmaxf(__ldg(qr + k) - V, -10.0f), 10.0f);
                 if (adv > amax) { amax = adv; best = k; }
-                zz[k] = a.beta * adv;
-                zmax = fmaxf(zmax, zz[k]);
+                zmax = fmaxf(zmax, a.beta * adv);
             }
             float sum = 0.0f;
-            for (int k = 0; k < NA; ++k) { zz[k] = expf(zz[k] - zmax); sum += zz[k]; }
+            for (int k = 0; k < NA; ++k) sum += expf(a.beta * fminf(fmaxf(__ldg(qr + k) - V, -10.0f), 10.0f) - zmax);
             float* po = a.pi_out + ((int64_t)net * B + b) * NA;
-            for (int k = 0; k < NA; ++k) po[k] = zz[k] / sum;
+            for (int k = 0; k < NA; ++k)
+                po[k] = expf(a.beta * fminf(fmaxf(__ldg(qr + k) - V, -10.0f), 10.0f) - zmax) / sum;
             if (a.argmax_out != nullptr) a.argmax_out[(int64_t)net * B + b] = best;
         }
     }
@@ -311,17 +314,18 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
         const int c0 = cg * 32 + cc * 16;
-        float g[16], hw[16], gs[16];
+        float g[16], hw[16];
+        umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, g);
+        umma::tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-            const float z = z2[cc * 16 + j];
+            const float z = g[j] + sm.b2[c0 + j];
             g[j] = z > 0.0f ? dv * sm.w3[c0 + j] : 0.0f;
             hw[j] = dv * (z < 0.0f ? 0.0f : z);
-            gs[j] = g[j];
         }
         store16<NP>(sm.r1, row, c0, g);
         const float s3 = colsum16(hw);
-        const float s2 = colsum16(gs);
+        const float s2 = colsum16(g);
         if ((lane & 1) == 0) {
             sm.red[0][warp][cc * 16 + ((lane >> 1) & 15)] = s3;
             sm.red[1][warp][cc * 16 + ((lane >> 1) & 15)] = s2;
@@ -380,10 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = ((mask1 >> (cc * 16 + j)) & 1u) ? v[j] : 0.0f;
         store16<NP>(sm.r0, row, c0, v);
-        float vs[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) vs[j] = v[j];
-        const float s1 = colsum16(vs);
+        const float s1 = colsum16(v);
         if ((lane & 1) == 0) sm.red[2][warp][cc * 16 + ((lane >> 1) & 15)] = s1;
     }
     if (!xi) build_x(sm.r1, NP, a.states, a.stride, row0, B, S);
@@ -406,27 +407,22 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     wait_mma();
 
     // ---- dW2 (lane = output unit, 128 columns) and dW1 (lane = unit, 64 columns) ----
-    // Staged in shared memory in their global layout (R0, R1 are free now),
-    // then written by two bulk copies.  A lane writes its 8 float4s in an
-    // order rotated by the lane, so each 8-lane store phase covers all banks.
+    // Staged in shared memory (R0, R1 are free now) and written by bulk
+    // copies: dW2 rows at a padded stride of 132 floats, so the float4
+    // stores of 8 consecutive lanes (8 rows) fall on distinct banks, then one
+    // 512-byte copy per row; dW1 unpadded, one copy of the whole block.
     {
-        float* st2 = reinterpret_cast<float*>(sm.r0);            // [HH][HH]
+        constexpr int kStride2 = HH + 4;
+        float* st2 = reinterpret_cast<float*>(sm.r0);            // [HH][kStride2]
         float* st1 = reinterpret_cast<float*>(sm.r1);            // [HH][S]
-        {
-            float w[32];
-            umma::tmem_ld16(tq + TM_DW2 + (uint32_t)(cg * 32), *reinterpret_cast<float(*)[16]>(w));
-            umma::tmem_ld16(tq + TM_DW2 + (uint32_t)(cg * 32 + 16), *reinterpret_cast<float(*)[16]>(w + 16));
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            float v[16];
+            umma::tmem_ld16(tq + TM_DW2 + (uint32_t)(cg * 32 + cc * 16), v);
             umma::tmem_ld_wait();
-            float4* dst = reinterpret_cast<float4*>(st2 + row * HH + cg * 32);
+            float4* dst = reinterpret_cast<float4*>(st2 + row * kStride2 + cg * 32 + cc * 16);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                // select float4 number f = (i + lane) & 7 without dynamic register indexing
-                float4 t = make_float4(w[0], w[1], w[2], w[3]);
-#pragma unroll
-                for (int f = 1; f < 8; ++f)
-                    if (((i + lane) & 7) == f) t = make_float4(w[4 * f], w[4 * f + 1], w[4 * f + 2], w[4 * f + 3]);
-                dst[(i + lane) & 7] = t;
-            }
+            for (int f = 0; f < 4; ++f) dst[f] = make_float4(v[4 * f], v[4 * f + 1], v[4 * f + 2], v[4 * f + 3]);
         }
         const int c0 = cg * 16;
         float v[16];
@@ -437,9 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
             if (c0 + j < S) st1[row * S + c0 + j] = v[j];
         umma::fence_smem_to_async();
         __syncthreads();
-        if (tid == 0) {
-            umma::bulk_s2g(part + off.w2, st2, (uint32_t)(HH * HH * 4));
-            umma::bulk_s2g(part + off.w1, st1, (uint32_t)(HH * S * 4));
+        if (tid < HH) {
+            umma::bulk_s2g(part + off.w2 + tid * HH, st2 + tid * kStride2, (uint32_t)(HH * 4));
+            if (tid == 0) umma::bulk_s2g(part + off.w1, st1, (uint32_t)(HH * S * 4));
             umma::bulk_commit();
             umma::bulk_wait_read();
         }
