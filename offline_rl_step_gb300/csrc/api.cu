@@ -173,6 +173,13 @@ cudaError_t launch_vnet(ofrl_ctx* ctx, const VnetLaunch& v, bool packed, cudaStr
     return launch_vnet_fwd_bwd(v, st);
 }
 
+// Gradient partials per network that launch_vnet leaves for n_tiles tiles:
+// one per tile from the CUDA-core kernel, one per cluster of tiles from the
+// tensor-core kernel.
+int vnet_parts(const VnetLaunch& v, int n_tiles) {
+    return vnet_tc_supported(v) ? n_tiles / vnet_tc_cluster(n_tiles) : n_tiles;
+}
+
 void bias_corrections(float beta1, float beta2, int32_t t, float* bc1, float* bc2) {
     *bc1 = (float)(1.0 - std::pow((double)beta1, (double)t));
     *bc2 = (float)(1.0 - std::pow((double)beta2, (double)t));
@@ -319,6 +326,7 @@ ofrl_status ofrl_iql_value_fwd_bwd(ofrl_ctx* ctx, const float* params, const flo
     r.n_nets = 1;
     r.P = ctx->n_params;
     r.n_tiles = n_tiles;
+    r.n_parts = vnet_parts(v, n_tiles);
     r.partials = ctx->ws.partials;
     r.part_stride = v.part_stride;
     r.net_partial_stride = v.net_partial_stride;
@@ -529,6 +537,7 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
     r.n_nets = n_nets;
     r.P = P;
     r.n_tiles = (B + tm - 1) / tm;
+    r.n_parts = vnet_parts(v, r.n_tiles);
     r.partials = ctx->ws.partials;
     r.part_stride = v.part_stride;
     r.net_partial_stride = v.net_partial_stride;

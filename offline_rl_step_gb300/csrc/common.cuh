@@ -147,6 +147,27 @@ inline cudaError_t launch_pdl(void (*kernel)(Arg0, Arg1), dim3 grid, dim3 block,
     return cudaLaunchKernelEx(&cfg, kernel, a0, a1);
 }
 
+// launch_pdl with thread-block clusters of `cluster` CTAs along x.
+template <typename Arg0, typename Arg1>
+inline cudaError_t launch_pdl_cluster(void (*kernel)(Arg0, Arg1), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                      unsigned cluster, Arg0 a0, Arg1 a1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, a0, a1);
+}
+
 inline int64_t n_params_of(int s, int h) {
     return (int64_t)h * s + h + (int64_t)h * h + h + h + 1;
 }
@@ -240,6 +261,7 @@ struct VnetLaunch {
     int64_t net_partial_stride;  // floats between networks in partials
     int32_t net_tile_stride;     // floats between networks in tile_loss
     int32_t* status;
+    int32_t cluster;             // tensor-core kernel: tiles per partial (set by its launcher)
 };
 int vnet_tile_rows(int hidden);
 cudaError_t launch_vnet_fwd_bwd(const VnetLaunch& a, cudaStream_t st);
@@ -248,12 +270,17 @@ int64_t vnet_tc_image_bytes();
 bool vnet_tc_supported(const VnetLaunch& a);
 cudaError_t launch_vnet_tc_pack(const VnetLaunch& a, uint8_t* img, cudaStream_t st);
 cudaError_t launch_vnet_tc(const VnetLaunch& a, const uint8_t* img, cudaStream_t st);
+// Tiles whose gradient partials the tensor-core kernel sums into one (a
+// thread-block cluster): the largest of 4, 2, 1 that divides n_tiles and
+// that the device can schedule.  Its partials count is n_tiles / that.
+int vnet_tc_cluster(int n_tiles);
 
 struct ReduceLaunch {
     int n_nets;
     int64_t P;
-    int n_tiles;
-    const float* partials;       // [n_nets][n_tiles][part_stride]; null: g0 is given in src[.][0]
+    int n_tiles;                 // tiles: entries of tile_loss per network
+    int n_parts;                 // gradient partials per network (0: n_tiles)
+    const float* partials;       // [n_nets][n_parts][part_stride]; null: g0 is given in src[.][0]
     int64_t part_stride;
     int64_t net_partial_stride;
     const float* tile_loss;      // [n_nets][n_tiles] or null
@@ -271,7 +298,7 @@ struct ReduceLaunch {
     float* norms_out;            // [n_nets][5] or null: n_0..n_3, combined
     float* loss_out;             // [n_nets] or null
 };
-int reduce_grid(int64_t P);
+int reduce_grid(int64_t P, int elem_lanes);
 cudaError_t launch_reduce_gram(const ReduceLaunch& a, cudaStream_t st);
 
 struct AdamLaunch {

@@ -23,35 +23,39 @@
 namespace ofrl {
 namespace {
 
-constexpr int kRedThreads = 256;   // 8 element lanes (float4) x 32 tile lanes
-constexpr int kElemLanes = 8;
-constexpr int kTileLanes = kRedThreads / kElemLanes;
-constexpr int kRedElems = 4 * kElemLanes;   // elements per block per pass
+// A reduce block is EL element lanes (a float4 each) x 256 / EL partial
+// lanes: EL = 8 for many partials (32 partial lanes), EL = 32 for few.
+constexpr int kRedThreads = 256;
+constexpr int kManyParts = 64;     // more partials than this: EL = 8
 constexpr int kMaxGramBlocks = 2048;
 
-// Sum of the tile partials of element group i4..i4+3 over tiles ty, ty + 32,
+// Sum of the partials of element group i4..i4+3 over partials ty, ty + TL,
 // ... (fixed order; independent 16-byte loads in flight).
-__device__ __forceinline__ float4 sum_tiles(const float* __restrict__ pp, int64_t stride, int n_tiles, int ty,
+template <int TL>
+__device__ __forceinline__ float4 sum_tiles(const float* __restrict__ pp, int64_t stride, int n_parts, int ty,
                                             int64_t i4) {
     float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
     int t = ty;
-    for (; t + kTileLanes < n_tiles; t += 2 * kTileLanes) {
+    for (; t + TL < n_parts; t += 2 * TL) {
         const float4 a = __ldcg(reinterpret_cast<const float4*>(pp + (int64_t)t * stride + i4));
-        const float4 b = __ldcg(reinterpret_cast<const float4*>(pp + (int64_t)(t + kTileLanes) * stride + i4));
+        const float4 b = __ldcg(reinterpret_cast<const float4*>(pp + (int64_t)(t + TL) * stride + i4));
         s0.x += a.x; s0.y += a.y; s0.z += a.z; s0.w += a.w;
         s1.x += b.x; s1.y += b.y; s1.z += b.z; s1.w += b.w;
     }
-    if (t < n_tiles) {
+    if (t < n_parts) {
         const float4 a = __ldcg(reinterpret_cast<const float4*>(pp + (int64_t)t * stride + i4));
         s0.x += a.x; s0.y += a.y; s0.z += a.z; s0.w += a.w;
     }
     return make_float4(s0.x + s1.x, s0.y + s1.y, s0.z + s1.z, s0.w + s1.w);
 }
 
-__global__ void __launch_bounds__(kRedThreads, 8) reduce_gram_kernel(const ReduceLaunch a) {
-    __shared__ float4 sh[kTileLanes][kElemLanes + 1];
+template <int EL>
+__global__ void __launch_bounds__(kRedThreads, EL == 8 ? 5 : 4) reduce_gram_kernel(const ReduceLaunch a) {
+    constexpr int TL = kRedThreads / EL, kRedElems = 4 * EL;
+    __shared__ float4 sh[TL][EL + 1];
     __shared__ unsigned int ticket;
-    const int tid = threadIdx.x, tx = tid % kElemLanes, ty = tid / kElemLanes;
+    const int tid = threadIdx.x, tx = tid % EL, ty = tid / EL;
+    const int n_parts = a.n_parts > 0 ? a.n_parts : a.n_tiles;
     const int lane = tid & 31, wid = tid >> 5;
     const int net = blockIdx.y;
     const int64_t P = a.P;
@@ -74,11 +78,11 @@ __global__ void __launch_bounds__(kRedThreads, 8) reduce_gram_kernel(const Reduc
             // partial rows are padded to a multiple of 32 floats: the float4 at
             // i4 < P stays inside the tile's slice
             const float* pp = a.partials + (int64_t)net * a.net_partial_stride;
-            sh[ty][tx] = i4 < P ? sum_tiles(pp, a.part_stride, a.n_tiles, ty, i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            sh[ty][tx] = i4 < P ? sum_tiles<TL>(pp, a.part_stride, n_parts, ty, i4) : make_float4(0.f, 0.f, 0.f, 0.f);
             __syncthreads();
             if (ty == 0) {
                 float g[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                for (int y = 0; y < kTileLanes; ++y) {
+                for (int y = 0; y < TL; ++y) {
                     const float4 v = sh[y][tx];
                     g[0] += v.x; g[1] += v.y; g[2] += v.z; g[3] += v.w;
                 }
@@ -97,10 +101,11 @@ __global__ void __launch_bounds__(kRedThreads, 8) reduce_gram_kernel(const Reduc
                 if (i4 + e < P) x[0][e] = __ldg(a.src[net][0] + i4 + e);
         }
         if (ty == 0 && nsrc > 0) {
-            for (int k = 1; k < nsrc; ++k)
+#pragma unroll
+            for (int k = 1; k < kMaxSrc; ++k)
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    if (i4 + e < P) x[k][e] = __ldg(a.src[net][k] + i4 + e);
+                    if (k < nsrc && i4 + e < P) x[k][e] = __ldg(a.src[net][k] + i4 + e);
 #pragma unroll
             for (int e = 0; e < 4; ++e)
 #pragma unroll
@@ -111,7 +116,7 @@ __global__ void __launch_bounds__(kRedThreads, 8) reduce_gram_kernel(const Reduc
         }
     }
     float* gp = a.gram_part + ((int64_t)net * gridDim.x + blockIdx.x) * kGramPairs;
-    // the element lanes (ty == 0) are lanes 0..7 of warp 0; the rest hold zeros.
+    // the element lanes (ty == 0) are lanes 0..EL-1 of warp 0; the rest hold zeros.
     // Lane 0 writes the block's Gram partial and alone fences before taking a
     // ticket: the last block reads nothing else written in this launch.
     if (wid == 0) {
@@ -157,37 +162,49 @@ __global__ void __launch_bounds__(kRedThreads, 8) reduce_gram_kernel(const Reduc
         if (lane == 0) tot[p][wid] = s;
     }
     __syncthreads();
+    __shared__ float totals[kGramPairs + 1];
+    if (tid <= kGramPairs) {
+        float s = 0.0f;
+        for (int y = 0; y < kRedThreads / 32; ++y) s += tot[tid][y];
+        totals[tid] = s;
+    }
+    __syncthreads();
     if (tid == 0) {
         float gram[kGramPairs];
-        float loss = 0.0f;
-        for (int p = 0; p <= kGramPairs; ++p) {
-            float s = 0.0f;
-            for (int y = 0; y < kRedThreads / 32; ++y) s += tot[p][y];
-            if (p < kGramPairs) gram[p] = s; else loss = s;
-        }
+#pragma unroll
+        for (int p = 0; p < kGramPairs; ++p) gram[p] = totals[p];
+        const float loss = totals[kGramPairs];
         float* sc = a.scalars + (int64_t)net * kScalars;
+        // (loops unrolled over kMaxSrc with guards, so the arrays stay in registers)
         float coef[kMaxSrc] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float nrm[kMaxSrc] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
         for (int k = 0; k < kMaxSrc; ++k) {
-            const float nk = k < nsrc ? sqrtf(gram[gram_index(k, k)]) : 0.0f;
-            sc[SC_NORM0 + k] = nk;
-            if (k < nsrc) coef[k] = a.alpha[k] * clip_scale(nk, a.budget[k] * a.max_grad_norm);
+            if (k < nsrc) {
+                nrm[k] = sqrtf(gram[gram_index(k, k)]);
+                coef[k] = a.alpha[k] * clip_scale(nrm[k], a.budget[k] * a.max_grad_norm);
+            }
+            sc[SC_NORM0 + k] = nrm[k];
             sc[SC_COEF0 + k] = coef[k];
         }
         // IEEE arithmetic throughout: a NaN source norm gives coefficient 1
         // and a NaN total; an infinite one gives coefficient 0 and 0 * inf =
         // NaN, as the element-wise sum of the clipped sources would.
         float c2 = 0.0f;
-        for (int j = 0; j < nsrc; ++j)
-            for (int k = 0; k < nsrc; ++k) {
+#pragma unroll
+        for (int j = 0; j < kMaxSrc; ++j)
+#pragma unroll
+            for (int k = 0; k < kMaxSrc; ++k) {
                 const int lo = j < k ? j : k, hi = j < k ? k : j;
-                c2 += coef[j] * coef[k] * gram[gram_index(lo, hi)];
+                if (j < nsrc && k < nsrc) c2 += coef[j] * coef[k] * gram[gram_index(lo, hi)];
             }
         const float cn = c2 < 0.0f ? 0.0f : sqrtf(c2);
         sc[SC_COMBINED] = cn;
         const float lmean = loss * a.inv_batch;
         sc[SC_LOSS] = lmean;
         if (a.norms_out != nullptr) {
-            for (int k = 0; k < kMaxSrc; ++k) a.norms_out[net * 5 + k] = sc[SC_NORM0 + k];
+#pragma unroll
+            for (int k = 0; k < kMaxSrc; ++k) a.norms_out[net * 5 + k] = nrm[k];
             a.norms_out[net * 5 + 4] = cn;
         }
         if (a.loss_out != nullptr) a.loss_out[net] = lmean;
@@ -296,20 +313,27 @@ __global__ void __launch_bounds__(256) policy_kernel(const float* __restrict__ q
 
 }  // namespace
 
-int reduce_grid(int64_t P) {
-    const int64_t g = (P + kRedElems - 1) / kRedElems;
+int reduce_grid(int64_t P, int el) {
+    const int64_t g = (P + 4 * el - 1) / (4 * el);
     return (int)(g < kMaxGramBlocks ? (g < 1 ? 1 : g) : kMaxGramBlocks);
 }
 
-cudaError_t launch_reduce_gram(const ReduceLaunch& a, cudaStream_t st) {
-    const dim3 grid(reduce_grid(a.P), a.n_nets);
+template <int EL>
+cudaError_t launch_reduce_el(const ReduceLaunch& a, cudaStream_t st) {
     static bool configured = false;
     if (!configured) {
-        const cudaError_t e = set_max_shared_carveout(reduce_gram_kernel);
+        const cudaError_t e = set_max_shared_carveout(reduce_gram_kernel<EL>);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    return launch_pdl(reduce_gram_kernel, grid, dim3(kRedThreads), 0, st, a);
+    const dim3 grid(reduce_grid(a.P, EL), a.n_nets);
+    return launch_pdl(reduce_gram_kernel<EL>, grid, dim3(kRedThreads), 0, st, a);
+}
+
+cudaError_t launch_reduce_gram(const ReduceLaunch& a, cudaStream_t st) {
+    const int parts = a.n_parts > 0 ? a.n_parts : a.n_tiles;
+    if (a.partials != nullptr && parts <= kManyParts) return launch_reduce_el<32>(a, st);
+    return launch_reduce_el<8>(a, st);
 }
 
 cudaError_t launch_adam(const AdamLaunch& a, cudaStream_t st) {

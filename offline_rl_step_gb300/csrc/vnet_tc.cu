@@ -137,6 +137,33 @@ __device__ __forceinline__ float colsum16(float (&v)[16]) {
     return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
+// Sum, in rank order, of the value at shared address p in CTAs 0..cn-1 of
+// the cluster (cn <= 8); the loads are all issued before the adds.
+__device__ __forceinline__ float4 cluster_sum4(const float* p, int cn) {
+    const uint32_t a = umma::smem_u32(p);
+    float4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        if (k < cn) v[k] = umma::ld_cluster4(umma::cluster_map(a, (uint32_t)k));
+    float4 s = v[0];
+#pragma unroll
+    for (int k = 1; k < 8; ++k)
+        if (k < cn) { s.x += v[k].x; s.y += v[k].y; s.z += v[k].z; s.w += v[k].w; }
+    return s;
+}
+__device__ __forceinline__ float cluster_sum1(const float* p, int cn) {
+    const uint32_t a = umma::smem_u32(p);
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        if (k < cn) v[k] = umma::ld_cluster1(umma::cluster_map(a, (uint32_t)k));
+    float s = v[0];
+#pragma unroll
+    for (int k = 1; k < 8; ++k)
+        if (k < cn) s += v[k];
+    return s;
+}
+
 struct TcSmem {
     uint8_t r0[kRegion];
     uint8_t r1[kRegion];
@@ -144,6 +171,8 @@ struct TcSmem {
     float vsum[4][TM];
     float red[3][kWarps][32];   // per warp column sums: dW3, db2, db1
     float lred[2][4];           // per lane-quarter warp of column group 0: loss, db3
+    __align__(16) float vec[3][HH];   // this tile's dW3, db2, db1
+    float vb3;                  // this tile's db3
     uint64_t bar_mma, bar_load;
     uint32_t tmem_slot;
 };
@@ -161,7 +190,6 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     const Offsets off = offsets_of(S, HH);
     const float* __restrict__ prm = a.params[net];
     const float tau = a.tau[net];
-    float* part = a.partials + (int64_t)net * a.net_partial_stride + (int64_t)tile * a.part_stride;
     const uint8_t* w1i = wimg + (int64_t)net * tc::weight_image_bytes();
     const uint8_t* w2i = w1i + 3 * kPlaneX;
     const uint8_t* xi = a.ximg != nullptr ? a.ximg + (int64_t)tile * NP * kPlaneX : nullptr;
@@ -289,23 +317,48 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         lossp = w * d * d;
         dv = (-2.0f * w * d) / (float)B;
         if (cg == 0 && a.v_out != nullptr) a.v_out[(int64_t)net * B + b] = V;
-        if (cg == 1 && a.pi_out != nullptr) {
-            // three passes over the row of Q: max / argmax, sum of exps, outputs
-            const float* qr = a.q + (int64_t)b * NA;
-            float zmax = -INFINITY, amax = -INFINITY;
-            int best = 0;
-            for (int k = 0; k < NA; ++k) {
-                const float adv = fminf(fmaxf(__ldg(qr + k) - V, -10.0f), 10.0f);
-                if (adv > amax) { amax = adv; best = k; }
-                zmax = fmaxf(zmax, a.beta * adv);
-            }
-            float sum = 0.0f;
-            for (int k = 0; k < NA; ++k) sum += expf(a.beta * fminf(fmaxf(__ldg(qr + k) - V, -10.0f), 10.0f) - zmax);
-            float* po = a.pi_out + ((int64_t)net * B + b) * NA;
-            for (int k = 0; k < NA; ++k)
-                po[k] = expf(a.beta * fminf(fmaxf(__ldg(qr + k) - V, -10.0f), 10.0f) - zmax) / sum;
-            if (a.argmax_out != nullptr) a.argmax_out[(int64_t)net * B + b] = best;
+    }
+    // dz2 -> R1 (what G3 and G4 need); the column sums, the loss partial and
+    // the policy are computed while G3 runs
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        const int c0 = cg * 32 + cc * 16;
+        float g[16];
+        umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, g);
+        umma::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float z = g[j] + sm.b2[c0 + j];
+            g[j] = z > 0.0f ? dv * sm.w3[c0 + j] : 0.0f;
         }
+        store16<NP>(sm.r1, row, c0, g);
+    }
+    umma::fence_smem_to_async();
+    umma::fence_before_sync();
+    __syncthreads();
+    // ---- G3: dW2 = dz2^T . h1 ----
+    if (tid == 0) {
+        umma::fence_after_sync();
+        gemm<NP>(tmem + TM_DW2, sm.r1, kPlaneH, HH, true, sm.r0, kPlaneH, HH, true, TM / 16, HH);
+        umma::commit(&sm.bar_mma);
+    }
+    // (G3 writes the dW2 columns of TMEM; z2 is read again from its own)
+    if (cg == 1 && b < B && a.pi_out != nullptr) {
+        // three passes over the row of Q: max / argmax, sum of exps, outputs
+        const float* qr = a.q + (int64_t)b * NA;
+        float zmax = -INFINITY, amax = -INFINITY;
+        int best = 0;
+        for (int k = 0; k < NA; ++k) {
+            const float adv = fminf(fmaxf(__ldg(qr + k) - V, -10.0f), 10.0f);
+            if (adv > amax) { amax = adv; best = k; }
+            zmax = fmaxf(zmax, a.beta * adv);
+        }
+        float sum = 0.0f;
+        for (int k = 0; k < NA; ++k) sum += expf(a.beta * fminf(fmaxf(__ldg(qr + k) - V, -10.0f), 10.0f) - zmax);
+        float* po = a.pi_out + ((int64_t)net * B + b) * NA;
+        for (int k = 0; k < NA; ++k)
+            po[k] = expf(a.beta * fminf(fmaxf(__ldg(qr + k) - V, -10.0f), 10.0f) - zmax) / sum;
+        if (a.argmax_out != nullptr) a.argmax_out[(int64_t)net * B + b] = best;
     }
     if (cg == 0) {
         const float ls = warp_sum(lossp), ds = warp_sum(dv);
@@ -323,7 +376,6 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
             g[j] = z > 0.0f ? dv * sm.w3[c0 + j] : 0.0f;
             hw[j] = dv * (z < 0.0f ? 0.0f : z);
         }
-        store16<NP>(sm.r1, row, c0, g);
         const float s3 = colsum16(hw);
         const float s2 = colsum16(g);
         if ((lane & 1) == 0) {
@@ -331,28 +383,20 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
             sm.red[1][warp][cc * 16 + ((lane >> 1) & 15)] = s2;
         }
     }
-    umma::fence_smem_to_async();
-    umma::fence_before_sync();
     __syncthreads();
-    // ---- G3: dW2 = dz2^T . h1 ----
-    if (tid == 0) {
-        umma::fence_after_sync();
-        gemm<NP>(tmem + TM_DW2, sm.r1, kPlaneH, HH, true, sm.r0, kPlaneH, HH, true, TM / 16, HH);
-        umma::commit(&sm.bar_mma);
-    }
     // dW3, db2, db3 and the loss partial of the tile (fixed order over warps)
     for (int c = tid; c < HH; c += kThreads) {
         const int g = c >> 5, cl = c & 31;
         float s3 = 0.0f, s2 = 0.0f;
         for (int qq = 0; qq < 4; ++qq) { s3 += sm.red[0][g * 4 + qq][cl]; s2 += sm.red[1][g * 4 + qq][cl]; }
-        part[off.w3 + c] = s3;
-        part[off.b2 + c] = s2;
+        sm.vec[0][c] = s3;
+        sm.vec[1][c] = s2;
     }
     if (tid == 0) {
         const float l = (sm.lred[0][0] + sm.lred[0][1]) + (sm.lred[0][2] + sm.lred[0][3]);
         const float d3 = (sm.lred[1][0] + sm.lred[1][1]) + (sm.lred[1][2] + sm.lred[1][3]);
         a.tile_loss[(int64_t)net * a.net_tile_stride + tile] = l;
-        part[off.b3] = d3;
+        sm.vb3 = d3;
     }
     wait_mma();
     // ---- stage 3: W2 image -> R0 (h1 is no longer read) ----
@@ -384,8 +428,6 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = ((mask1 >> (cc * 16 + j)) & 1u) ? v[j] : 0.0f;
         store16<NP>(sm.r0, row, c0, v);
-        const float s1 = colsum16(v);
-        if ((lane & 1) == 0) sm.red[2][warp][cc * 16 + ((lane >> 1) & 15)] = s1;
     }
     if (!xi) build_x(sm.r1, NP, a.states, a.stride, row0, B, S);
     umma::fence_smem_to_async();
@@ -398,32 +440,44 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         gemm<NP>(tmem + TM_DW1, sm.r0, kPlaneH, HH, true, sm.r1, kPlaneX, KX, true, TM / 16, KX);
         umma::commit(&sm.bar_mma);
     }
+    // db1 while G5 runs (G5 writes the dW1 columns; dh1 is read again from its own)
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        const int c0 = cg * 32 + cc * 16;
+        float v[16];
+        umma::tmem_ld16(tq + TM_Z1 + (uint32_t)c0, v);
+        umma::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = ((mask1 >> (cc * 16 + j)) & 1u) ? v[j] : 0.0f;
+        const float s1 = colsum16(v);
+        if ((lane & 1) == 0) sm.red[2][warp][cc * 16 + ((lane >> 1) & 15)] = s1;
+    }
+    __syncthreads();
     for (int c = tid; c < HH; c += kThreads) {
         const int g = c >> 5, cl = c & 31;
         float s1 = 0.0f;
         for (int qq = 0; qq < 4; ++qq) s1 += sm.red[2][g * 4 + qq][cl];
-        part[off.b1 + c] = s1;
+        sm.vec[2][c] = s1;
     }
     wait_mma();
 
     // ---- dW2 (lane = output unit, 128 columns) and dW1 (lane = unit, 64 columns) ----
-    // Staged in shared memory (R0, R1 are free now) and written by bulk
-    // copies: dW2 rows at a padded stride of 132 floats, so the float4
-    // stores of 8 consecutive lanes (8 rows) fall on distinct banks, then one
-    // 512-byte copy per row; dW1 unpadded, one copy of the whole block.
+    // Staged in shared memory (R0, R1 are free now): dW2 rows at a padded
+    // stride of 132 floats, so the float4 stores of 8 consecutive lanes
+    // (8 rows) fall on distinct banks; dW1 unpadded.
+    constexpr int kStride2 = HH + 4;
+    float* st2 = reinterpret_cast<float*>(sm.r0);            // [HH][kStride2]
+    float* st1 = reinterpret_cast<float*>(sm.r1);            // [HH][S]
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        float v[16];
+        umma::tmem_ld16(tq + TM_DW2 + (uint32_t)(cg * 32 + cc * 16), v);
+        umma::tmem_ld_wait();
+        float4* dst = reinterpret_cast<float4*>(st2 + row * kStride2 + cg * 32 + cc * 16);
+#pragma unroll
+        for (int f = 0; f < 4; ++f) dst[f] = make_float4(v[4 * f], v[4 * f + 1], v[4 * f + 2], v[4 * f + 3]);
+    }
     {
-        constexpr int kStride2 = HH + 4;
-        float* st2 = reinterpret_cast<float*>(sm.r0);            // [HH][kStride2]
-        float* st1 = reinterpret_cast<float*>(sm.r1);            // [HH][S]
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            float v[16];
-            umma::tmem_ld16(tq + TM_DW2 + (uint32_t)(cg * 32 + cc * 16), v);
-            umma::tmem_ld_wait();
-            float4* dst = reinterpret_cast<float4*>(st2 + row * kStride2 + cg * 32 + cc * 16);
-#pragma unroll
-            for (int f = 0; f < 4; ++f) dst[f] = make_float4(v[4 * f], v[4 * f + 1], v[4 * f + 2], v[4 * f + 3]);
-        }
         const int c0 = cg * 16;
         float v[16];
         umma::tmem_ld16(tq + TM_DW1 + (uint32_t)c0, v);
@@ -431,14 +485,49 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
 #pragma unroll
         for (int j = 0; j < 16; ++j)
             if (c0 + j < S) st1[row * S + c0 + j] = v[j];
+    }
+
+    const int cn = a.cluster;
+    float* dst = a.partials + (int64_t)net * a.net_partial_stride + (int64_t)(tile / cn) * a.part_stride;
+    if (cn == 1) {
+        // the tile's partial: one 512-byte bulk copy per dW2 row, one for
+        // dW1, one per vector (all offsets and sizes multiples of 16 bytes)
         umma::fence_smem_to_async();
         __syncthreads();
         if (tid < HH) {
-            umma::bulk_s2g(part + off.w2 + tid * HH, st2 + tid * kStride2, (uint32_t)(HH * 4));
-            if (tid == 0) umma::bulk_s2g(part + off.w1, st1, (uint32_t)(HH * S * 4));
+            umma::bulk_s2g(dst + off.w2 + tid * HH, st2 + tid * kStride2, (uint32_t)(HH * 4));
+            if (tid == 0) umma::bulk_s2g(dst + off.w1, st1, (uint32_t)(HH * S * 4));
+            if (tid == 1) umma::bulk_s2g(dst + off.w3, sm.vec[0], (uint32_t)(HH * 4));
+            if (tid == 2) umma::bulk_s2g(dst + off.b2, sm.vec[1], (uint32_t)(HH * 4));
+            if (tid == 3) umma::bulk_s2g(dst + off.b1, sm.vec[2], (uint32_t)(HH * 4));
+            if (tid == 4) dst[off.b3] = sm.vb3;
             umma::bulk_commit();
             umma::bulk_wait_read();
         }
+    } else {
+        // sum of the cluster's tiles: CTA `rank` of a cluster of cn adds rows
+        // [rank * HH / cn, (rank + 1) * HH / cn) of dW2 and dW1 and the same
+        // entries of dW3, db2, db1 over the cluster's CTAs in rank order,
+        // reading their staging through distributed shared memory, and
+        // stores that slice of the cluster's partial.
+        umma::cluster_sync();
+        const int rank = (int)umma::cluster_rank();
+        const int rows = HH / cn, r0 = rank * rows;
+        for (int e = tid; e < rows * (HH / 4); e += kThreads) {
+            const int r = r0 + e / (HH / 4), c = 4 * (e % (HH / 4));
+            *reinterpret_cast<float4*>(dst + off.w2 + r * HH + c) = cluster_sum4(st2 + r * kStride2 + c, cn);
+        }
+        for (int e = tid; e < rows * S / 4; e += kThreads) {
+            const int i = r0 * S + 4 * e;
+            *reinterpret_cast<float4*>(dst + off.w1 + i) = cluster_sum4(st1 + i, cn);
+        }
+        for (int e = tid; e < 3 * rows; e += kThreads) {
+            const int k = e / rows, c = r0 + e % rows;
+            dst[(k == 0 ? off.w3 : k == 1 ? off.b2 : off.b1) + c] = cluster_sum1(&sm.vec[k][c], cn);
+        }
+        if (rank == 0 && tid == 0) dst[off.b3] = cluster_sum1(&sm.vb3, cn);
+        // no CTA leaves (and frees its shared memory) while a peer still reads it
+        umma::cluster_sync();
     }
     if (!ok && tid == 0) atomicAdd(a.status + OFRL_STAT_TIMEOUT, 1);
     umma::fence_before_sync();
@@ -474,23 +563,72 @@ __global__ void pack_weights_kernel(const VnetLaunch a, uint8_t* __restrict__ im
 }
 
 template <int NP>
-cudaError_t launch_np(const VnetLaunch& a, const uint8_t* wimg, cudaStream_t st) {
-    auto kern = vnet_tc_kernel<NP>;
-    const size_t smem = sizeof(TcSmem);
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess) e = set_max_shared_carveout(kern);
-        if (e != cudaSuccess) return e;
-        configured = true;
+cudaError_t configure_np() {
+    static cudaError_t state = cudaErrorNotReady;
+    if (state == cudaErrorNotReady) {
+        auto kern = vnet_tc_kernel<NP>;
+        state = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(TcSmem));
+        if (state == cudaSuccess) state = set_max_shared_carveout(kern);
     }
-    const dim3 grid((a.batch + TM - 1) / TM, a.n_nets);
-    return launch_pdl(kern, grid, dim3(kThreads), smem, st, a, wimg);
+    return state;
+}
+
+// Largest cluster (4, 2, 1) of 1-CTA-per-SM tiles the device schedules.
+// Clusters of 8 such CTAs do not all fit at once on a 152-SM part (the grid
+// then runs in two waves), and the summation through distributed shared
+// memory costs as much as it saves in the reduction beyond 4.
+constexpr int kMaxCluster = 4;
+int max_cluster() {
+    static int best = 0;
+    if (best == 0) {
+        best = 1;
+        if (configure_np<3>() == cudaSuccess && configure_np<1>() == cudaSuccess) {
+            for (int c = kMaxCluster; c >= 2; c >>= 1) {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3((unsigned)c, 1, 1);
+                cfg.blockDim = dim3(kThreads, 1, 1);
+                cfg.dynamicSmemBytes = sizeof(TcSmem);
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = (unsigned)c;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                int n = 0;
+                if (cudaOccupancyMaxActiveClusters(&n, vnet_tc_kernel<3>, &cfg) == cudaSuccess && n > 0) {
+                    best = c;
+                    break;
+                }
+                cudaGetLastError();
+            }
+        }
+    }
+    return best;
+}
+
+template <int NP>
+cudaError_t launch_np(const VnetLaunch& a, const uint8_t* wimg, cudaStream_t st) {
+    const cudaError_t e = configure_np<NP>();
+    if (e != cudaSuccess) return e;
+    const int n_tiles = (a.batch + TM - 1) / TM;
+    VnetLaunch c = a;
+    c.cluster = vnet_tc_cluster(n_tiles);
+    const dim3 grid((unsigned)n_tiles, a.n_nets);
+    return launch_pdl_cluster(vnet_tc_kernel<NP>, grid, dim3(kThreads), sizeof(TcSmem), st, (unsigned)c.cluster, c,
+                              wimg);
 }
 
 }  // namespace
 
 int64_t vnet_tc_image_bytes() { return tc::weight_image_bytes(); }
+
+int vnet_tc_cluster(int n_tiles) {
+    const int m = max_cluster();
+    for (int c = m; c > 1; c >>= 1)
+        if (n_tiles % c == 0) return c;
+    return 1;
+}
 
 bool vnet_tc_supported(const VnetLaunch& a) {
     return a.hidden == HH && a.state_dim <= KX && (a.stride & 3) == 0 &&
