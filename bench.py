@@ -31,6 +31,11 @@ UNIT = "samples/s"
 SMS = 152
 FP32_LANES_PER_SM = 128
 PROFILE_NOTE = "profiles/ (ncu launch list and per-kernel summaries)"
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
+# kernel, from the ncu --set full capture summarised under profiles/ (taken
+# on the kernel as it stands; a changed kernel drops its entry until it is
+# captured again)
+NCU_TRAFFIC = {("vnet_tc (tcgen05)", "prod_fp32_B16384_S50_H128_A5"): 6944512}
 
 
 def parse():
@@ -170,6 +175,23 @@ def run_reference(args, w):
     }))
 
 
+def max_over_ranks(x, device):
+    """Largest value of the float x over the ranks of the process group (x itself with one process)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, steps, rows_per_rank, ms_max):
+    """Rows per second of the whole job: every rank processed steps x rows_per_rank rows, and the job took
+    the slowest rank's time."""
+    return world * steps * rows_per_rank / (ms_max / 1e3)
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -232,13 +254,9 @@ def run_ours(args, w):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), "cuda")
     ms_per_step = ms / args.steps
-    value = world * args.steps * w.batch / (ms / 1e3)
+    value = whole_job_rate(world, args.steps, w.batch, ms)
 
     # ---- per-phase device time (CUDA events inside the step, same stream) ----
     ofrl.profile_begin(ctx, args.steps)
@@ -264,12 +282,8 @@ def run_ours(args, w):
             norms_h.copy_(norms_out, non_blocking=True)
         e3.record()
         torch.cuda.synchronize()
-        ems = e2.elapsed_time(e3)
-        if world > 1:
-            t = torch.tensor([ems], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * args.steps * w.batch / (ems / 1e3), "unit": UNIT,
+        ems = max_over_ranks(e2.elapsed_time(e3), "cuda")
+        e2e = {"value": whole_job_rate(world, args.steps, w.batch, ems), "unit": UNIT,
                "h2d_bytes_per_step": int(b * a * 4), "d2h_bytes_per_step": int(n * 4 + n * 5 * 4)}
     plan.sync_t()
     status = ctx.poll_status()
@@ -286,11 +300,16 @@ def run_ours(args, w):
         # sustained bf16 peak (the kernel runs inside a long step)
         peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
         ach = alg["vnet_flops"] / dur_s / 1e12
-        mma_mult = 1 if w.prec == "bf16" else 6
+        # MMA work as executed: 128-row tiles, S padded to 64, five GEMMs,
+        # one product per K-step (bf16) or six (fp32 through the split)
+        prods = 1 if w.prec == "bf16" else 6
+        tiles = -(-w.batch // 128)
+        mma = w.n_nets * tiles * prods * 2 * 128 * (2 * w.hidden * 64 + 3 * w.hidden ** 2)
         roof = {"kernel": "vnet_tc (tcgen05)", "bound": "tensor", "achieved": ach, "peak": peak,
-                "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": ach / peak,
+                "traffic": NCU_TRAFFIC.get(("vnet_tc (tcgen05)", w.name)),
                 "peak_source": f"bf16_tflops_sustained ({pk_kind})",
-                "mma_tflops_executed": ach * mma_mult, "mma_frac_executed": ach * mma_mult / peak}
+                "mma_tflops_executed": mma / dur_s / 1e12, "mma_frac_executed": mma / dur_s / 1e12 / peak}
     elif dominant == "vnet":
         fp32_peak = SMS * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
         ach = alg["vnet_flops"] / dur_s / 1e12
