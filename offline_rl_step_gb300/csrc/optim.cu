@@ -19,6 +19,7 @@
 // combined gradient is never stored.  Every reduction is in a fixed order.
 
 #include "common.cuh"
+#include "step_math.cuh"
 
 namespace ofrl {
 namespace {
@@ -173,39 +174,21 @@ __global__ void __launch_bounds__(kRedThreads, EL == 8 ? 5 : 4) reduce_gram_kern
         float gram[kGramPairs];
 #pragma unroll
         for (int p = 0; p < kGramPairs; ++p) gram[p] = totals[p];
-        const float loss = totals[kGramPairs];
+        const NormResult r = finish_norms(gram, totals[kGramPairs], nsrc, a.budget, a.alpha, a.max_grad_norm,
+                                          a.inv_batch);
         float* sc = a.scalars + (int64_t)net * kScalars;
-        // (loops unrolled over kMaxSrc with guards, so the arrays stay in registers)
-        float coef[kMaxSrc] = {0.0f, 0.0f, 0.0f, 0.0f};
-        float nrm[kMaxSrc] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int k = 0; k < kMaxSrc; ++k) {
-            if (k < nsrc) {
-                nrm[k] = sqrtf(gram[gram_index(k, k)]);
-                coef[k] = a.alpha[k] * clip_scale(nrm[k], a.budget[k] * a.max_grad_norm);
-            }
-            sc[SC_NORM0 + k] = nrm[k];
-            sc[SC_COEF0 + k] = coef[k];
+            sc[SC_NORM0 + k] = r.nrm[k];
+            sc[SC_COEF0 + k] = r.coef[k];
         }
-        // IEEE arithmetic throughout: a NaN source norm gives coefficient 1
-        // and a NaN total; an infinite one gives coefficient 0 and 0 * inf =
-        // NaN, as the element-wise sum of the clipped sources would.
-        float c2 = 0.0f;
-#pragma unroll
-        for (int j = 0; j < kMaxSrc; ++j)
-#pragma unroll
-            for (int k = 0; k < kMaxSrc; ++k) {
-                const int lo = j < k ? j : k, hi = j < k ? k : j;
-                if (j < nsrc && k < nsrc) c2 += coef[j] * coef[k] * gram[gram_index(lo, hi)];
-            }
-        const float cn = c2 < 0.0f ? 0.0f : sqrtf(c2);
-        sc[SC_COMBINED] = cn;
-        const float lmean = loss * a.inv_batch;
-        sc[SC_LOSS] = lmean;
+        sc[SC_COMBINED] = r.combined;
+        sc[SC_LOSS] = r.loss;
+        const float lmean = r.loss;
         if (a.norms_out != nullptr) {
 #pragma unroll
-            for (int k = 0; k < kMaxSrc; ++k) a.norms_out[net * 5 + k] = nrm[k];
-            a.norms_out[net * 5 + 4] = cn;
+            for (int k = 0; k < kMaxSrc; ++k) a.norms_out[net * 5 + k] = r.nrm[k];
+            a.norms_out[net * 5 + 4] = r.combined;
         }
         if (a.loss_out != nullptr) a.loss_out[net] = lmean;
         a.counter[net] = 0u;
@@ -233,18 +216,13 @@ __global__ void __launch_bounds__(256) adam_kernel(const AdamLaunch a) {
         float gsum = 0.0f;
         for (int k = 0; k < a.n_src; ++k) gsum = fmaf(coef[k], __ldg(a.src[net][k] + i), gsum);
         const float g = s * gsum;
-        if (!isfinite(g)) {
-            bad = true;
-        } else {
-            float m = a.m[net][i], v = a.v[net][i], p = a.p[net][i];
-            m = a.beta1 * m + (1.0f - a.beta1) * g;
-            v = a.beta2 * v + (1.0f - a.beta2) * g * g;
-            const float mhat = m / a.bc1[net];
-            const float vhat = v / a.bc2[net];
-            p = p - a.lr[net] * (mhat / (sqrtf(vhat) + a.eps) + a.weight_decay * p);
+        float m = a.m[net][i], v = a.v[net][i], p = a.p[net][i];
+        if (adam_element(p, m, v, g, a.beta1, a.beta2, a.eps, a.weight_decay, a.lr[net], a.bc1[net], a.bc2[net])) {
             a.m[net][i] = m;
             a.v[net][i] = v;
             a.p[net][i] = p;
+        } else {
+            bad = true;
         }
     }
     const unsigned ballot = __ballot_sync(0xffffffffu, bad);
