@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerL
         float x[4] = {sv.x, sv.y, sv.z, sv.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            if (!has || 4 * sub + j >= a.state_dim) x[j] = 0.0f;
+            if (!has || 4 * sub + j >= a.state_dim) x[j] = tc::ones_column(4 * sub + j, a.state_dim) ? 1.0f : 0.0f;
         tc::put4(a.ximg + (int64_t)(row / tc::TM) * a.img_planes * tc::kPlaneX, tc::kPlaneX, a.img_planes, tc::KX,
                  row % tc::TM, 4 * sub, x);
     }

@@ -21,6 +21,12 @@ constexpr int KX = 64;      // state columns, zero-padded
 constexpr uint32_t kPlaneH = TM * HH * 2;    // one plane of a [128 x 128] image
 constexpr uint32_t kPlaneX = TM * KX * 2;    // one plane of a [128 x 64] image
 
+// A state-tile image ([128 x 64], S state columns zero-padded) holds 1.0 in
+// its last column when S < 64: the W1 image is zero there, so z1 is
+// unchanged, and the weight-gradient GEMM dz1^T X then also yields the bias
+// gradient sum_rows dz1 in that column.  Rows past the batch stay all zero.
+__host__ __device__ __forceinline__ bool ones_column(int c, int S) { return S < KX && c == KX - 1; }
+
 // Byte offset of element (r, c) inside one plane of an image with C columns.
 __host__ __device__ __forceinline__ uint32_t img_off(int r, int c, int C) {
     return (uint32_t)((r >> 3) * (C >> 3) * 128 + (c >> 3) * 128 + (r & 7) * 16 + (c & 7) * 2);

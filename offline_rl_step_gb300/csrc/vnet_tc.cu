@@ -28,8 +28,9 @@
 // Images arrive by bulk asynchronous copies (cp.async.bulk) on an mbarrier:
 // the weights from the per-step pack, the state tiles from the relabel
 // kernel (or, without those, are built here from the fp32 batch).
-// 16 warps: warp w reads TMEM lane quarter w % 4 (tile rows, or hidden units
-// for the weight gradients) and column group w / 4 (32 columns).
+// 17 warps: warp 0 issues the MMAs and bulk copies; epilogue warp w = 1..16
+// reads TMEM lane quarter w % 4 (tile rows, or hidden units for the weight
+// gradients) and column group (w - 1) / 4 (32 columns).
 
 #include "common.cuh"
 #include "tc_image.cuh"
@@ -44,8 +45,11 @@ using tc::kPlaneH;
 using tc::kPlaneX;
 using tc::TM;
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
+// Warp 0 issues the MMAs and the bulk copies and owns TMEM; warps 1..16 run
+// the epilogues (warp w reads TMEM lane quarter w % 4; column group
+// (w - 1) / 4), so the MMA issue never waits behind epilogue work.
+constexpr int kThreads = 544;
+constexpr int kEpiWarps = 16;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_Z1 = 0, TM_Z2 = 128, TM_DW2 = 256, TM_DW1 = 384;   // TM_Z1 also holds dh1
 constexpr uint32_t kRegion = 3 * kPlaneH;    // 96 KB
@@ -115,7 +119,7 @@ __device__ __forceinline__ void build_x(uint8_t* img, int np, const float* __res
         float x[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            if (c + j >= S) x[j] = 0.0f;
+            if (c + j >= S) x[j] = row0 + r < B && tc::ones_column(c + j, S) ? 1.0f : 0.0f;
         tc::put4(img, kPlaneX, np, KX, r, c, x);
     }
 }
@@ -139,18 +143,6 @@ __device__ __forceinline__ float colsum16(float (&v)[16]) {
 
 // Sum, in rank order, of the value at shared address p in CTAs 0..cn-1 of
 // the cluster (cn <= 8); the loads are all issued before the adds.
-__device__ __forceinline__ float4 cluster_sum4(const float* p, int cn) {
-    const uint32_t a = umma::smem_u32(p);
-    float4 v[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        if (k < cn) v[k] = umma::ld_cluster4(umma::cluster_map(a, (uint32_t)k));
-    float4 s = v[0];
-#pragma unroll
-    for (int k = 1; k < 8; ++k)
-        if (k < cn) { s.x += v[k].x; s.y += v[k].y; s.z += v[k].z; s.w += v[k].w; }
-    return s;
-}
 __device__ __forceinline__ float cluster_sum1(const float* p, int cn) {
     const uint32_t a = umma::smem_u32(p);
     float v[8];
@@ -169,20 +161,26 @@ struct TcSmem {
     uint8_t r1[kRegion];
     float b1[HH], b2[HH], w3[HH];
     float vsum[4][TM];
-    float red[3][kWarps][32];   // per warp column sums: dW3, db2, db1
+    float red[3][kEpiWarps][32];   // per epilogue warp column sums: dW3, db2, db1
     float lred[2][4];           // per lane-quarter warp of column group 0: loss, db3
     __align__(16) float vec[3][HH];   // this tile's dW3, db2, db1
+    float qt[TM * kMaxActions];       // the tile's Q rows [row][action] (or q_taken [row])
+    int32_t act[TM];                  // the tile's actions
+    float vrow[TM];                   // V of each row
     float vb3;                  // this tile's db3
     uint64_t bar_mma, bar_load;
     uint32_t tmem_slot;
 };
+static_assert(sizeof(TcSmem) <= 227 * 1024, "tensor-core kernel shared memory above the per-CTA limit");
 
 template <int NP>
 __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a, const uint8_t* __restrict__ wimg) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     TcSmem& sm = *reinterpret_cast<TcSmem*>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q = warp & 3, cg = warp >> 2;     // TMEM lane quarter, column group (32 columns)
+    const bool epi = warp != 0;                 // an epilogue warp
+    const int ew = warp - 1, et = tid - 32;     // epilogue warp / thread index
+    const int q = warp & 3, cg = (warp - 1) >> 2;   // TMEM lane quarter, column group (32 columns)
     const int row = 32 * q + lane;              // tile row / accumulator lane of this thread
     const int tile = blockIdx.x, net = blockIdx.y;
     const int S = a.state_dim, B = a.batch, NA = a.num_actions;
@@ -203,12 +201,30 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     if (warp == 0) umma::tmem_alloc(&sm.tmem_slot, kTmemCols);
     pdl_trigger();
     pdl_wait();
+    // ---- stage 1: X image -> R0, W1 image -> R1 (issued first; the loads
+    // below overlap it) ----
+    if (tid == 0) {
+        umma::mbar_expect_tx(&sm.bar_load, (xi ? kXBytes : 0u) + kXBytes);
+        if (xi) umma::bulk_g2s(sm.r0, xi, kXBytes, &sm.bar_load);
+        umma::bulk_g2s(sm.r1, w1i, kXBytes, &sm.bar_load);
+    }
     for (int i = tid; i < HH; i += kThreads) {
         sm.b1[i] = __ldg(prm + off.b1 + i);
         sm.b2[i] = __ldg(prm + off.b2 + i);
         sm.w3[i] = __ldg(prm + off.w3 + i);
     }
     const float b3 = __ldg(prm + off.b3);
+    // the tile's actions and Q rows (one contiguous block) for the loss and
+    // the policy, read long before they are needed
+    {
+        const int nrow = B - row0 < TM ? B - row0 : TM;
+        if (a.q != nullptr) {
+            for (int e = tid; e < nrow * NA; e += kThreads) sm.qt[e] = __ldg(a.q + (int64_t)row0 * NA + e);
+            for (int e = tid; e < nrow; e += kThreads) sm.act[e] = __ldg(a.actions + row0 + e);
+        } else {
+            for (int e = tid; e < nrow; e += kThreads) sm.qt[e] = __ldg(a.q_taken + row0 + e);
+        }
+    }
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
@@ -226,12 +242,6 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         ph_load ^= 1u;
     };
 
-    // ---- stage 1: X image -> R0, W1 image -> R1 ----
-    if (tid == 0) {
-        umma::mbar_expect_tx(&sm.bar_load, (xi ? kXBytes : 0u) + kXBytes);
-        if (xi) umma::bulk_g2s(sm.r0, xi, kXBytes, &sm.bar_load);
-        umma::bulk_g2s(sm.r1, w1i, kXBytes, &sm.bar_load);
-    }
     if (!xi) build_x(sm.r0, NP, a.states, a.stride, row0, B, S);
     umma::fence_smem_to_async();
     __syncthreads();
@@ -251,19 +261,21 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
 
     // ---- epilogue 1: h1 = relu(z1 + b1) -> R0; ReLU mask bits kept ----
     uint32_t mask1 = 0;
+    if (epi) {
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-        const int c0 = cg * 32 + cc * 16;
-        float v[16];
-        umma::tmem_ld16(tq + TM_Z1 + (uint32_t)c0, v);
-        umma::tmem_ld_wait();
+        for (int cc = 0; cc < 2; ++cc) {
+            const int c0 = cg * 32 + cc * 16;
+            float v[16];
+            umma::tmem_ld16(tq + TM_Z1 + (uint32_t)c0, v);
+            umma::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const float z = v[j] + sm.b1[c0 + j];
-            v[j] = z < 0.0f ? 0.0f : z;
-            if (v[j] > 0.0f) mask1 |= 1u << (cc * 16 + j);
+            for (int j = 0; j < 16; ++j) {
+                const float z = v[j] + sm.b1[c0 + j];
+                v[j] = z < 0.0f ? 0.0f : z;
+                if (v[j] > 0.0f) mask1 |= 1u << (cc * 16 + j);
+            }
+            store16<NP>(sm.r0, row, c0, v);
         }
-        store16<NP>(sm.r0, row, c0, v);
     }
     umma::fence_smem_to_async();
     umma::fence_before_sync();
@@ -280,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     // ---- epilogue 2: V, loss, dV, policy, dz2 -> R1, dW3 / db2 / db3 ----
     // z2 is read from TMEM twice (for V, then for dz2) instead of being kept
     // in registers across the row reduction.
-    {
+    if (epi) {
         float vp = 0.0f;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
@@ -300,17 +312,17 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     const float V = ((sm.vsum[0][row] + sm.vsum[1][row]) + (sm.vsum[2][row] + sm.vsum[3][row])) + b3;
     const int b = row0 + row;
     float dv = 0.0f, lossp = 0.0f;
-    if (b < B) {
+    if (epi && b < B) {
         float qv;
         if (a.q != nullptr) {
-            int act = __ldg(a.actions + b);
+            int act = sm.act[row];
             if (act < 0 || act >= NA) {
                 if (cg == 0) atomicAdd(a.status + OFRL_STAT_BAD_ACTION, 1);
                 act = 0;
             }
-            qv = __ldg(a.q + (int64_t)b * NA + act);
+            qv = sm.qt[row * NA + act];
         } else {
-            qv = __ldg(a.q_taken + b);
+            qv = sm.qt[row];
         }
         const float d = qv - V;
         const float w = d >= 0.0f ? tau : 1.0f - tau;
@@ -318,20 +330,23 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         dv = (-2.0f * w * d) / (float)B;
         if (cg == 0 && a.v_out != nullptr) a.v_out[(int64_t)net * B + b] = V;
     }
-    // dz2 -> R1 (what G3 and G4 need); the column sums, the loss partial and
-    // the policy are computed while G3 runs
+    if (epi && cg == 0) sm.vrow[row] = V;
+    // dz2 -> R1 (what G3 and G4 need); the column sums and the loss partial
+    // are computed while G3 runs, the policy while G4 runs
+    if (epi) {
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-        const int c0 = cg * 32 + cc * 16;
-        float g[16];
-        umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, g);
-        umma::tmem_ld_wait();
+        for (int cc = 0; cc < 2; ++cc) {
+            const int c0 = cg * 32 + cc * 16;
+            float g[16];
+            umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, g);
+            umma::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const float z = g[j] + sm.b2[c0 + j];
-            g[j] = z > 0.0f ? dv * sm.w3[c0 + j] : 0.0f;
+            for (int j = 0; j < 16; ++j) {
+                const float z = g[j] + sm.b2[c0 + j];
+                g[j] = z > 0.0f ? dv * sm.w3[c0 + j] : 0.0f;
+            }
+            store16<NP>(sm.r1, row, c0, g);
         }
-        store16<NP>(sm.r1, row, c0, g);
     }
     umma::fence_smem_to_async();
     umma::fence_before_sync();
@@ -342,61 +357,9 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         gemm<NP>(tmem + TM_DW2, sm.r1, kPlaneH, HH, true, sm.r0, kPlaneH, HH, true, TM / 16, HH);
         umma::commit(&sm.bar_mma);
     }
-    // (G3 writes the dW2 columns of TMEM; z2 is read again from its own)
-    if (cg == 1 && b < B && a.pi_out != nullptr) {
-        // three passes over the row of Q: max / argmax, sum of exps, outputs
-        const float* qr = a.q + (int64_t)b * NA;
-        float zmax = -INFINITY, amax = -INFINITY;
-        int best = 0;
-        for (int k = 0; k < NA; ++k) {
-            const float adv = fminf(fmaxf(__ldg(qr + k) - V, -10.0f), 10.0f);
-            if (adv > amax) { amax = adv; best = k; }
-            zmax = fmaxf(zmax, a.beta * adv);
-        }
-        float sum = 0.0f;
-        for (int k = 0; k < NA; ++k) sum += expf(a.beta * fminf(fmaxf(__ldg(qr + k) - V, -10.0f), 10.0f) - zmax);
-        float* po = a.pi_out + ((int64_t)net * B + b) * NA;
-        for (int k = 0; k < NA; ++k)
-            po[k] = expf(a.beta * fminf(fmaxf(__ldg(qr + k) - V, -10.0f), 10.0f) - zmax) / sum;
-        if (a.argmax_out != nullptr) a.argmax_out[(int64_t)net * B + b] = best;
-    }
-    if (cg == 0) {
+    if (epi && cg == 0) {
         const float ls = warp_sum(lossp), ds = warp_sum(dv);
         if (lane == 0) { sm.lred[0][q] = ls; sm.lred[1][q] = ds; }
-    }
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-        const int c0 = cg * 32 + cc * 16;
-        float g[16], hw[16];
-        umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, g);
-        umma::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const float z = g[j] + sm.b2[c0 + j];
-            g[j] = z > 0.0f ? dv * sm.w3[c0 + j] : 0.0f;
-            hw[j] = dv * (z < 0.0f ? 0.0f : z);
-        }
-        const float s3 = colsum16(hw);
-        const float s2 = colsum16(g);
-        if ((lane & 1) == 0) {
-            sm.red[0][warp][cc * 16 + ((lane >> 1) & 15)] = s3;
-            sm.red[1][warp][cc * 16 + ((lane >> 1) & 15)] = s2;
-        }
-    }
-    __syncthreads();
-    // dW3, db2, db3 and the loss partial of the tile (fixed order over warps)
-    for (int c = tid; c < HH; c += kThreads) {
-        const int g = c >> 5, cl = c & 31;
-        float s3 = 0.0f, s2 = 0.0f;
-        for (int qq = 0; qq < 4; ++qq) { s3 += sm.red[0][g * 4 + qq][cl]; s2 += sm.red[1][g * 4 + qq][cl]; }
-        sm.vec[0][c] = s3;
-        sm.vec[1][c] = s2;
-    }
-    if (tid == 0) {
-        const float l = (sm.lred[0][0] + sm.lred[0][1]) + (sm.lred[0][2] + sm.lred[0][3]);
-        const float d3 = (sm.lred[1][0] + sm.lred[1][1]) + (sm.lred[1][2] + sm.lred[1][3]);
-        a.tile_loss[(int64_t)net * a.net_tile_stride + tile] = l;
-        sm.vb3 = d3;
     }
     wait_mma();
     // ---- stage 3: W2 image -> R0 (h1 is no longer read) ----
@@ -404,12 +367,86 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         umma::mbar_expect_tx(&sm.bar_load, kW2Bytes);
         umma::bulk_g2s(sm.r0, w2i, kW2Bytes, &sm.bar_load);
     }
+    // column sums for dW3 and db2 while W2 arrives (no MMA runs: TMEM reads
+    // and shuffles beside a running GEMM slow both)
+    if (epi) {
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            const int c0 = cg * 32 + cc * 16;
+            float g[16], hw[16];
+            umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, g);
+            umma::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float z = g[j] + sm.b2[c0 + j];
+                g[j] = z > 0.0f ? dv * sm.w3[c0 + j] : 0.0f;
+                hw[j] = dv * (z < 0.0f ? 0.0f : z);
+            }
+            const float s3 = colsum16(hw);
+            const float s2 = colsum16(g);
+            if ((lane & 1) == 0) {
+                sm.red[0][ew][cc * 16 + ((lane >> 1) & 15)] = s3;
+                sm.red[1][ew][cc * 16 + ((lane >> 1) & 15)] = s2;
+            }
+        }
+    }
+    __syncthreads();
+    // dW3, db2, db3 and the loss partial of the tile (fixed order over warps)
+    for (int c = et; c >= 0 && c < HH; c += kThreads) {
+        const int g = c >> 5, cl = c & 31;
+        float s3 = 0.0f, s2 = 0.0f;
+        for (int qq = 0; qq < 4; ++qq) { s3 += sm.red[0][g * 4 + qq][cl]; s2 += sm.red[1][g * 4 + qq][cl]; }
+        sm.vec[0][c] = s3;
+        sm.vec[1][c] = s2;
+    }
+    if (et == 0) {
+        const float l = (sm.lred[0][0] + sm.lred[0][1]) + (sm.lred[0][2] + sm.lred[0][3]);
+        const float d3 = (sm.lred[1][0] + sm.lred[1][1]) + (sm.lred[1][2] + sm.lred[1][3]);
+        a.tile_loss[(int64_t)net * a.net_tile_stride + tile] = l;
+        sm.vb3 = d3;
+    }
     wait_load();
     // ---- G4: dh1 = dz2 . W2 ----
     if (tid == 0) {
         umma::fence_after_sync();
         gemm<NP>(tmem + TM_Z1, sm.r1, kPlaneH, HH, false, sm.r0, kPlaneH, HH, true, HH / 16, HH);
         umma::commit(&sm.bar_mma);
+    }
+    // the policy while G4 runs: four threads per row (lanes 4r .. 4r + 3 of
+    // a warp), each over actions j, j + 4, ...; max / argmax (lowest index on
+    // ties) and the sum of exponentials combined over the four lanes
+    if (epi && a.pi_out != nullptr) {
+        const int pr = et >> 2, j = et & 3;
+        const int pb = row0 + pr;
+        const bool prow = pb < B;
+        const float Vp = sm.vrow[pr];
+        const float* qr = sm.qt + pr * NA;
+        float zmax = -INFINITY, amax = -INFINITY;
+        int best = NA;
+        if (prow)
+            for (int k = j; k < NA; k += 4) {
+                const float adv = fminf(fmaxf(qr[k] - Vp, -10.0f), 10.0f);
+                if (adv > amax) { amax = adv; best = k; }
+                zmax = fmaxf(zmax, a.beta * adv);
+            }
+#pragma unroll
+        for (int o = 1; o < 4; o <<= 1) {
+            const float oa = __shfl_xor_sync(0xffffffffu, amax, o);
+            const int ob = __shfl_xor_sync(0xffffffffu, best, o);
+            if (oa > amax || (oa == amax && ob < best)) { amax = oa; best = ob; }
+            zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
+        }
+        float sum = 0.0f;
+        if (prow)
+            for (int k = j; k < NA; k += 4) sum += expf(a.beta * fminf(fmaxf(qr[k] - Vp, -10.0f), 10.0f) - zmax);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        if (prow) {
+            float* po = a.pi_out + ((int64_t)net * B + pb) * NA;
+            for (int k = j; k < NA; k += 4)
+                po[k] = expf(a.beta * fminf(fmaxf(qr[k] - Vp, -10.0f), 10.0f) - zmax) / sum;
+            if (j == 0 && a.argmax_out != nullptr) a.argmax_out[(int64_t)net * B + pb] = best < NA ? best : 0;
+        }
     }
     wait_mma();
     // dz2 is no longer read: the X image streams into R1 during epilogue 4
@@ -419,15 +456,17 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     }
 
     // ---- epilogue 4: dz1 = dh1 * 1[z1 > 0] -> R0; db1 ----
+    if (epi) {
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-        const int c0 = cg * 32 + cc * 16;
-        float v[16];
-        umma::tmem_ld16(tq + TM_Z1 + (uint32_t)c0, v);
-        umma::tmem_ld_wait();
+        for (int cc = 0; cc < 2; ++cc) {
+            const int c0 = cg * 32 + cc * 16;
+            float v[16];
+            umma::tmem_ld16(tq + TM_Z1 + (uint32_t)c0, v);
+            umma::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = ((mask1 >> (cc * 16 + j)) & 1u) ? v[j] : 0.0f;
-        store16<NP>(sm.r0, row, c0, v);
+            for (int j = 0; j < 16; ++j) v[j] = ((mask1 >> (cc * 16 + j)) & 1u) ? v[j] : 0.0f;
+            store16<NP>(sm.r0, row, c0, v);
+        }
     }
     if (!xi) build_x(sm.r1, NP, a.states, a.stride, row0, B, S);
     umma::fence_smem_to_async();
@@ -440,24 +479,27 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         gemm<NP>(tmem + TM_DW1, sm.r0, kPlaneH, HH, true, sm.r1, kPlaneX, KX, true, TM / 16, KX);
         umma::commit(&sm.bar_mma);
     }
-    // db1 while G5 runs (G5 writes the dW1 columns; dh1 is read again from its own)
+    // db1: with S < 64 G5 yields it in its last column (the ones column of
+    // the state-tile image); else column sums while G5 runs
+    if (epi && !tc::ones_column(KX - 1, S)) {
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-        const int c0 = cg * 32 + cc * 16;
-        float v[16];
-        umma::tmem_ld16(tq + TM_Z1 + (uint32_t)c0, v);
-        umma::tmem_ld_wait();
+        for (int cc = 0; cc < 2; ++cc) {
+            const int c0 = cg * 32 + cc * 16;
+            float v[16];
+            umma::tmem_ld16(tq + TM_Z1 + (uint32_t)c0, v);
+            umma::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = ((mask1 >> (cc * 16 + j)) & 1u) ? v[j] : 0.0f;
-        const float s1 = colsum16(v);
-        if ((lane & 1) == 0) sm.red[2][warp][cc * 16 + ((lane >> 1) & 15)] = s1;
+            for (int j = 0; j < 16; ++j) v[j] = ((mask1 >> (cc * 16 + j)) & 1u) ? v[j] : 0.0f;
+            const float s1 = colsum16(v);
+            if ((lane & 1) == 0) sm.red[2][ew][cc * 16 + ((lane >> 1) & 15)] = s1;
+        }
     }
     __syncthreads();
-    for (int c = tid; c < HH; c += kThreads) {
+    for (int c = et; c >= 0 && c < HH; c += kThreads) {
         const int g = c >> 5, cl = c & 31;
         float s1 = 0.0f;
         for (int qq = 0; qq < 4; ++qq) s1 += sm.red[2][g * 4 + qq][cl];
-        sm.vec[2][c] = s1;
+        if (!tc::ones_column(KX - 1, S)) sm.vec[2][c] = s1;
     }
     wait_mma();
 
@@ -468,16 +510,18 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     constexpr int kStride2 = HH + 4;
     float* st2 = reinterpret_cast<float*>(sm.r0);            // [HH][kStride2]
     float* st1 = reinterpret_cast<float*>(sm.r1);            // [HH][S]
+    if (epi) {
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-        float v[16];
-        umma::tmem_ld16(tq + TM_DW2 + (uint32_t)(cg * 32 + cc * 16), v);
-        umma::tmem_ld_wait();
-        float4* dst = reinterpret_cast<float4*>(st2 + row * kStride2 + cg * 32 + cc * 16);
+        for (int cc = 0; cc < 2; ++cc) {
+            float v[16];
+            umma::tmem_ld16(tq + TM_DW2 + (uint32_t)(cg * 32 + cc * 16), v);
+            umma::tmem_ld_wait();
+            float4* dst = reinterpret_cast<float4*>(st2 + row * kStride2 + cg * 32 + cc * 16);
 #pragma unroll
-        for (int f = 0; f < 4; ++f) dst[f] = make_float4(v[4 * f], v[4 * f + 1], v[4 * f + 2], v[4 * f + 3]);
+            for (int f = 0; f < 4; ++f) dst[f] = make_float4(v[4 * f], v[4 * f + 1], v[4 * f + 2], v[4 * f + 3]);
+        }
     }
-    {
+    if (epi) {
         const int c0 = cg * 16;
         float v[16];
         umma::tmem_ld16(tq + TM_DW1 + (uint32_t)c0, v);
@@ -485,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
 #pragma unroll
         for (int j = 0; j < 16; ++j)
             if (c0 + j < S) st1[row * S + c0 + j] = v[j];
+        if (c0 + 15 == KX - 1 && tc::ones_column(KX - 1, S)) sm.vec[2][row] = v[15];
     }
 
     const int cn = a.cluster;
@@ -513,13 +558,40 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         umma::cluster_sync();
         const int rank = (int)umma::cluster_rank();
         const int rows = HH / cn, r0 = rank * rows;
-        for (int e = tid; e < rows * (HH / 4); e += kThreads) {
-            const int r = r0 + e / (HH / 4), c = 4 * (e % (HH / 4));
-            *reinterpret_cast<float4*>(dst + off.w2 + r * HH + c) = cluster_sum4(st2 + r * kStride2 + c, cn);
-        }
-        for (int e = tid; e < rows * S / 4; e += kThreads) {
-            const int i = r0 * S + 4 * e;
-            *reinterpret_cast<float4*>(dst + off.w1 + i) = cluster_sum4(st1 + i, cn);
+        // one flat list of float4 items: the dW2 rows, then the dW1 rows of
+        // the slice; every thread issues the loads of up to kItems items from
+        // all cn CTAs before it adds (the loads are latency-bound)
+        constexpr int kItems = 3;
+        const int n2 = rows * (HH / 4), n1 = rows * S / 4;
+        for (int base = tid; base < n2 + n1; base += kItems * kThreads) {
+            float4 v[kItems][4];
+            uint32_t src[kItems];
+            float* dp[kItems];
+#pragma unroll
+            for (int k = 0; k < kItems; ++k) {
+                const int e = base + k * kThreads;
+                if (e < n2) {
+                    const int r = r0 + e / (HH / 4), c = 4 * (e % (HH / 4));
+                    src[k] = umma::smem_u32(st2 + r * kStride2 + c);
+                    dp[k] = dst + off.w2 + r * HH + c;
+                } else {
+                    const int i = r0 * S + 4 * (e - n2);
+                    src[k] = umma::smem_u32(st1 + i);
+                    dp[k] = dst + off.w1 + i;
+                }
+#pragma unroll
+                for (int rk = 0; rk < 4; ++rk)
+                    if (e < n2 + n1 && rk < cn) v[k][rk] = umma::ld_cluster4(umma::cluster_map(src[k], (uint32_t)rk));
+            }
+#pragma unroll
+            for (int k = 0; k < kItems; ++k) {
+                if (base + k * kThreads >= n2 + n1) continue;
+                float4 t = v[k][0];
+#pragma unroll
+                for (int rk = 1; rk < 4; ++rk)
+                    if (rk < cn) { t.x += v[k][rk].x; t.y += v[k][rk].y; t.z += v[k][rk].z; t.w += v[k][rk].w; }
+                *reinterpret_cast<float4*>(dp[k]) = t;
+            }
         }
         for (int e = tid; e < 3 * rows; e += kThreads) {
             const int k = e / rows, c = r0 + e % rows;
