@@ -66,6 +66,7 @@ enum {
     OFRL_STAT_BAD_ACTION = 1,      /* batch actions outside [0, A) (treated as action 0) */
     OFRL_STAT_BAD_INDEX = 2,       /* episode boundary lookups that fell outside the buffer */
     OFRL_STAT_TIMEOUT = 3,         /* bounded device waits that gave up */
+    OFRL_STAT_SANITIZED = 4,       /* gradient-source elements counted as 0 (ofrl_opt.sanitize_sources) */
     OFRL_STAT_WORDS = 8
 };
 
@@ -123,13 +124,20 @@ typedef struct {
 
 /* One V network's trainable state, device buffers of P floats.  `t` is
  * the Adam step counter (host side); ofrl_train_step increments it before
- * the Adam phase, so the first step runs with t = 1. */
+ * the Adam phase, so the first step runs with t = 1.  `target`: the
+ * network's target copy ("GPU IQL + HER Porting Plan", "Rust Integration:
+ * gpu_iql_trainer.rs", target_ema_update: EMA target update for the V
+ * network, Polyak averaging; step 4 of "Where in the Training Loop IQL Gets
+ * Called"), or NULL; when set, ofrl_train_step updates it in the Adam pass,
+ * after the weights: target = (1 - polyak) target + polyak params. */
 typedef struct {
     float* params;
     float* m;
     float* v;
     int32_t t;
     float tau;            /* expectile, 0 < tau < 1 */
+    float* target;        /* device [P] or NULL */
+    float polyak;         /* 0 <= polyak <= 1 (read when target != NULL) */
 } ofrl_vnet;
 
 /* Optimiser and policy hyper-parameters ("GPU IQL + HER Porting Plan",
@@ -141,6 +149,13 @@ typedef struct {
     float beta;           /* advantage temperature */
     float budget[4];      /* budget fractions, primary first (pages: 0.70, 0.15, 0.10, 0.05) */
     float alpha[4];       /* SAXPY coefficient per source, primary first (1.0 each) */
+    /* "DQN Backward-Path NaN Audit": a bound on |weight| applied in the Adam
+     * kernel after each update (0 disables it) ... */
+    float weight_clamp_max_abs;
+    /* ... and the SAXPY's isfinite guard: 1 counts non-finite elements of
+     * every gradient source as 0 (in the source norms, the Gram matrix and
+     * the combination; counted in OFRL_STAT_SANITIZED); 0 leaves them. */
+    int32_t sanitize_sources;
 } ofrl_opt;
 
 /* ---- context -------------------------------------------------------- */
@@ -198,6 +213,26 @@ ofrl_status ofrl_iql_value_fwd_bwd(ofrl_ctx* ctx, const float* params, const flo
                                    float tau, float* v_out, float* loss_out, float* grad_out,
                                    void* stream);
 
+/* V forward only, the network's value of each state ("GPU IQL + HER
+ * Porting Plan", "Rust Integration: gpu_iql_trainer.rs", forward_values:
+ * a forward-only pass of the V network, result kept on the device).
+ * params: device [P] (the online or the target network); states: device
+ * [batch, state_stride] (columns >= S ignored).  v_out: device [batch].
+ * 1 <= batch <= max_batch; asynchronous on `stream`. */
+ofrl_status ofrl_forward_values(ofrl_ctx* ctx, const float* params, const float* states,
+                                int32_t state_stride, int32_t batch, float* v_out, void* stream);
+
+/* IQL bootstrap target for the Q loss ("GPU IQL + HER Porting Plan", "IQL
+ * modifies the target computation": r + gamma V(s') in place of the
+ * max-over-actions target): target_out[b] = rewards[b] + gamma (1 - dones[b])
+ * V(next_states[b]) with V from `params` (terminal rows bootstrap nothing).
+ * rewards, dones: device [batch] (e.g. the relabelled batch's); v_next_out:
+ * device [batch] or NULL, receives V(s').  gamma in [0, 1]. */
+ofrl_status ofrl_iql_target(ofrl_ctx* ctx, const float* params, const float* next_states,
+                            int32_t state_stride, const float* rewards, const float* dones,
+                            int32_t batch, float gamma, float* v_next_out, float* target_out,
+                            void* stream);
+
 /* Expectile loss alone ("IQL (CPU)" item 2): q_taken, v device [batch];
  * loss_out device [1] = mean(w d^2), d = q - v; dv_out device [batch] or
  * NULL: dloss/dv = -2 w d / batch.  batch >= 1. */
@@ -232,10 +267,17 @@ ofrl_status ofrl_budgeted_clip_saxpy(ofrl_ctx* ctx, const float* const* src,
  * or NULL to compute ||g|| here); per element g' = s * g[i]; a non-finite
  * g' leaves p, m, v unchanged and is counted in the status word; else
  * m = b1 m + (1-b1) g', v = b2 v + (1-b2) g'^2, p -= lr (m/(1-b1^t) /
- * (sqrt(v/(1-b2^t)) + eps) + weight_decay p).  t >= 1. */
+ * (sqrt(v/(1-b2^t)) + eps) + weight_decay p), then p clamped to
+ * [-w, w] with w = opt->weight_clamp_max_abs when w > 0.  t >= 1. */
 ofrl_status ofrl_adam_step(ofrl_ctx* ctx, float* p, const float* g, float* m, float* v,
                            int64_t n, int32_t t, const ofrl_opt* opt, const float* grad_norm,
                            void* stream);
+
+/* Polyak (EMA) update of a target network ("GPU IQL + HER Porting Plan",
+ * "Rust Integration: gpu_iql_trainer.rs", target_ema_update):
+ * target[i] = (1 - polyak) target[i] + polyak params[i], i < n.  Device
+ * buffers; 0 <= polyak <= 1.  Needs no context. */
+ofrl_status ofrl_target_ema(const float* params, float* target, int64_t n, float polyak, void* stream);
 
 /* The fused train step: relabel -> per network {V fwd, expectile loss on
  * Q[b, action_b], policy, V bwd -> primary gradient g0; budgeted combine of

@@ -24,7 +24,7 @@ import torch
 
 from . import _abi
 from ._abi import (HER_FINAL, HER_FUTURE, HER_RANDOM, PREC_BF16, PREC_FP32,  # noqa: F401
-                   STAT_BAD_ACTION, STAT_BAD_INDEX, STAT_NONFINITE_GRAD, STAT_TIMEOUT, OfrlError)
+                   STAT_BAD_ACTION, STAT_BAD_INDEX, STAT_NONFINITE_GRAD, STAT_SANITIZED, STAT_TIMEOUT, OfrlError)
 
 STRATEGY = {"final": HER_FINAL, "future": HER_FUTURE, "random": HER_RANDOM}
 PRECISION = {"fp32": PREC_FP32, "bf16": PREC_BF16}
@@ -117,17 +117,25 @@ class Batch:
 
 @dataclass
 class VNet:
-    """One V network's trainable state: params, Adam moments m and v, step t."""
+    """One V network's trainable state: params, Adam moments m and v, step t; optionally a Polyak target copy
+    that train_step moves toward the weights after every update (target = (1 - polyak) target + polyak params)."""
     params: torch.Tensor
     m: torch.Tensor
     v: torch.Tensor
     tau: float
     t: int = 0
+    target: Optional[torch.Tensor] = None
+    polyak: float = 0.0
 
     @classmethod
-    def from_params(cls, params: torch.Tensor, tau: float):
+    def from_params(cls, params: torch.Tensor, tau: float, polyak: Optional[float] = None):
         p = params.detach().to(device="cuda", dtype=F32).contiguous().clone()
-        return cls(p, torch.zeros_like(p), torch.zeros_like(p), float(tau), 0)
+        tgt = p.clone() if polyak is not None else None
+        return cls(p, torch.zeros_like(p), torch.zeros_like(p), float(tau), 0, tgt, float(polyak or 0.0))
+
+    def c(self):
+        return _abi.VNet(_ptr(self.params, F32, "params"), _ptr(self.m, F32, "m"), _ptr(self.v, F32, "v"),
+                         self.t, self.tau, _ptr(self.target, F32, "target"), self.polyak)
 
 
 @dataclass
@@ -141,12 +149,14 @@ class Opt:
     beta: float = 3.0
     budget: Sequence[float] = BUDGET
     alpha: Sequence[float] = (1.0, 1.0, 1.0, 1.0)
+    weight_clamp_max_abs: float = 0.0    # > 0: |weight| bound after every Adam update
+    sanitize_sources: bool = False       # non-finite gradient-source elements count as 0
 
     def c(self):
         b = (C.c_float * 4)(*[float(x) for x in (list(self.budget) + [0.0] * 4)[:4]])
         a = (C.c_float * 4)(*[float(x) for x in (list(self.alpha) + [0.0] * 4)[:4]])
         return _abi.Opt(self.lr, self.beta1, self.beta2, self.eps, self.weight_decay, self.max_grad_norm,
-                        self.beta, b, a)
+                        self.beta, b, a, self.weight_clamp_max_abs, 1 if self.sanitize_sources else 0)
 
 
 class Context:
@@ -178,7 +188,8 @@ class Context:
         words = (C.c_int32 * _abi.STAT_WORDS)()
         _abi.check("ofrl_poll_status", self._lib.ofrl_poll_status(self.handle, _stream(stream), words))
         return {"nonfinite_grad": words[_abi.STAT_NONFINITE_GRAD], "bad_action": words[_abi.STAT_BAD_ACTION],
-                "bad_index": words[_abi.STAT_BAD_INDEX], "timeout": words[_abi.STAT_TIMEOUT]}
+                "bad_index": words[_abi.STAT_BAD_INDEX], "timeout": words[_abi.STAT_TIMEOUT],
+                "sanitized": words[_abi.STAT_SANITIZED]}
 
     def workspace_bytes(self) -> int:
         return int(self._lib.ofrl_workspace_bytes(C.byref(self.shape), self.max_batch, self.max_nets))
@@ -197,6 +208,22 @@ def iql_value_fwd_bwd(ctx: Context, params, states, q_taken, tau: float, v_out, 
         ctx.handle, _ptr(params, F32, "params"), _ptr(states, F32, "states"), states.shape[1], batch,
         _ptr(q_taken, F32, "q_taken"), tau, _ptr(v_out, F32, "v_out"), _ptr(loss_out, F32, "loss_out"),
         _ptr(grad_out, F32, "grad_out"), _stream(stream)))
+
+
+def forward_values(ctx: Context, params, states, v_out, stream=None):
+    """V(s) of every row of `states` [batch, stride] into v_out [batch] (forward only)."""
+    _abi.check("ofrl_forward_values", ctx._lib.ofrl_forward_values(
+        ctx.handle, _ptr(params, F32, "params"), _ptr(states, F32, "states"), states.shape[1],
+        int(states.shape[0]), _ptr(v_out, F32, "v_out"), _stream(stream)))
+
+
+def iql_target(ctx: Context, params, next_states, rewards, dones, gamma: float, target_out, v_next_out=None,
+               stream=None):
+    """target_out = rewards + gamma (1 - dones) V(next_states); V(s') into v_next_out when given."""
+    _abi.check("ofrl_iql_target", ctx._lib.ofrl_iql_target(
+        ctx.handle, _ptr(params, F32, "params"), _ptr(next_states, F32, "next_states"), next_states.shape[1],
+        _ptr(rewards, F32, "rewards"), _ptr(dones, F32, "dones"), int(next_states.shape[0]), gamma,
+        _ptr(v_next_out, F32, "v_next_out"), _ptr(target_out, F32, "target_out"), _stream(stream)))
 
 
 def noalloc_max_batch(state_dim: int, hidden: int, num_actions: int, prec: str = "fp32") -> int:
@@ -260,8 +287,7 @@ def train_step(ctx: Context, replay: Replay, her: HerConfig, step: int, batch: B
     """One fused step; increments every net's t."""
     r, h, b, o = replay.c(), her.c(), batch.c(), opt.c()
     n_nets = len(nets)
-    cn = (_abi.VNet * n_nets)(*[_abi.VNet(_ptr(x.params, F32, "params"), _ptr(x.m, F32, "m"),
-                                          _ptr(x.v, F32, "v"), x.t, x.tau) for x in nets])
+    cn = (_abi.VNet * n_nets)(*[x.c() for x in nets])
     n_aux = 0 if not aux else len(aux[0])
     aux_arr = None
     if n_aux:
@@ -291,8 +317,7 @@ class StepPlan:
         self._keep = (replay, batch, nets, v_out, pi_out, argmax_out, loss_out, norms_out, grad_out)
         self.r, self.h, self.b, self.o = replay.c(), her.c(), batch.c(), opt.c()
         self.n_nets = len(nets)
-        self.cn = (_abi.VNet * self.n_nets)(*[_abi.VNet(_ptr(x.params, F32), _ptr(x.m, F32), _ptr(x.v, F32),
-                                                        x.t, x.tau) for x in nets])
+        self.cn = (_abi.VNet * self.n_nets)(*[x.c() for x in nets])
         self.n_aux = n_aux
         self.aux_arr = (C.c_void_p * max(1, self.n_nets * n_aux))()
         self.outs = [_ptr(v_out, F32), _ptr(pi_out, F32), _ptr(argmax_out, I32), _ptr(loss_out, F32),
@@ -314,6 +339,14 @@ class StepPlan:
     def sync_t(self):
         for k in range(self.n_nets):
             self.nets[k].t = self.cn[k].t
+
+
+def target_ema(params, target, polyak: float, stream=None):
+    """target = (1 - polyak) target + polyak params, element-wise (Polyak averaging of a target network)."""
+    if params.numel() != target.numel():
+        raise ValueError("params and target differ in size")
+    _abi.check("ofrl_target_ema", _abi.load().ofrl_target_ema(
+        _ptr(params, F32, "params"), _ptr(target, F32, "target"), int(params.numel()), polyak, _stream(stream)))
 
 
 def profile_begin(ctx: Context, max_steps: int):

@@ -8,7 +8,7 @@ LIB_PATH = os.path.join(HERE, "libofrl.so")
 OK, EINVAL, EUNSUPPORTED, ECUDA, ETIMEOUT = 0, -1, -2, -3, -4
 HER_FINAL, HER_FUTURE, HER_RANDOM = 0, 1, 2
 PREC_FP32, PREC_BF16 = 0, 1
-STAT_NONFINITE_GRAD, STAT_BAD_ACTION, STAT_BAD_INDEX, STAT_TIMEOUT, STAT_WORDS = 0, 1, 2, 3, 8
+STAT_NONFINITE_GRAD, STAT_BAD_ACTION, STAT_BAD_INDEX, STAT_TIMEOUT, STAT_SANITIZED, STAT_WORDS = 0, 1, 2, 3, 4, 8
 
 vp = C.c_void_p
 
@@ -35,13 +35,15 @@ class VShape(C.Structure):
 
 
 class VNet(C.Structure):
-    _fields_ = [("params", vp), ("m", vp), ("v", vp), ("t", C.c_int32), ("tau", C.c_float)]
+    _fields_ = [("params", vp), ("m", vp), ("v", vp), ("t", C.c_int32), ("tau", C.c_float), ("target", vp),
+                ("polyak", C.c_float)]
 
 
 class Opt(C.Structure):
     _fields_ = [("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float), ("eps", C.c_float),
                 ("weight_decay", C.c_float), ("max_grad_norm", C.c_float), ("beta", C.c_float),
-                ("budget", C.c_float * 4), ("alpha", C.c_float * 4)]
+                ("budget", C.c_float * 4), ("alpha", C.c_float * 4), ("weight_clamp_max_abs", C.c_float),
+                ("sanitize_sources", C.c_int32)]
 
 
 # name -> (restype, argtypes)
@@ -53,10 +55,13 @@ SIGNATURES = {
     "ofrl_workspace_bytes": (C.c_int64, [C.POINTER(VShape), C.c_int32, C.c_int32]),
     "ofrl_her_relabel": (C.c_int32, [vp, C.POINTER(Replay), C.POINTER(HerCfg), C.c_uint64, C.POINTER(Batch), vp]),
     "ofrl_iql_value_fwd_bwd": (C.c_int32, [vp, vp, vp, C.c_int32, C.c_int32, vp, C.c_float, vp, vp, vp, vp]),
+    "ofrl_forward_values": (C.c_int32, [vp, vp, vp, C.c_int32, C.c_int32, vp, vp]),
+    "ofrl_iql_target": (C.c_int32, [vp, vp, vp, C.c_int32, vp, vp, C.c_int32, C.c_float, vp, vp, vp]),
     "ofrl_expectile_loss": (C.c_int32, [vp, vp, vp, C.c_int32, C.c_float, vp, vp, vp]),
     "ofrl_adv_weighted_policy": (C.c_int32, [vp, vp, vp, C.c_int32, C.c_int32, C.c_float, vp, vp, vp]),
     "ofrl_budgeted_clip_saxpy": (C.c_int32, [vp, C.POINTER(vp), C.POINTER(C.c_float), C.POINTER(C.c_float),
                                              C.c_int32, C.c_int64, C.c_float, vp, vp, vp]),
+    "ofrl_target_ema": (C.c_int32, [vp, vp, C.c_int64, C.c_float, vp]),
     "ofrl_adam_step": (C.c_int32, [vp, vp, vp, vp, vp, C.c_int64, C.c_int32, C.POINTER(Opt), vp, vp]),
     "ofrl_train_step": (C.c_int32, [vp, C.POINTER(Replay), C.POINTER(HerCfg), C.c_uint64, C.POINTER(Batch), vp,
                                     C.POINTER(VNet), C.c_int32, C.POINTER(Opt), C.POINTER(vp), C.c_int32,

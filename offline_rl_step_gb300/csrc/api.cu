@@ -104,6 +104,8 @@ ofrl_status check_opt(const ofrl_opt* o) {
     if (!(o->max_grad_norm > 0.0f)) return OFRL_EINVAL;   // also rejects NaN
     if (!(o->beta1 >= 0.0f && o->beta1 < 1.0f) || !(o->beta2 >= 0.0f && o->beta2 < 1.0f)) return OFRL_EINVAL;
     if (!std::isfinite(o->lr) || !std::isfinite(o->eps) || !std::isfinite(o->weight_decay)) return OFRL_EINVAL;
+    if (!(o->weight_clamp_max_abs >= 0.0f)) return OFRL_EINVAL;          // also rejects NaN
+    if (o->sanitize_sources != 0 && o->sanitize_sources != 1) return OFRL_EINVAL;
     return OFRL_OK;
 }
 
@@ -285,6 +287,53 @@ ofrl_status ofrl_her_relabel(ofrl_ctx* ctx, const ofrl_replay* replay, const ofr
     return cuda_status(launch_her_relabel(a, static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+
+ofrl_status value_forward(ofrl_ctx* ctx, const float* params, const float* states, int32_t state_stride,
+                          int32_t batch, const float* rewards, const float* dones, float gamma, float* v_out,
+                          float* target_out, void* stream) {
+    ofrl_status s = check_ctx(ctx);
+    if (s != OFRL_OK) return s;
+    const ofrl_vshape& sh = ctx->shape;
+    if (!params || !states || (!v_out && !target_out)) return OFRL_EINVAL;
+    if (batch < 1 || batch > ctx->max_batch || state_stride < sh.state_dim) return OFRL_EINVAL;
+    VnetLaunch v;
+    std::memset(&v, 0, sizeof(v));
+    v.params[0] = params;
+    v.n_nets = 1;
+    v.state_dim = sh.state_dim;
+    v.hidden = sh.hidden;
+    v.num_actions = sh.num_actions;
+    v.prec = sh.prec;
+    v.states = states;
+    v.stride = state_stride;
+    v.batch = batch;
+    v.v_out = v_out;
+    v.rewards = rewards;
+    v.dones = dones;
+    v.gamma = gamma;
+    v.target_out = target_out;
+    v.status = ctx->ws.status;
+    return cuda_status(launch_vnet_forward(v, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+ofrl_status ofrl_forward_values(ofrl_ctx* ctx, const float* params, const float* states, int32_t state_stride,
+                                int32_t batch, float* v_out, void* stream) {
+    if (v_out == nullptr) return OFRL_EINVAL;
+    return value_forward(ctx, params, states, state_stride, batch, nullptr, nullptr, 0.0f, v_out, nullptr, stream);
+}
+
+ofrl_status ofrl_iql_target(ofrl_ctx* ctx, const float* params, const float* next_states, int32_t state_stride,
+                            const float* rewards, const float* dones, int32_t batch, float gamma, float* v_next_out,
+                            float* target_out, void* stream) {
+    if (!rewards || !dones || !target_out) return OFRL_EINVAL;
+    if (!(gamma >= 0.0f && gamma <= 1.0f)) return OFRL_EINVAL;
+    return value_forward(ctx, params, next_states, state_stride, batch, rewards, dones, gamma, v_next_out,
+                         target_out, stream);
+}
+
 ofrl_status ofrl_iql_value_fwd_bwd(ofrl_ctx* ctx, const float* params, const float* states,
                                    int32_t state_stride, int32_t batch, const float* q_taken, float tau,
                                    float* v_out, float* loss_out, float* grad_out, void* stream) {
@@ -404,6 +453,11 @@ ofrl_status ofrl_budgeted_clip_saxpy(ofrl_ctx* ctx, const float* const* src, con
     return cuda_status(launch_combine(c, st));
 }
 
+ofrl_status ofrl_target_ema(const float* params, float* target, int64_t n, float polyak, void* stream) {
+    if (!params || !target || n < 1 || !(polyak >= 0.0f && polyak <= 1.0f)) return OFRL_EINVAL;
+    return cuda_status(launch_target_ema(params, target, n, polyak, static_cast<cudaStream_t>(stream)));
+}
+
 ofrl_status ofrl_adam_step(ofrl_ctx* ctx, float* p, const float* g, float* m, float* v, int64_t n, int32_t t,
                            const ofrl_opt* opt, const float* grad_norm, void* stream) {
     ofrl_status s = check_ctx(ctx);
@@ -428,6 +482,7 @@ ofrl_status ofrl_adam_step(ofrl_ctx* ctx, float* p, const float* g, float* m, fl
     a.weight_decay = opt->weight_decay;
     a.max_grad_norm = opt->max_grad_norm;
     a.status = ctx->ws.status;
+    a.clamp = opt->weight_clamp_max_abs;
     if (grad_norm == nullptr) {
         ReduceLaunch r;
         std::memset(&r, 0, sizeof(r));
@@ -468,6 +523,7 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
     for (int k = 0; k < n_nets; ++k) {
         if (!nets[k].params || !nets[k].m || !nets[k].v || nets[k].t < 0) return OFRL_EINVAL;
         if (!(nets[k].tau >= 0.0f && nets[k].tau <= 1.0f)) return OFRL_EINVAL;
+        if (nets[k].target != nullptr && !(nets[k].polyak >= 0.0f && nets[k].polyak <= 1.0f)) return OFRL_EINVAL;
         for (int j = 0; j < n_aux; ++j)
             if (aux_src[k * n_aux + j] == nullptr) return OFRL_EINVAL;
     }
@@ -560,6 +616,8 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
     r.counter = ctx->ws.counter;
     r.norms_out = norms_out;
     r.loss_out = loss_out;
+    r.sanitize = opt->sanitize_sources;
+    r.status = ctx->ws.status;
     e = launch_reduce_gram(r, st);
     if (e != cudaSuccess) return OFRL_ECUDA;
     prof_mark(ctx, 3, st);
@@ -577,7 +635,11 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
         for (int j = 0; j <= n_aux; ++j) a.src[k][j] = r.src[k][j];
         a.lr[k] = opt->lr;
         bias_corrections(opt->beta1, opt->beta2, nets[k].t, &a.bc1[k], &a.bc2[k]);
+        a.target[k] = nets[k].target;
+        a.polyak[k] = nets[k].polyak;
     }
+    a.sanitize = opt->sanitize_sources;
+    a.clamp = opt->weight_clamp_max_abs;
     a.n_src = 1 + n_aux;
     a.scalars = ctx->ws.scalars;
     a.beta1 = opt->beta1;

@@ -262,9 +262,17 @@ struct VnetLaunch {
     int32_t net_tile_stride;     // floats between networks in tile_loss
     int32_t* status;
     int32_t cluster;             // tensor-core kernel: tiles per partial (set by its launcher)
+    // forward-only launches (launch_vnet_forward): the IQL target inputs
+    const float* rewards;        // [B] or null
+    const float* dones;          // [B] or null
+    float gamma;
+    float* target_out;           // [n_nets, B] or null
 };
 int vnet_tile_rows(int hidden);
 cudaError_t launch_vnet_fwd_bwd(const VnetLaunch& a, cudaStream_t st);
+// V forward only (CUDA cores, every hidden size): v_out and, with target_out,
+// rewards + gamma (1 - dones) V.
+cudaError_t launch_vnet_forward(const VnetLaunch& a, cudaStream_t st);
 // tensor-core kernel (hidden 128): packed weight images per network
 int64_t vnet_tc_image_bytes();
 bool vnet_tc_supported(const VnetLaunch& a);
@@ -297,6 +305,8 @@ struct ReduceLaunch {
     unsigned int* counter;       // [n_nets]
     float* norms_out;            // [n_nets][5] or null: n_0..n_3, combined
     float* loss_out;             // [n_nets] or null
+    int sanitize;                // 1: non-finite source elements count as 0
+    int32_t* status;             // counts them (OFRL_STAT_SANITIZED) when sanitize
 };
 int reduce_grid(int64_t P, int elem_lanes);
 cudaError_t launch_reduce_gram(const ReduceLaunch& a, cudaStream_t st);
@@ -314,7 +324,12 @@ struct AdamLaunch {
     float lr[kMaxNets], bc1[kMaxNets], bc2[kMaxNets];
     float beta1, beta2, eps, weight_decay, max_grad_norm;
     int32_t* status;
+    int sanitize;                // 1: non-finite source elements count as 0
+    float clamp;                 // > 0: |p| <= clamp after the update
+    float* target[kMaxNets];     // Polyak target per network, or null
+    float polyak[kMaxNets];
 };
+cudaError_t launch_target_ema(const float* p, float* target, int64_t n, float polyak, cudaStream_t st);
 cudaError_t launch_adam(const AdamLaunch& a, cudaStream_t st);
 
 struct CombineLaunch {

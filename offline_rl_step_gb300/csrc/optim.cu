@@ -107,6 +107,15 @@ __global__ void __launch_bounds__(kRedThreads, EL == 8 ? 5 : 4) reduce_gram_kern
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     if (k < nsrc && i4 + e < P) x[k][e] = __ldg(a.src[net][k] + i4 + e);
+            if (a.sanitize) {
+                int bad = 0;
+#pragma unroll
+                for (int k = 0; k < kMaxSrc; ++k)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (!isfinite(x[k][e])) { x[k][e] = 0.0f; ++bad; }
+                if (bad) atomicAdd(a.status + OFRL_STAT_SANITIZED, bad);
+            }
 #pragma unroll
             for (int e = 0; e < 4; ++e)
 #pragma unroll
@@ -214,15 +223,25 @@ __global__ void __launch_bounds__(256) adam_kernel(const AdamLaunch a) {
     bool bad = false;
     if (i < a.n) {
         float gsum = 0.0f;
-        for (int k = 0; k < a.n_src; ++k) gsum = fmaf(coef[k], __ldg(a.src[net][k] + i), gsum);
+        for (int k = 0; k < a.n_src; ++k) {
+            float x = __ldg(a.src[net][k] + i);
+            if (a.sanitize && !isfinite(x)) x = 0.0f;
+            gsum = fmaf(coef[k], x, gsum);
+        }
         const float g = s * gsum;
         float m = a.m[net][i], v = a.v[net][i], p = a.p[net][i];
         if (adam_element(p, m, v, g, a.beta1, a.beta2, a.eps, a.weight_decay, a.lr[net], a.bc1[net], a.bc2[net])) {
+            if (a.clamp > 0.0f) p = fminf(fmaxf(p, -a.clamp), a.clamp);
             a.m[net][i] = m;
             a.v[net][i] = v;
             a.p[net][i] = p;
         } else {
             bad = true;
+        }
+        // the target network follows the (possibly unchanged) weights
+        if (a.target[net] != nullptr) {
+            const float pk = a.polyak[net];
+            a.target[net][i] = (1.0f - pk) * a.target[net][i] + pk * p;
         }
     }
     const unsigned ballot = __ballot_sync(0xffffffffu, bad);
@@ -324,6 +343,18 @@ cudaError_t launch_adam(const AdamLaunch& a, cudaStream_t st) {
         configured = true;
     }
     return launch_pdl(adam_kernel, grid, dim3(256), 0, st, a);
+}
+
+__global__ void __launch_bounds__(256) target_ema_kernel(const float* __restrict__ p, float* __restrict__ target,
+                                                         int64_t n, float polyak) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) target[i] = (1.0f - polyak) * target[i] + polyak * __ldg(p + i);
+}
+
+cudaError_t launch_target_ema(const float* p, float* target, int64_t n, float polyak, cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    target_ema_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(p, target, n, polyak);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const CombineLaunch& a, cudaStream_t st) {

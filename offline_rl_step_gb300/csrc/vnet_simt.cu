@@ -123,7 +123,10 @@ __device__ __forceinline__ void gemm_tn_store(const float* A, int lda, int NI, c
     }
 }
 
-template <int H, bool BF16>
+// FWD: forward only -- V of every row into v_out and, with target_out, the
+// IQL bootstrap target r + gamma (1 - done) V ("GPU IQL + HER Porting Plan",
+// "IQL modifies the target computation" and forward_values).
+template <int H, bool BF16, bool FWD>
 __global__ void __launch_bounds__(kThreads, 1) vnet_fwd_bwd_kernel(const VnetLaunch a) {
     constexpr int TM = TileRows<H>::value;
     constexpr int RPT = TM / 8, CPT = H / 32;
@@ -187,6 +190,31 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_fwd_bwd_kernel(const VnetLau
     const float b3 = __ldg(prm + off.b3);
     float vrow[RPT], dv[RPT];
     float loss_part = 0.0f, db3_part = 0.0f;
+    if constexpr (FWD) {
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {
+            float s = 0.0f;
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) {
+                const float h = acc[i][j] < 0.0f ? 0.0f : acc[i][j];
+                s = fmaf(h, w3[j], s);
+            }
+            vrow[i] = warp_sum(s) + b3;
+        }
+        if (tx < RPT) {
+            float myv = 0.0f;
+#pragma unroll
+            for (int i = 0; i < RPT; ++i) if (tx == i) myv = vrow[i];
+            const int b = row0 + ty + 8 * tx;
+            if (b < B) {
+                if (a.v_out != nullptr) a.v_out[(int64_t)net * B + b] = myv;
+                if (a.target_out != nullptr)
+                    a.target_out[(int64_t)net * B + b] =
+                        __ldg(a.rewards + b) + a.gamma * (1.0f - __ldg(a.dones + b)) * myv;
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
         float s = 0.0f;
@@ -319,11 +347,11 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_fwd_bwd_kernel(const VnetLau
     gemm_tn_store<TM>(h1s, H, H, Xs, kXStride, S, part + off.w1, S);
 }
 
-template <int H, bool BF16>
+template <int H, bool BF16, bool FWD = false>
 cudaError_t launch_h(const VnetLaunch& a, cudaStream_t st) {
     constexpr int TM = TileRows<H>::value;
     const size_t smem = smem_floats<H, TM>() * sizeof(float);
-    auto kern = vnet_fwd_bwd_kernel<H, BF16>;
+    auto kern = vnet_fwd_bwd_kernel<H, BF16, FWD>;
     static bool configured = false;   // per instantiation; setting it twice is harmless
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -345,6 +373,17 @@ cudaError_t launch_vnet_fwd_bwd(const VnetLaunch& a, cudaStream_t st) {
         case 64: return bf ? launch_h<64, true>(a, st) : launch_h<64, false>(a, st);
         case 128: return bf ? launch_h<128, true>(a, st) : launch_h<128, false>(a, st);
         case 256: return bf ? launch_h<256, true>(a, st) : launch_h<256, false>(a, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_vnet_forward(const VnetLaunch& a, cudaStream_t st) {
+    if (a.batch <= 0) return cudaSuccess;
+    const bool bf = a.prec == OFRL_PREC_BF16;
+    switch (a.hidden) {
+        case 64: return bf ? launch_h<64, true, true>(a, st) : launch_h<64, false, true>(a, st);
+        case 128: return bf ? launch_h<128, true, true>(a, st) : launch_h<128, false, true>(a, st);
+        case 256: return bf ? launch_h<256, true, true>(a, st) : launch_h<256, false, true>(a, st);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -49,6 +49,21 @@ def forward(flat, states, state_dim: int, hidden: int):
     return v, dict(x=x, z1=z1, h1=h1, z2=z2, h2=h2)
 
 
+def iql_target(flat, next_states, rewards, dones, gamma: float, state_dim: int, hidden: int):
+    """IQL bootstrap target for the Q loss and V(s').
+
+    "GPU IQL + HER Porting Plan", "IQL modifies the target computation": the
+    target r + gamma max_a Q_target(s', a') becomes r + gamma V(s'), V(s')
+    from the value network's forward pass on the next states
+    (forward_values).  A terminal transition (done = 1) bootstraps nothing:
+    target = r + gamma (1 - done) V(s').
+    """
+    v, _ = forward(flat, next_states, state_dim, hidden)
+    r = np.asarray(rewards, dtype=np.float64)
+    d = np.asarray(dones, dtype=np.float64)
+    return r + float(gamma) * (1.0 - d) * v, v
+
+
 def q_taken(q, actions):
     """Q(s, a_taken): the entry of each Q row at the row's action."""
     q = np.asarray(q, dtype=np.float64)

@@ -11,13 +11,16 @@ Order of one step (for each V network; twin networks share the batch and Q):
      source ("Gradient Stability ...", "Proper design", pipeline steps 2-6).
   4. t <- t + 1, then Adam with its safety clip at max_grad_norm (pipeline
      step 7; the step counter is incremented before Adam reads it, "DQN
-     Backward-Path NaN Audit", Adam findings).
+     Backward-Path NaN Audit", Adam findings), the optional weight bound
+     after the update, and the optional Polyak update of the network's
+     target copy ("GPU IQL + HER Porting Plan", target_ema_update).
 
 The twin workload runs two networks (high and low tau) with identical shapes
 and independent weights on one batch ("Phase 2: Multi-Stream Graph
 Parallelism", "2C. Grouped GEMM for IQL").
 """
 from dataclasses import dataclass
+from typing import Optional
 
 import numpy as np
 
@@ -31,11 +34,14 @@ class NetState:
     v: np.ndarray
     t: int = 0
     tau: float = 0.7
+    target: Optional[np.ndarray] = None   # Polyak target copy, or None
+    polyak: float = 0.0
 
     @classmethod
-    def fresh(cls, params, tau):
+    def fresh(cls, params, tau, polyak=None):
         p = np.asarray(params, dtype=np.float64).copy()
-        return cls(params=p, m=np.zeros_like(p), v=np.zeros_like(p), t=0, tau=float(tau))
+        return cls(params=p, m=np.zeros_like(p), v=np.zeros_like(p), t=0, tau=float(tau),
+                   target=None if polyak is None else p.copy(), polyak=float(polyak or 0.0))
 
 
 @dataclass
@@ -58,6 +64,8 @@ class StepConfig:
     max_grad_norm: float
     budget: tuple = optim.BUDGET
     alpha: tuple = (1.0, 1.0, 1.0, 1.0)
+    weight_clamp_max_abs: float = 0.0
+    sanitize_sources: bool = False
 
 
 def config_from_workload(w) -> StepConfig:
@@ -92,6 +100,8 @@ def train_step(cfg: StepConfig, replay: dict, step: int, q, nets, aux=None):
         if aux is not None and aux[k] is not None:
             sources += [np.asarray(a, dtype=np.float64) for a in aux[k]]
         n = len(sources)
+        if cfg.sanitize_sources:
+            sources = [optim.sanitize(x) for x in sources]
         g, norms = optim.budgeted_combine(sources, cfg.budget[:n], cfg.alpha[:n], cfg.max_grad_norm)
         # magnitude scale of each combined element: |coef_0| * sum|terms of g0|
         # plus |coef_k g_k| for the (exact) auxiliary inputs
@@ -102,7 +112,9 @@ def train_step(cfg: StepConfig, replay: dict, step: int, q, nets, aux=None):
         net.t += 1
         net.params, net.m, net.v, skipped = optim.adam(
             net.params, g, net.m, net.v, net.t, cfg.lr, cfg.beta1, cfg.beta2, cfg.eps,
-            cfg.weight_decay, cfg.max_grad_norm, norms[-1])
+            cfg.weight_decay, cfg.max_grad_norm, norms[-1], cfg.weight_clamp_max_abs)
+        if net.target is not None:
+            net.target = optim.polyak(net.target, net.params, net.polyak)
         full = np.zeros(5)
         full[:n] = norms[:n]
         full[4] = norms[-1]

@@ -53,13 +53,14 @@ def replay_dev(w, rep):
                        dev(rep["dones"]), w.state_dim, w.goal_dim, dev(rep["episode_ends"]))
 
 
-def oracle_cfg(w):
+def oracle_cfg(w, weight_clamp_max_abs=0.0, sanitize_sources=False):
     """Oracle step config with the fp32-rounded constants the library gets."""
     c = ostep.config_from_workload(w)
     return dataclasses.replace(
         c, goal_threshold=f32(w.goal_threshold), beta=f32(w.beta), lr=f32(w.lr), beta1=f32(w.beta1),
         beta2=f32(w.beta2), eps=f32(w.eps), weight_decay=f32(w.weight_decay),
-        max_grad_norm=f32(w.max_grad_norm), budget=tuple(f32(b) for b in w.budget))
+        max_grad_norm=f32(w.max_grad_norm), budget=tuple(f32(b) for b in w.budget),
+        weight_clamp_max_abs=f32(weight_clamp_max_abs), sanitize_sources=bool(sanitize_sources))
 
 
 def report(gpu, ref, rtol, atol):
@@ -109,7 +110,7 @@ def argmax_ok(gpu_am, q, v_ref, beta, margin=1e-3):
 class GpuStep:
     """The fused train step of one workload on the GPU, through the C ABI."""
 
-    def __init__(self, w):
+    def __init__(self, w, weight_clamp_max_abs=0.0, sanitize_sources=False, polyak=None):
         import offline_rl_step_gb300 as ofrl
         self.ofrl = ofrl
         self.w = w
@@ -119,9 +120,11 @@ class GpuStep:
         self.ctx = ofrl.Context(w.state_dim, w.hidden, w.num_actions, w.prec, max_batch=w.batch,
                                 max_nets=w.n_nets)
         self.params0 = [synth.make_params(w, k) for k in range(w.n_nets)]
-        self.nets = [ofrl.VNet.from_params(torch.from_numpy(p), w.taus[k]) for k, p in enumerate(self.params0)]
+        self.nets = [ofrl.VNet.from_params(torch.from_numpy(p), w.taus[k], polyak=polyak)
+                     for k, p in enumerate(self.params0)]
         self.opt = ofrl.Opt(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
-                            max_grad_norm=w.max_grad_norm, beta=w.beta, budget=w.budget)
+                            max_grad_norm=w.max_grad_norm, beta=w.beta, budget=w.budget,
+                            weight_clamp_max_abs=weight_clamp_max_abs, sanitize_sources=sanitize_sources)
         self.batch = ofrl.Batch.empty(w.batch, w.state_stride)
         n, b, a, p = w.n_nets, w.batch, w.num_actions, w.n_params
         self.v = torch.empty(n, b, device="cuda")
@@ -142,14 +145,16 @@ class GpuStep:
                            ("states", "next_states", "actions", "rewards", "dones", "src_idx", "donor_idx")},
                     v=cpu(self.v), pi=cpu(self.pi), argmax=cpu(self.am), loss=cpu(self.loss),
                     norms=cpu(self.norms), grad=cpu(self.grad),
-                    params=[cpu(n.params) for n in self.nets])
+                    params=[cpu(n.params) for n in self.nets],
+                    target=[cpu(n.target) if n.target is not None else None for n in self.nets])
 
     def close(self):
         self.ctx.close()
 
 
-def oracle_nets(w):
-    return [ostep.NetState.fresh(synth.make_params(w, k), f32(w.taus[k])) for k in range(w.n_nets)]
+def oracle_nets(w, polyak=None):
+    return [ostep.NetState.fresh(synth.make_params(w, k), f32(w.taus[k]), None if polyak is None else f32(polyak))
+            for k in range(w.n_nets)]
 
 
 def her_rows(w):

@@ -55,8 +55,8 @@ int main(void) {
   P(ofrl_replay, episode_ends) P(ofrl_replay, capacity) P(ofrl_replay, num_episodes) P(ofrl_replay, goal_dim)
   P(ofrl_her_cfg, goal_threshold) P(ofrl_her_cfg, seed)
   P(ofrl_batch, donor_idx) P(ofrl_batch, stride)
-  P(ofrl_vnet, t) P(ofrl_vnet, tau)
-  P(ofrl_opt, beta) P(ofrl_opt, budget) P(ofrl_opt, alpha)
+  P(ofrl_vnet, t) P(ofrl_vnet, tau) P(ofrl_vnet, target) P(ofrl_vnet, polyak)
+  P(ofrl_opt, beta) P(ofrl_opt, budget) P(ofrl_opt, alpha) P(ofrl_opt, weight_clamp_max_abs) P(ofrl_opt, sanitize_sources)
   return 0;
 }
 """

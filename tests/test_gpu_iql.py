@@ -90,3 +90,77 @@ def test_policy(b, a):
     np.testing.assert_allclose(pi.cpu().numpy().sum(axis=1), 1.0, atol=1e-5)
     argmax_ok(am.cpu().numpy(), q, v, 3.0)
     ctx.close()
+
+
+def _forward_case(s, h, b, prec="fp32", seed=0):
+    import offline_rl_step_gb300 as ofrl
+    need_gpu()
+    w = dataclasses.replace(synth.PROD, state_dim=s, hidden=h, net_seeds=(seed + 11,))
+    params = synth.make_params(w)
+    rng = np.random.default_rng(seed)
+    st = (s + 7) & ~7
+    x = np.zeros((b, st), dtype=np.float32)
+    x[:, :s] = rng.standard_normal((b, s))
+    r = rng.standard_normal(b).astype(np.float32)
+    d = (rng.random(b) < 0.1).astype(np.float32)
+    ctx = ofrl.Context(s, h, 5, prec, max_batch=b)
+    return ofrl, ctx, w, params, x, r, d
+
+
+@pytest.mark.parametrize("s,h,b", [(50, 128, 16384), (48, 64, 256), (50, 256, 333), (7, 64, 1), (64, 128, 129)])
+def test_forward_values_fp32(s, h, b):
+    ofrl, ctx, w, params, x, _, _ = _forward_case(s, h, b, seed=s + b)
+    v = torch.empty(b, device="cuda")
+    ofrl.forward_values(ctx, dev(params), dev(x), v)
+    torch.cuda.synchronize()
+    rv, _, vu, _ = value_uncertainty(params.astype(np.float64), x, np.zeros(b, np.float32), f32(0.7), s, h)
+    ctx.close()
+    assert within(v.cpu().numpy(), rv, vu, RTOL, ATOL).all(), "V outside tolerance and fp32 bound"
+
+
+@pytest.mark.parametrize("s,h,b", [(50, 128, 16384), (50, 256, 1000)])
+def test_iql_target_fp32(s, h, b):
+    ofrl, ctx, w, params, x, r, d = _forward_case(s, h, b, seed=3 * b)
+    gamma = 0.99
+    t = torch.empty(b, device="cuda")
+    vn = torch.empty(b, device="cuda")
+    ofrl.iql_target(ctx, dev(params), dev(x), dev(r), dev(d), gamma, t, v_next_out=vn)
+    torch.cuda.synchronize()
+    rt, rv = iql.iql_target(params, x, r, d, f32(gamma), s, h)
+    _, _, vu, _ = value_uncertainty(params.astype(np.float64), x, np.zeros(b, np.float32), f32(0.7), s, h)
+    ctx.close()
+    tg, vg = t.cpu().numpy(), vn.cpu().numpy()
+    assert within(vg, rv, vu, RTOL, ATOL).all()
+    # target = r + gamma (1 - d) V: V's bound scaled by gamma, plus the fp32 rounding of the sum
+    tu = float(gamma) * (1.0 - d) * vu + 4 * np.finfo(np.float32).eps * (np.abs(rt) + 1.0)
+    assert within(tg, rt, tu, RTOL, ATOL).all()
+    # terminal rows bootstrap nothing: exactly the reward
+    term = d == 1.0
+    assert np.array_equal(tg[term], r[term])
+
+
+def test_forward_values_bf16():
+    ofrl, ctx, w, params, x, _, _ = _forward_case(50, 128, 4096, prec="bf16", seed=5)
+    v = torch.empty(4096, device="cuda")
+    ofrl.forward_values(ctx, dev(params), dev(x), v)
+    torch.cuda.synchronize()
+    rv, _ = iql.forward(params, x, 50, 128)
+    ctx.close()
+    vg = v.cpu().numpy()
+    # bf16 operands: the pages' 2e-2, on the values' scale
+    assert np.abs(vg - rv).max() <= BF16_RTOL * max(1.0, np.abs(rv).max())
+
+
+def test_forward_rejects_bad_arguments():
+    import offline_rl_step_gb300 as ofrl
+    need_gpu()
+    ctx = ofrl.Context(50, 128, 5, "fp32", max_batch=64)
+    p = torch.zeros(synth.PROD.n_params, device="cuda")
+    x = torch.zeros(65, 56, device="cuda")
+    v = torch.empty(65, device="cuda")
+    with pytest.raises(Exception):
+        ofrl.forward_values(ctx, p, x, v)           # batch above max_batch
+    r = torch.zeros(8, device="cuda")
+    with pytest.raises(Exception):
+        ofrl.iql_target(ctx, p, x[:8], r, r, 1.5, r)   # gamma outside [0, 1]
+    ctx.close()

@@ -109,3 +109,44 @@ def test_budget_with_non_finite_source_follows_ieee_reading():
     ok = np.isfinite(rg)
     assert_close(go[ok], rg[ok], what="finite elements")
     ctx.close()
+
+
+def test_adam_step_weight_bound():
+    import offline_rl_step_gb300 as ofrl
+    ctx = _ctx()
+    n = 23169
+    rng = np.random.default_rng(21)
+    p = (rng.standard_normal(n) * 0.1).astype(np.float32)
+    g = (rng.standard_normal(n) * 0.3).astype(np.float32)
+    z = np.zeros(n, np.float32)
+    opt = ofrl.Opt(lr=3e-4, max_grad_norm=np.inf, weight_clamp_max_abs=0.12)
+    tp, tm, tv = dev(p), dev(z), dev(z)
+    ofrl.adam_step(ctx, tp, dev(g), tm, tv, 1, opt, grad_norm=torch.tensor([1.0], device="cuda"))
+    torch.cuda.synchronize()
+    rp, _, _, _ = optim.adam(p, g, z, z, 1, f32(3e-4), f32(0.9), f32(0.999), f32(1e-8), 0.0, np.inf, 1.0,
+                             weight_clamp=f32(0.12))
+    gp = tp.cpu().numpy()
+    assert (np.abs(gp) <= f32(0.12)).all()
+    assert ((np.abs(rp) >= f32(0.12) * (1 - 1e-7)) == (np.abs(gp) >= f32(0.12) * (1 - 1e-7))).mean() > 0.999
+    assert_close(gp, rp, what="p")
+    ctx.close()
+
+
+@pytest.mark.parametrize("n,rate", [(1, 0.5), (23169, 0.005), (1_000_003, 1.0), (4096, 0.0)])
+def test_target_ema(n, rate):
+    import offline_rl_step_gb300 as ofrl
+    need_gpu()
+    rng = np.random.default_rng(n)
+    p = rng.standard_normal(n).astype(np.float32)
+    t = rng.standard_normal(n).astype(np.float32)
+    tp, tt = dev(p), dev(t)
+    ofrl.target_ema(tp, tt, f32(rate))
+    torch.cuda.synchronize()
+    ref = optim.polyak(t, p, f32(rate))
+    got = tt.cpu().numpy().astype(np.float64)
+    # two fp32 products and a sum: a few units in the last place of the inputs' scale
+    assert (np.abs(got - ref) <= 3 * np.finfo(np.float32).eps * (np.abs(t) + np.abs(p))).all()
+    if rate == 1.0:
+        assert np.array_equal(tt.cpu().numpy(), p)
+    if rate == 0.0:
+        assert np.array_equal(tt.cpu().numpy(), t)

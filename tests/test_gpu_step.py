@@ -37,7 +37,7 @@ import torch
 
 import synth
 from _errmodel import grad_ok, value_uncertainty, within
-from _gpu import (ATOL, BF16_RTOL, RTOL, GpuStep, argmax_ok, assert_bits, assert_close, need_gpu,
+from _gpu import (ATOL, BF16_RTOL, RTOL, GpuStep, argmax_ok, assert_bits, assert_close, f32, need_gpu,
                   oracle_cfg, oracle_nets, replay_np)
 from oracle import iql, optim
 from oracle import step as ostep
@@ -45,6 +45,7 @@ from oracle import step as ostep
 pytestmark = pytest.mark.gpu
 
 FULL = os.environ.get("OFRL_FULL_STEPS", "0") == "1"
+EPS32 = float(np.finfo(np.float32).eps)
 STRICT = 10
 TRAJ_RTOL = 1e-3   # norm-wise V and weight agreement past the strict horizon
 RESYNC = (25, 50, 75, 99)   # steps checked strictly from the oracle's state
@@ -178,3 +179,50 @@ def test_single_row_batch_step():
     need_gpu()
     w = dataclasses.replace(synth.TINY, batch=1, her_ratio=1.0, steps=2)
     test_train_step_matches_oracle(w)
+
+
+def test_step_with_source_guard_weight_bound_and_target():
+    # three auxiliary sources with planted NaN / +-inf elements and the
+    # isfinite guard on; a weight bound below the initial weight range (it
+    # binds from the first step); a Polyak target copy of every network
+    need_gpu()
+    w = dataclasses.replace(synth.PROD, batch=1000, capacity=1 << 14, steps=3,
+                            aux_sigmas=synth.BUDGETED.aux_sigmas, weight_decay=1e-4)
+    opts = dict(weight_clamp_max_abs=0.15, sanitize_sources=True)
+    rate = 0.05
+    g = GpuStep(w, polyak=rate, **opts)
+    cfg = oracle_cfg(w, **opts)
+    rep = replay_np(w)
+    nets = oracle_nets(w, polyak=rate)
+    flagged = [np.zeros(w.n_params, dtype=bool) for _ in range(w.n_nets)]
+    gpu_params = [p.copy() for p in g.params0]
+    tbound = [np.zeros(w.n_params) for _ in range(w.n_nets)]
+    planted = 0
+    try:
+        for k in range(w.steps):
+            q = synth.make_q(w, k)
+            aux = [synth.make_aux(w, k, n) for n in range(w.n_nets)]
+            for n in range(w.n_nets):
+                for j, src in enumerate(aux[n]):
+                    src[[7 + j, 1000 + 13 * j, w.n_params - 1 - j]] = [np.nan, np.inf, -np.inf]
+                    planted += 3
+            got = g.step(k, q, aux)
+            p_before = [n.params.copy() for n in nets]
+            ref = ostep.train_step(cfg, rep, k, q, nets, aux)
+            _check_step(w, k, got, ref, flagged, nets, p_before, gpu_params, q)
+            gpu_params = got["params"]
+            for n in range(w.n_nets):
+                assert np.isfinite(got["params"][n]).all()
+                assert (np.abs(got["params"][n]) <= f32(0.15)).all()
+                assert got["norms"][n, 4] <= w.max_grad_norm * (1 + 1e-5)
+                # the target follows the weights: e_k <= (1 - r) e_{k-1} + r |dp_k|
+                # + rounding, with dp_k the measured weight difference
+                tg, tr = got["target"][n].astype(np.float64), nets[n].target
+                pe = np.abs(got["params"][n].astype(np.float64) - nets[n].params)
+                tbound[n] = (1 - rate) * tbound[n] + rate * pe + 4 * EPS32 * (np.abs(tr) + np.abs(nets[n].params))
+                assert (np.abs(tg - tr) <= tbound[n] + 1e-12).all()
+        st = g.ctx.poll_status()
+        assert st["sanitized"] == planted, st
+        assert st["nonfinite_grad"] == 0, st
+    finally:
+        g.close()

@@ -205,3 +205,46 @@ def test_backward_abs_bounds_and_equality():
     g = iql.backward(flat, act, dv, s, h)
     ga = iql.backward_abs(flat, act, dv, s, h)
     np.testing.assert_allclose(np.abs(g), ga, rtol=1e-12)
+
+
+# ---- IQL target r + gamma (1 - done) V(s') ----------------------------------
+
+def _target_case(seed=3, b=9, s=6, h=5):
+    rng = np.random.default_rng(seed)
+    flat = rng.standard_normal(h * s + h + h * h + h + h + 1)
+    xs = rng.standard_normal((b, s))
+    r = rng.standard_normal(b)
+    d = (rng.random(b) < 0.4).astype(np.float64)
+    return flat, xs, r, d, s, h
+
+
+def test_target_terminal_rows_bootstrap_nothing():
+    flat, xs, r, _, s, h = _target_case()
+    t, _ = iql.iql_target(flat, xs, r, np.ones_like(r), 0.99, s, h)
+    assert np.array_equal(t, r)
+
+
+def test_target_gamma_zero_is_the_reward():
+    flat, xs, r, d, s, h = _target_case(seed=4)
+    t, _ = iql.iql_target(flat, xs, r, d, 0.0, s, h)
+    assert np.array_equal(t, r)
+
+
+def test_target_zero_weights_closed_form():
+    # W1 = W2 = W3 = 0: V = b3 for every state, so target = r + gamma (1 - d) b3
+    flat, xs, r, d, s, h = _target_case(seed=5)
+    w1, b1, w2, b2, w3, b3 = iql.unflatten(flat, s, h)
+    flat0 = iql.flatten(np.zeros_like(w1), b1, np.zeros_like(w2), b2, np.zeros_like(w3), b3)
+    t, v = iql.iql_target(flat0, xs, r, d, 0.9, s, h)
+    assert np.allclose(v, b3[0], rtol=0, atol=0)
+    assert np.allclose(t, r + 0.9 * (1.0 - d) * b3[0], rtol=1e-15, atol=0)
+
+
+def test_target_mixes_rows_by_done_flag():
+    # rows with done = 0 carry gamma V(s'); rows with done = 1 do not
+    flat, xs, r, d, s, h = _target_case(seed=6, b=40)
+    t, v = iql.iql_target(flat, xs, r, d, 0.5, s, h)
+    live = d == 0.0
+    assert live.any() and (~live).any()
+    assert np.allclose(t[live] - r[live], 0.5 * v[live], rtol=1e-14, atol=1e-15)
+    assert np.array_equal(t[~live], r[~live])

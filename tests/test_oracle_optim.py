@@ -145,3 +145,74 @@ def test_adam_skips_non_finite_elements():
         assert p[i] == p0[i] and m[i] == m0[i] and v[i] == v0[i]
     for i in (0, 2, 5):
         assert p[i] != p0[i]
+
+
+# ---- isfinite guard on the sources, weight bound, Polyak target -------------
+
+def _sources(seed=11, n=4, p=257, scales=(3.0, 1.0, 0.5, 2.0)):
+    rng = np.random.default_rng(seed)
+    return [rng.standard_normal(p) * s for s in scales[:n]]
+
+
+def test_sanitize_is_identity_on_finite_sources():
+    srcs = _sources()
+    g0, n0 = optim.budgeted_combine(srcs, optim.BUDGET, (1, 1, 1, 1), 1.0)
+    g1, n1 = optim.budgeted_combine(srcs, optim.BUDGET, (1, 1, 1, 1), 1.0, sanitize_sources=True)
+    assert np.array_equal(g0, g1) and np.array_equal(n0, n1)
+
+
+def test_sanitized_sources_keep_the_budget_bound():
+    # NaN and +-inf planted in every source: the guarded combination stays
+    # finite and inside the budget sum (sum f_k mgn = mgn)
+    srcs = _sources(seed=12)
+    for k, s in enumerate(srcs):
+        s[[k, 40 + k, 99]] = [np.nan, np.inf, -np.inf]
+    g, norms = optim.budgeted_combine(srcs, optim.BUDGET, (1, 1, 1, 1), 1.0, sanitize_sources=True)
+    assert np.isfinite(g).all() and np.isfinite(norms).all()
+    assert norms[-1] <= 1.0 * (1 + 1e-12)
+    # without the guard the planted values reach the sum
+    g_raw, _ = optim.budgeted_combine(srcs, optim.BUDGET, (1, 1, 1, 1), 1.0)
+    assert not np.isfinite(g_raw).all()
+
+
+def test_an_all_nonfinite_source_contributes_nothing():
+    srcs = _sources(seed=13, n=3)
+    bad = np.full_like(srcs[2], np.nan)
+    g, norms = optim.budgeted_combine([srcs[0], srcs[1], bad], optim.BUDGET[:3], (1, 1, 1), 1.0,
+                                      sanitize_sources=True)
+    g2, _ = optim.budgeted_combine(srcs[:2], optim.BUDGET[:2], (1, 1), 1.0)
+    assert norms[2] == 0.0
+    assert np.allclose(g, g2, rtol=0, atol=0)
+
+
+def test_weight_bound_closed_form():
+    # first step from m = v = 0 moves p by ~lr sign(g); 0.99995 + 3e-4 is
+    # past the bound 1.0, so the weight ends exactly on it
+    p = np.array([0.99995, -0.5, 0.2])
+    g = np.array([-1.0, 1.0, 1e-3])
+    z = np.zeros(3)
+    pc, _, _, _ = optim.adam(p, g, z, z, 1, 3e-4, 0.9, 0.999, 1e-8, 0.0, np.inf, 0.0, weight_clamp=1.0)
+    pu, _, _, _ = optim.adam(p, g, z, z, 1, 3e-4, 0.9, 0.999, 1e-8, 0.0, np.inf, 0.0)
+    assert pc[0] == 1.0 and pu[0] > 1.0
+    assert np.array_equal(pc[1:], pu[1:])
+    assert (np.abs(pc) <= 1.0).all()
+
+
+def test_weight_bound_leaves_skipped_elements_alone():
+    p = np.array([5.0, 0.1])
+    g = np.array([np.nan, 1.0])
+    z = np.zeros(2)
+    pc, _, _, skipped = optim.adam(p, g, z, z, 1, 3e-4, 0.9, 0.999, 1e-8, 0.0, np.inf, 0.0, weight_clamp=1.0)
+    assert skipped == 1 and pc[0] == 5.0
+
+
+def test_polyak_rates_and_closed_form():
+    rng = np.random.default_rng(14)
+    t0, p = rng.standard_normal(50), rng.standard_normal(50)
+    assert np.array_equal(optim.polyak(t0, p, 1.0), p)
+    assert np.array_equal(optim.polyak(t0, p, 0.0), t0)
+    # k updates toward a fixed p: target_k = p + (1 - r)^k (target_0 - p)
+    t, r = t0.copy(), 0.05
+    for _ in range(20):
+        t = optim.polyak(t, p, r)
+    assert np.allclose(t, p + (1 - r) ** 20 * (t0 - p), rtol=1e-13, atol=1e-14)
