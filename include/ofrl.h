@@ -52,8 +52,10 @@ enum {
 
 /* HER donor strategies ("GPU IQL + HER Porting Plan", "Donor Index
  * Generation"; the string map "final" / "future" / anything else -> Random
- * is in "Config Wiring" of the HER part). */
-enum { OFRL_HER_FINAL = 0, OFRL_HER_FUTURE = 1, OFRL_HER_RANDOM = 2 };
+ * is in "Config Wiring" of the HER part).  EPISODE is named in "HER (CPU)"
+ * item 5 without a definition: here, as in the HER paper's "episode"
+ * strategy, the donor is uniform over the source's whole episode. */
+enum { OFRL_HER_FINAL = 0, OFRL_HER_FUTURE = 1, OFRL_HER_RANDOM = 2, OFRL_HER_EPISODE = 3 };
 
 /* GEMM operand precision.  FP32: fp32 operands and accumulation.  BF16:
  * GEMM operands rounded to bf16 (round-to-nearest-even), fp32 accumulation,
@@ -188,8 +190,10 @@ int64_t ofrl_workspace_bytes(const ofrl_vshape* shape, int32_t max_batch, int32_
  * HER row the donor is: FINAL episode_end(src) - 1; FUTURE src + 1 +
  * below(draw(seed, step*2^32 + 2b + 1), episode_end(src) - src - 1), or src
  * itself when src is its episode's last transition; RANDOM
- * below(draw(seed, ...2b + 1), capacity).  episode_end(i) is the first
- * entry of episode_ends above i (binary search).  draw(k, n) is output n+1
+ * below(draw(seed, ...2b + 1), capacity); EPISODE episode_start(src) +
+ * below(draw(seed, ...2b + 1), episode_end(src) - episode_start(src)).
+ * episode_end(i) is the first entry of episode_ends above i (binary search),
+ * episode_start(i) the entry before it (0 for the first episode).  draw(k, n) is output n+1
  * of SplitMix64 seeded with k; below(r, n) = ((r >> 32) * n) >> 32.
  * Row output: states/next_states/action/reward/done of src; for HER rows the
  * first g elements of both states are replaced by next_states[donor, :g]
@@ -200,6 +204,32 @@ int64_t ofrl_workspace_bytes(const ofrl_vshape* shape, int32_t max_batch, int32_
  * Writes every field of `out`. */
 ofrl_status ofrl_her_relabel(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl_her_cfg* her,
                              uint64_t step, const ofrl_batch* out, void* stream);
+
+/* The relabel with the caller's sources ("GPU IQL + HER Porting Plan", "How
+ * HER Interacts with GPU PER": normal rows and the HER rows' sources come
+ * from the PER sampler; the HER rows' importance weights are 1, no PER
+ * bias).  src_idx: device [batch] source of every row (normal rows first,
+ * then the her_count HER rows; outside [0, capacity) is clamped and counted
+ * in OFRL_STAT_BAD_INDEX).  is_weights: device [batch] or NULL (weight 1).
+ * is_weights_out: device [batch] or NULL: the normal rows' weights, 1 for
+ * HER rows.  Donors, rewards and the copies as ofrl_her_relabel. */
+ofrl_status ofrl_her_relabel_sources(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl_her_cfg* her,
+                                     uint64_t step, const int32_t* src_idx, const float* is_weights,
+                                     const ofrl_batch* out, float* is_weights_out, void* stream);
+
+/* Episode-boundary maintenance on the device ("GPU IQL + HER Porting
+ * Plan", "Episode Boundary Tracking on GPU": each finished episode's end is
+ * appended to a GPU-resident boundary array that grows as episodes
+ * complete).  n new transitions were stored at buffer positions
+ * first_index .. first_index + n - 1 with done flags dones[0 .. n) (device);
+ * for every i with dones[i] != 0 the exclusive end first_index + i + 1 is
+ * appended to episode_ends (device, max_episodes entries) after the
+ * *num_episodes (device int32) already there, in ascending order, and
+ * *num_episodes grows by their number.  Ends that do not fit are dropped and
+ * counted in OFRL_STAT_BAD_INDEX.  first_index + n <= 2^31 - 1. */
+ofrl_status ofrl_episode_ends_append(ofrl_ctx* ctx, const float* dones, int64_t first_index, int32_t n,
+                                     int32_t* episode_ends, int32_t* num_episodes, int32_t max_episodes,
+                                     void* stream);
 
 /* V forward + expectile loss + V backward ("GPU IQL + HER Porting Plan",
  * "IQL (CPU)" items 1-2 and "CUDA Kernel: iql_value_kernel.cu").

@@ -23,10 +23,10 @@ from typing import List, Optional, Sequence
 import torch
 
 from . import _abi
-from ._abi import (HER_FINAL, HER_FUTURE, HER_RANDOM, PREC_BF16, PREC_FP32,  # noqa: F401
+from ._abi import (HER_EPISODE, HER_FINAL, HER_FUTURE, HER_RANDOM, PREC_BF16, PREC_FP32,  # noqa: F401
                    STAT_BAD_ACTION, STAT_BAD_INDEX, STAT_NONFINITE_GRAD, STAT_SANITIZED, STAT_TIMEOUT, OfrlError)
 
-STRATEGY = {"final": HER_FINAL, "future": HER_FUTURE, "random": HER_RANDOM}
+STRATEGY = {"final": HER_FINAL, "future": HER_FUTURE, "random": HER_RANDOM, "episode": HER_EPISODE}
 PRECISION = {"fp32": PREC_FP32, "bf16": PREC_BF16}
 BUDGET = (0.70, 0.15, 0.10, 0.05)
 
@@ -199,6 +199,23 @@ def her_relabel(ctx: Context, replay: Replay, her: HerConfig, step: int, out: Ba
     r, h, b = replay.c(), her.c(), out.c()
     _abi.check("ofrl_her_relabel", ctx._lib.ofrl_her_relabel(ctx.handle, C.byref(r), C.byref(h), step,
                                                               C.byref(b), _stream(stream)))
+
+
+def her_relabel_sources(ctx: Context, replay: Replay, her: HerConfig, step: int, src_idx, out: Batch,
+                        is_weights=None, is_weights_out=None, stream=None):
+    """her_relabel with the caller's (e.g. PER-sampled) source of every row; HER rows get importance weight 1."""
+    r, h, b = replay.c(), her.c(), out.c()
+    _abi.check("ofrl_her_relabel_sources", ctx._lib.ofrl_her_relabel_sources(
+        ctx.handle, C.byref(r), C.byref(h), step, _ptr(src_idx, I32, "src_idx"), _ptr(is_weights, F32, "is_weights"),
+        C.byref(b), _ptr(is_weights_out, F32, "is_weights_out"), _stream(stream)))
+
+
+def episode_ends_append(ctx: Context, dones, first_index: int, episode_ends, num_episodes, stream=None):
+    """Append the exclusive end of every done transition among the n = dones.numel() new ones stored at
+    first_index.. to episode_ends (device int32, in order), growing the device counter num_episodes."""
+    _abi.check("ofrl_episode_ends_append", ctx._lib.ofrl_episode_ends_append(
+        ctx.handle, _ptr(dones, F32, "dones"), int(first_index), int(dones.numel()), _ptr(episode_ends, I32, "episode_ends"),
+        _ptr(num_episodes, I32, "num_episodes"), int(episode_ends.numel()), _stream(stream)))
 
 
 def iql_value_fwd_bwd(ctx: Context, params, states, q_taken, tau: float, v_out, loss_out, grad_out,

@@ -6,7 +6,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libofrl.so")
 
 OK, EINVAL, EUNSUPPORTED, ECUDA, ETIMEOUT = 0, -1, -2, -3, -4
-HER_FINAL, HER_FUTURE, HER_RANDOM = 0, 1, 2
+HER_FINAL, HER_FUTURE, HER_RANDOM, HER_EPISODE = 0, 1, 2, 3
 PREC_FP32, PREC_BF16 = 0, 1
 STAT_NONFINITE_GRAD, STAT_BAD_ACTION, STAT_BAD_INDEX, STAT_TIMEOUT, STAT_SANITIZED, STAT_WORDS = 0, 1, 2, 3, 4, 8
 
@@ -54,6 +54,9 @@ SIGNATURES = {
     "ofrl_status_string": (C.c_char_p, [C.c_int32]),
     "ofrl_workspace_bytes": (C.c_int64, [C.POINTER(VShape), C.c_int32, C.c_int32]),
     "ofrl_her_relabel": (C.c_int32, [vp, C.POINTER(Replay), C.POINTER(HerCfg), C.c_uint64, C.POINTER(Batch), vp]),
+    "ofrl_her_relabel_sources": (C.c_int32, [vp, C.POINTER(Replay), C.POINTER(HerCfg), C.c_uint64, vp, vp,
+                                             C.POINTER(Batch), vp, vp]),
+    "ofrl_episode_ends_append": (C.c_int32, [vp, vp, C.c_int64, C.c_int32, vp, vp, C.c_int32, vp]),
     "ofrl_iql_value_fwd_bwd": (C.c_int32, [vp, vp, vp, C.c_int32, C.c_int32, vp, C.c_float, vp, vp, vp, vp]),
     "ofrl_forward_values": (C.c_int32, [vp, vp, vp, C.c_int32, C.c_int32, vp, vp]),
     "ofrl_iql_target": (C.c_int32, [vp, vp, vp, C.c_int32, vp, vp, C.c_int32, C.c_float, vp, vp, vp]),

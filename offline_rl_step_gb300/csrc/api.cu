@@ -81,7 +81,8 @@ ofrl_status check_replay(const ofrl_replay* r, const ofrl_her_cfg* h) {
     if (r->state_dim > kMaxStateDim) return OFRL_EUNSUPPORTED;
     if (!aligned16(r->states) || !aligned16(r->next_states)) return OFRL_EINVAL;
     if (h->batch < 0 || h->her_count < 0 || h->her_count > h->batch) return OFRL_EINVAL;
-    if (h->strategy != OFRL_HER_FINAL && h->strategy != OFRL_HER_FUTURE && h->strategy != OFRL_HER_RANDOM)
+    if (h->strategy != OFRL_HER_FINAL && h->strategy != OFRL_HER_FUTURE && h->strategy != OFRL_HER_RANDOM &&
+        h->strategy != OFRL_HER_EPISODE)
         return OFRL_EINVAL;
     if (h->her_count > 0 && h->strategy != OFRL_HER_RANDOM) {
         if (r->episode_ends == nullptr || r->num_episodes < 1) return OFRL_EINVAL;
@@ -285,6 +286,32 @@ ofrl_status ofrl_her_relabel(ofrl_ctx* ctx, const ofrl_replay* replay, const ofr
     if ((int64_t)her->batch >= (1ll << 31)) return OFRL_EINVAL;
     const HerLaunch a = her_args(ctx, replay, her, step, out);
     return cuda_status(launch_her_relabel(a, static_cast<cudaStream_t>(stream)));
+}
+
+ofrl_status ofrl_her_relabel_sources(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl_her_cfg* her,
+                                     uint64_t step, const int32_t* src_idx, const float* is_weights,
+                                     const ofrl_batch* out, float* is_weights_out, void* stream) {
+    ofrl_status s = check_ctx(ctx);
+    if (s == OFRL_OK) s = check_replay(replay, her);
+    if (s == OFRL_OK) s = check_batch(out, replay->state_dim);
+    if (s != OFRL_OK) return s;
+    if (src_idx == nullptr || step >= (1ull << 32)) return OFRL_EINVAL;
+    HerLaunch a = her_args(ctx, replay, her, step, out);
+    a.src_in = src_idx;
+    a.isw_in = is_weights;
+    a.isw_out = is_weights_out;
+    return cuda_status(launch_her_relabel(a, static_cast<cudaStream_t>(stream)));
+}
+
+ofrl_status ofrl_episode_ends_append(ofrl_ctx* ctx, const float* dones, int64_t first_index, int32_t n,
+                                     int32_t* episode_ends, int32_t* num_episodes, int32_t max_episodes,
+                                     void* stream) {
+    ofrl_status s = check_ctx(ctx);
+    if (s != OFRL_OK) return s;
+    if (n < 0 || first_index < 0 || first_index + (int64_t)n > INT32_MAX || max_episodes < 0) return OFRL_EINVAL;
+    if (n > 0 && (!dones || !episode_ends || !num_episodes)) return OFRL_EINVAL;
+    return cuda_status(launch_episode_ends_append(dones, first_index, n, episode_ends, num_episodes, max_episodes,
+                                                  ctx->ws.status, static_cast<cudaStream_t>(stream)));
 }
 
 namespace {

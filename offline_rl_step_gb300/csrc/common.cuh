@@ -236,7 +236,15 @@ struct HerLaunch {
     int32_t pack_nets;
     const float* pack_params[kMaxNets];
     uint8_t* wimg;          // per network: W1 image then W2 image
+    // optional: caller-given sources (e.g. PER-sampled) and importance
+    // weights; HER rows get weight 1
+    const int32_t* src_in;  // [batch] or null: sources drawn here
+    const float* isw_in;    // [batch] or null: weight 1 for every row
+    float* isw_out;         // [batch] or null
 };
+cudaError_t launch_episode_ends_append(const float* dones, int64_t first_index, int32_t n, int32_t* episode_ends,
+                                       int32_t* num_episodes, int32_t max_episodes, int32_t* status,
+                                       cudaStream_t st);
 cudaError_t launch_her_relabel(const HerLaunch& a, cudaStream_t st);
 
 struct VnetLaunch {

@@ -101,9 +101,20 @@ __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerL
     const int row = live ? row_raw : a.batch - 1;   // dead half-warps shadow the last row, write nothing
     const uint64_t ctr = (a.step << 32) | ((uint64_t)row << 1);
 
-    // 1. source index, then the source rows' loads go out at once
-    int src = 0;
-    if (sub == 0) src = (int)below(sm64_at(a.seed, ctr), (uint64_t)a.capacity);
+    // 1. source index (drawn here, or the caller's), then the source rows'
+    // loads go out at once
+    int src = 0, bad = 0;
+    if (sub == 0) {
+        if (a.src_in != nullptr) {
+            src = __ldg(a.src_in + row);
+            if (src < 0 || src >= a.capacity) {   // flagged; the row stays inside the buffer
+                src = src < 0 ? 0 : a.capacity - 1;
+                bad = 1;
+            }
+        } else {
+            src = (int)below(sm64_at(a.seed, ctr), (uint64_t)a.capacity);
+        }
+    }
     src = __shfl_sync(kFull, src, 0, kLanesPerRow);
     const int chunks = a.copy_cols >> 2;   // <= 16 (state_dim <= 64)
     const bool has = sub < chunks;
@@ -122,19 +133,26 @@ __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerL
 
     // 2. donor (HER rows), overlapping the row loads
     const bool her = row >= a.first_her;
-    int donor = -1, bad = 0;
+    int donor = -1;
     if (a.strategy == OFRL_HER_RANDOM) {
         if (sub == 0 && her) donor = (int)below(sm64_at(a.seed, ctr | 1ull), (uint64_t)a.capacity);
     } else if (__any_sync(kFull, live && her)) {   // warp-uniform: only warps holding a HER row search
         const int k = episode_search(a.episode_ends, a.num_episodes, a.search_rounds, src, sub);
         if (sub == 0 && her) {
             int end = k < a.num_episodes ? __ldg(a.episode_ends + k) : a.capacity;
+            int start = k > 0 && k <= a.num_episodes ? __ldg(a.episode_ends + k - 1) : 0;
             if (k >= a.num_episodes || end > a.capacity || end <= src) {
                 end = a.capacity;   // malformed boundaries: flagged; the donor stays inside the buffer
                 bad = 1;
             }
+            if (start > src || start < 0) {
+                start = src;
+                bad = 1;
+            }
             if (a.strategy == OFRL_HER_FINAL) {
                 donor = end - 1;
+            } else if (a.strategy == OFRL_HER_EPISODE) {
+                donor = start + (int)below(sm64_at(a.seed, ctr | 1ull), (uint64_t)(end - start));
             } else {
                 const int lo = src + 1;
                 donor = lo < end ? lo + (int)below(sm64_at(a.seed, ctr | 1ull), (uint64_t)(end - lo)) : src;
@@ -195,11 +213,70 @@ __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerL
         a.out_rewards[row] = donor >= 0 ? r : rew;
         a.out_src[row] = src;
         a.out_donor[row] = donor;
+        if (a.isw_out != nullptr) a.isw_out[row] = her ? 1.0f : (a.isw_in != nullptr ? __ldg(a.isw_in + row) : 1.0f);
         if (bad) atomicAdd(a.status + OFRL_STAT_BAD_INDEX, 1);
     }
 }
 
+// Append the exclusive end (first_index + i + 1) of every transition i < n
+// with dones[i] != 0 to episode_ends, in ascending order, after the
+// *num_episodes entries already there ("GPU IQL + HER Porting Plan",
+// "Episode Boundary Tracking on GPU": the experience kernel records each
+// finished episode's end in a GPU-resident boundary array).  One CTA: thread
+// t scans its contiguous share of the new transitions, a block-wide
+// exclusive scan of the counts gives each thread its output position, so the
+// array stays sorted (the pages' atomicAdd slot order would not).  Ends past
+// max_episodes are dropped and counted as bad indices.
+constexpr int kAppendThreads = 1024;
+__global__ void __launch_bounds__(kAppendThreads) episode_ends_append_kernel(
+    const float* __restrict__ dones, int64_t first_index, int32_t n, int32_t* __restrict__ ends,
+    int32_t* __restrict__ count, int32_t max_ends, int32_t* __restrict__ status) {
+    __shared__ int warp_tot[kAppendThreads / 32];
+    __shared__ int base_s;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (n + kAppendThreads - 1) / kAppendThreads;
+    const int lo = tid * per < n ? tid * per : n;
+    const int hi = lo + per < n ? lo + per : n;
+    int c = 0;
+    for (int i = lo; i < hi; ++i) c += __ldg(dones + i) != 0.0f;
+    // inclusive scan inside the warp, then over the warp totals
+    int x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    if (tid == 0) base_s = *count;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += warp_tot[w];
+    int pos = base_s + before + x - c;   // exclusive prefix of this thread
+    int dropped = 0;
+    for (int i = lo; i < hi; ++i) {
+        if (__ldg(dones + i) != 0.0f) {
+            if (pos < max_ends) ends[pos] = (int32_t)(first_index + i + 1);
+            else ++dropped;
+            ++pos;
+        }
+    }
+    if (dropped) atomicAdd(status + OFRL_STAT_BAD_INDEX, dropped);
+    if (tid == kAppendThreads - 1) {
+        const int total = base_s + before + x;
+        *count = total < max_ends ? total : max_ends;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_episode_ends_append(const float* dones, int64_t first_index, int32_t n, int32_t* episode_ends,
+                                       int32_t* num_episodes, int32_t max_episodes, int32_t* status,
+                                       cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    episode_ends_append_kernel<<<1, kAppendThreads, 0, st>>>(dones, first_index, n, episode_ends, num_episodes,
+                                                             max_episodes, status);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_her_relabel(const HerLaunch& a_in, cudaStream_t st) {
     if (a_in.batch <= 0) return cudaSuccess;

@@ -17,11 +17,20 @@ Follows "GPU IQL + HER Porting Plan":
     compares next_states[source, :g] with next_states[donor, :g] in fp32
     (float accumulator, sqrtf, strict '<' against the threshold).
 
+  * "HER (CPU)" item 5 names a fourth strategy, Episode, without defining
+    it; "How HER Interacts with GPU PER": the HER rows' sources may come from
+    the PER sampler and their importance weights are 1 (no PER bias);
+    "Episode Boundary Tracking on GPU": each finished episode's end is
+    appended to the boundary array.
+
 Readings where the pages are open (each listed in the design notes):
   * episode_end is exclusive, so Final's donor is the last transition.
   * Future with an empty range (source is the episode's last transition)
     takes the source itself as donor.
   * Normal rows keep their stored reward and get donor index -1.
+  * Episode: the donor is uniform over the source's whole episode
+    [episode_start, episode_end), as the HER paper's "episode" strategy
+    (Andrychowicz et al. 2017); episode_start is the previous episode's end.
 """
 import bisect
 
@@ -29,8 +38,8 @@ import numpy as np
 
 from . import rng
 
-FINAL, FUTURE, RANDOM = 0, 1, 2
-STRATEGY = {"final": FINAL, "future": FUTURE, "random": RANDOM}
+FINAL, FUTURE, RANDOM, EPISODE = 0, 1, 2, 3
+STRATEGY = {"final": FINAL, "future": FUTURE, "random": RANDOM, "episode": EPISODE}
 
 
 def her_count(batch: int, her_ratio: float) -> int:
@@ -44,19 +53,27 @@ def episode_end(episode_ends, src: int) -> int:
     return int(episode_ends[k])
 
 
+def episode_start(episode_ends, src: int) -> int:
+    """First transition of the episode holding `src`: the previous episode's end, or 0."""
+    k = bisect.bisect_right(episode_ends, src)
+    return int(episode_ends[k - 1]) if k > 0 else 0
+
+
 def sample_indices(seed: int, step: int, batch: int, her_rows: int, strategy: int,
-                   capacity: int, episode_ends=None):
+                   capacity: int, episode_ends=None, sources=None):
     """Source and donor indices for one batch.
 
     Rows [0, batch - her_rows) are normal rows (donor -1); rows
     [batch - her_rows, batch) are HER rows with a donor by `strategy`.
+    `sources`: the caller's source of every row (e.g. PER-sampled) in place
+    of the drawn ones.
     """
     ends = None if episode_ends is None else [int(e) for e in episode_ends]
     src = np.empty(batch, dtype=np.int32)
     donor = np.full(batch, -1, dtype=np.int32)
     first_her = batch - her_rows
     for b in range(batch):
-        s = rng.below(rng.draw(seed, rng.counter(step, b, 0)), capacity)
+        s = int(sources[b]) if sources is not None else rng.below(rng.draw(seed, rng.counter(step, b, 0)), capacity)
         src[b] = s
         if b < first_her:
             continue
@@ -71,6 +88,9 @@ def sample_indices(seed: int, step: int, batch: int, her_rows: int, strategy: in
                 donor[b] = s
         elif strategy == RANDOM:
             donor[b] = rng.below(rng.draw(seed, rng.counter(step, b, 1)), capacity)
+        elif strategy == EPISODE:
+            lo, end = episode_start(ends, s), episode_end(ends, s)
+            donor[b] = lo + rng.below(rng.draw(seed, rng.counter(step, b, 1)), end - lo)
         else:
             raise ValueError(strategy)
     return src, donor
@@ -111,3 +131,19 @@ def relabel(replay: dict, src: np.ndarray, donor: np.ndarray, goal_dim: int,
         rew[her] = goal_reward(replay["next_states"], src[her], d, goal_dim, threshold)
     return dict(states=st, next_states=ns, actions=act, rewards=rew, dones=done,
                 src_idx=src.astype(np.int32), donor_idx=donor.astype(np.int32))
+
+
+def importance_weights(batch: int, her_rows: int, is_weights=None):
+    """Normal rows keep their (PER) importance weight; HER rows get 1 ("How
+    HER Interacts with GPU PER": uniform weight for HER samples, no PER bias)."""
+    w = np.ones(batch, dtype=np.float32) if is_weights is None else np.asarray(is_weights, np.float32).copy()
+    w[batch - her_rows:] = 1.0
+    return w
+
+
+def append_episode_ends(episode_ends, dones, first_index: int):
+    """The boundary array after n new transitions stored at first_index..:
+    each done transition i closes an episode ending (exclusively) at
+    first_index + i + 1, appended in order."""
+    new = [first_index + i + 1 for i, d in enumerate(np.asarray(dones)) if d != 0]
+    return list(episode_ends) + new

@@ -158,3 +158,72 @@ def test_anchor_workload_fires_both_branches():
     out = her.relabel(rep, src, donor, w.goal_dim, w.goal_threshold)
     frac = (out["rewards"][donor >= 0] == np.float32(1.0)).mean()
     assert 0.15 < frac < 0.25
+
+
+# ---- Episode strategy, caller-given sources, boundary maintenance ----------
+
+def _first_of_episode(episode_id, i):
+    # linear scan on episode ids: an independent way to find the episode start
+    j = i
+    while j > 0 and episode_id[j - 1] == episode_id[i]:
+        j -= 1
+    return j
+
+
+def test_episode_donors_stay_in_the_source_episode():
+    w, rep = _small("episode", ep=(5, 40))
+    n_her = her.her_count(w.batch, w.her_ratio)
+    src, donor = her.sample_indices(w.seed, 4, w.batch, n_her, her.EPISODE, w.capacity, rep["episode_ends"])
+    eid = rep["episode_id"]
+    before = after = 0
+    for b in range(w.batch - n_her, w.batch):
+        s, d = int(src[b]), int(donor[b])
+        assert _first_of_episode(eid, s) <= d <= _last_of_episode(eid, s)
+        assert eid[d] == eid[s]
+        before += d < s
+        after += d > s
+    # the whole episode is reachable: donors before and after the source
+    assert before > 0 and after > 0
+
+
+def test_episode_covers_the_whole_episode():
+    # 8-step episodes: from source 3 the donor is uniform on 0..7 of its episode
+    w, rep = _small("episode", cap=64, ep=(8, 8), batch=4096, ratio=1.0)
+    src, donor = her.sample_indices(w.seed, 0, w.batch, w.batch, her.EPISODE, w.capacity, rep["episode_ends"])
+    off = (donor - (src // 8) * 8)[src % 8 == 3]
+    assert set(off.tolist()) == set(range(8))
+
+
+def test_given_sources_are_used_and_donors_follow_them():
+    w, rep = _small("future", ep=(5, 40))
+    rng = np.random.default_rng(9)
+    given = rng.integers(0, w.capacity, w.batch).astype(np.int32)
+    n_her = her.her_count(w.batch, w.her_ratio)
+    src, donor = her.sample_indices(w.seed, 2, w.batch, n_her, her.FUTURE, w.capacity, rep["episode_ends"],
+                                    sources=given)
+    assert np.array_equal(src, given)
+    eid = rep["episode_id"]
+    for b in range(w.batch - n_her, w.batch):
+        s, d = int(src[b]), int(donor[b])
+        last = _last_of_episode(eid, s)
+        assert d == s if s == last else s + 1 <= d <= last
+
+
+def test_importance_weights_of_her_rows_are_one():
+    isw = np.linspace(0.1, 0.9, 10).astype(np.float32)
+    w = her.importance_weights(10, 3, isw)
+    assert np.array_equal(w[:7], isw[:7]) and (w[7:] == 1.0).all()
+    assert (her.importance_weights(5, 2) == 1.0).all()
+
+
+def test_boundary_append_rebuilds_the_buffer_ends():
+    # the generator builds episode_ends from episode lengths; appending its
+    # done flags (whole, or in two chunks) gives the same array
+    import dataclasses
+    w = dataclasses.replace(synth.TINY, capacity=3000, ep_len=(5, 40))
+    rep = synth.make_replay(w)
+    ends = [int(e) for e in rep["episode_ends"]]
+    assert her.append_episode_ends([], rep["dones"], 0) == ends
+    cut = 1234
+    part = her.append_episode_ends([], rep["dones"][:cut], 0)
+    assert her.append_episode_ends(part, rep["dones"][cut:], cut) == ends
