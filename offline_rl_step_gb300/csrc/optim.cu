@@ -252,7 +252,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineLaunch a) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i < a.n) {
         float g = 0.0f;
-        for (int k = 0; k < a.n_src; ++k) g = fmaf(a.scalars[SC_COEF0 + k], __ldg(a.src[k] + i), g);
+#pragma unroll
+        for (int k = 0; k < kMaxSrc; ++k)   // unrolled: the source pointers stay in registers
+            if (k < a.n_src) g = fmaf(a.scalars[SC_COEF0 + k], __ldg(a.src[k] + i), g);
         a.out[i] = g;
     }
     if (blockIdx.x == 0 && a.norms_out != nullptr) {
@@ -292,19 +294,19 @@ __global__ void __launch_bounds__(256) policy_kernel(const float* __restrict__ q
     if (b >= B) return;
     const float vb = __ldg(v + b);
     const float* qr = q + (int64_t)b * NA;
-    float z[kMaxActions];
+    // three passes over the row (no local array): max / argmax, sum of
+    // exponentials, outputs
     float zmax = -INFINITY, amax = -INFINITY;
     int best = 0;
     for (int k = 0; k < NA; ++k) {
         const float adv = fminf(fmaxf(__ldg(qr + k) - vb, -10.0f), 10.0f);
         if (adv > amax) { amax = adv; best = k; }
-        z[k] = beta * adv;
-        zmax = fmaxf(zmax, z[k]);
+        zmax = fmaxf(zmax, beta * adv);
     }
     float sum = 0.0f;
-    for (int k = 0; k < NA; ++k) { z[k] = expf(z[k] - zmax); sum += z[k]; }
+    for (int k = 0; k < NA; ++k) sum += expf(beta * fminf(fmaxf(__ldg(qr + k) - vb, -10.0f), 10.0f) - zmax);
     float* po = pi_out + (int64_t)b * NA;
-    for (int k = 0; k < NA; ++k) po[k] = z[k] / sum;
+    for (int k = 0; k < NA; ++k) po[k] = expf(beta * fminf(fmaxf(__ldg(qr + k) - vb, -10.0f), 10.0f) - zmax) / sum;
     if (argmax_out != nullptr) argmax_out[b] = best;
 }
 

@@ -123,10 +123,101 @@ __device__ __forceinline__ void gemm_tn_store(const float* A, int lda, int NI, c
     }
 }
 
-// FWD: forward only -- V of every row into v_out and, with target_out, the
-// IQL bootstrap target r + gamma (1 - done) V ("GPU IQL + HER Porting Plan",
-// "IQL modifies the target computation" and forward_values).
-template <int H, bool BF16, bool FWD>
+// The forward part shared by the training and the forward-only kernels: the
+// state tile into Xs (zero rows past the batch, zero columns past S), h1 =
+// relu(X W1^T + b1) into h1s, and z2 = h1 W2^T + b2 left in acc.
+template <int H, bool BF16>
+__device__ __forceinline__ void forward_tile(const VnetLaunch& a, float* Xs, float* h1s, float* wt,
+                                             float (&acc)[TileRows<H>::value / 8][H / 32]) {
+    constexpr int TM = TileRows<H>::value;
+    constexpr int RPT = TM / 8, CPT = H / 32;
+    const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
+    const int tile = blockIdx.x, net = blockIdx.y;
+    const int S = a.state_dim, B = a.batch;
+    const Offsets off = offsets_of(S, H);
+    const float* __restrict__ prm = a.params[net];
+    const int row0 = tile * TM;
+
+    for (int e = tid; e < TM * kXStride; e += kThreads) {
+        const int r = e / kXStride, k = e % kXStride;
+        float x = 0.0f;
+        if (k < S && row0 + r < B) x = __ldg(a.states + (int64_t)(row0 + r) * a.stride + k);
+        Xs[e] = op<BF16>(x);
+    }
+    // ---- layer 1: z1 = X W1^T + b1, h1 = relu(z1) ----
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+        const float bj = __ldg(prm + off.b1 + tx + 32 * j);
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) acc[i][j] = bj;
+    }
+    gemm_rows<H, TM, true, BF16>(acc, Xs, kXStride, prm + off.w1, S, wt);
+#pragma unroll
+    for (int i = 0; i < RPT; ++i)
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+            const float z = acc[i][j];
+            h1s[(ty + 8 * i) * H + tx + 32 * j] = op<BF16>(z < 0.0f ? 0.0f : z);
+        }
+    // ---- layer 2: z2 = h1 W2^T + b2 ----
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+        const float bj = __ldg(prm + off.b2 + tx + 32 * j);
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) acc[i][j] = bj;
+    }
+    gemm_rows<H, TM, true, BF16>(acc, h1s, H, prm + off.w2, H, wt);
+}
+
+// V forward only ("GPU IQL + HER Porting Plan", forward_values, and "IQL
+// modifies the target computation"): V of every row into v_out and, with
+// target_out, the IQL bootstrap target r + gamma (1 - done) V.
+template <int H, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1) vnet_forward_kernel(const VnetLaunch a) {
+    constexpr int TM = TileRows<H>::value;
+    constexpr int RPT = TM / 8, CPT = H / 32;
+    extern __shared__ float4 smem4[];
+    float* Xs = reinterpret_cast<float*>(smem4);   // [TM][kXStride]
+    float* h1s = Xs + TM * kXStride;               // [TM][H]
+    float* wt = h1s + 2 * TM * H + 2 * 8 * H;      // [kKChunk][H + 1] (same layout as the training kernel)
+    const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
+    const int net = blockIdx.y, B = a.batch;
+    const Offsets off = offsets_of(a.state_dim, H);
+    const float* __restrict__ prm = a.params[net];
+    const int row0 = blockIdx.x * TM;
+    pdl_trigger();
+    pdl_wait();
+    float acc[RPT][CPT];
+    forward_tile<H, BF16>(a, Xs, h1s, wt, acc);
+    float w3[CPT];
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) w3[j] = __ldg(prm + off.w3 + tx + 32 * j);
+    const float b3 = __ldg(prm + off.b3);
+    float vrow[RPT];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+        float s = 0.0f;
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+            const float h = acc[i][j] < 0.0f ? 0.0f : acc[i][j];
+            s = fmaf(h, w3[j], s);
+        }
+        vrow[i] = warp_sum(s) + b3;
+    }
+    if (tx < RPT) {
+        float myv = 0.0f;
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) if (tx == i) myv = vrow[i];
+        const int b = row0 + ty + 8 * tx;
+        if (b < B) {
+            if (a.v_out != nullptr) a.v_out[(int64_t)net * B + b] = myv;
+            if (a.target_out != nullptr)
+                a.target_out[(int64_t)net * B + b] = __ldg(a.rewards + b) + a.gamma * (1.0f - __ldg(a.dones + b)) * myv;
+        }
+    }
+}
+
+template <int H, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1) vnet_fwd_bwd_kernel(const VnetLaunch a) {
     constexpr int TM = TileRows<H>::value;
     constexpr int RPT = TM / 8, CPT = H / 32;
@@ -149,39 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_fwd_bwd_kernel(const VnetLau
     pdl_trigger();
     pdl_wait();
 
-    // ---- state tile (zero rows past the batch, zero columns past S) ----
-    for (int e = tid; e < TM * kXStride; e += kThreads) {
-        const int r = e / kXStride, k = e % kXStride;
-        float x = 0.0f;
-        if (k < S && row0 + r < B) x = __ldg(a.states + (int64_t)(row0 + r) * a.stride + k);
-        Xs[e] = op<BF16>(x);
-    }
-
     float acc[RPT][CPT];
-    // ---- layer 1: z1 = X W1^T + b1, h1 = relu(z1) ----
-#pragma unroll
-    for (int j = 0; j < CPT; ++j) {
-        const float bj = __ldg(prm + off.b1 + tx + 32 * j);
-#pragma unroll
-        for (int i = 0; i < RPT; ++i) acc[i][j] = bj;
-    }
-    gemm_rows<H, TM, true, BF16>(acc, Xs, kXStride, prm + off.w1, S, wt);
-#pragma unroll
-    for (int i = 0; i < RPT; ++i)
-#pragma unroll
-        for (int j = 0; j < CPT; ++j) {
-            const float z = acc[i][j];
-            h1s[(ty + 8 * i) * H + tx + 32 * j] = op<BF16>(z < 0.0f ? 0.0f : z);
-        }
-
-    // ---- layer 2: z2 = h1 W2^T + b2 ----
-#pragma unroll
-    for (int j = 0; j < CPT; ++j) {
-        const float bj = __ldg(prm + off.b2 + tx + 32 * j);
-#pragma unroll
-        for (int i = 0; i < RPT; ++i) acc[i][j] = bj;
-    }
-    gemm_rows<H, TM, true, BF16>(acc, h1s, H, prm + off.w2, H, wt);
+    forward_tile<H, BF16>(a, Xs, h1s, wt, acc);
 
     // ---- head: V = h2 w3 + b3, loss, dV, policy, dz2, dW3, db2, db3 ----
     float w3[CPT];
@@ -190,31 +250,6 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_fwd_bwd_kernel(const VnetLau
     const float b3 = __ldg(prm + off.b3);
     float vrow[RPT], dv[RPT];
     float loss_part = 0.0f, db3_part = 0.0f;
-    if constexpr (FWD) {
-#pragma unroll
-        for (int i = 0; i < RPT; ++i) {
-            float s = 0.0f;
-#pragma unroll
-            for (int j = 0; j < CPT; ++j) {
-                const float h = acc[i][j] < 0.0f ? 0.0f : acc[i][j];
-                s = fmaf(h, w3[j], s);
-            }
-            vrow[i] = warp_sum(s) + b3;
-        }
-        if (tx < RPT) {
-            float myv = 0.0f;
-#pragma unroll
-            for (int i = 0; i < RPT; ++i) if (tx == i) myv = vrow[i];
-            const int b = row0 + ty + 8 * tx;
-            if (b < B) {
-                if (a.v_out != nullptr) a.v_out[(int64_t)net * B + b] = myv;
-                if (a.target_out != nullptr)
-                    a.target_out[(int64_t)net * B + b] =
-                        __ldg(a.rewards + b) + a.gamma * (1.0f - __ldg(a.dones + b)) * myv;
-            }
-        }
-        return;
-    }
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
         float s = 0.0f;
@@ -259,21 +294,22 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_fwd_bwd_kernel(const VnetLau
         for (int i = 0; i < RPT; ++i) if (tx == i) myv = vrow[i];
         const int b = row0 + ty + 8 * tx;
         if (b < B) {
+            // three passes over the row of Q (no local array): max / argmax,
+            // sum of exponentials, outputs
             const float* qr = a.q + (int64_t)b * NA;
-            float z[kMaxActions];
             float zmax = -INFINITY;
             int best = 0;
             float amax = -INFINITY;
             for (int k = 0; k < NA; ++k) {
                 const float adv = fminf(fmaxf(__ldg(qr + k) - myv, -10.0f), 10.0f);
                 if (adv > amax) { amax = adv; best = k; }
-                z[k] = a.beta * adv;
-                zmax = fmaxf(zmax, z[k]);
+                zmax = fmaxf(zmax, a.beta * adv);
             }
             float sum = 0.0f;
-            for (int k = 0; k < NA; ++k) { z[k] = expf(z[k] - zmax); sum += z[k]; }
+            for (int k = 0; k < NA; ++k) sum += expf(a.beta * fminf(fmaxf(__ldg(qr + k) - myv, -10.0f), 10.0f) - zmax);
             float* po = a.pi_out + ((int64_t)net * B + b) * NA;
-            for (int k = 0; k < NA; ++k) po[k] = z[k] / sum;
+            for (int k = 0; k < NA; ++k)
+                po[k] = expf(a.beta * fminf(fmaxf(__ldg(qr + k) - myv, -10.0f), 10.0f) - zmax) / sum;
             if (a.argmax_out != nullptr) a.argmax_out[(int64_t)net * B + b] = best;
         }
     }
@@ -351,7 +387,7 @@ template <int H, bool BF16, bool FWD = false>
 cudaError_t launch_h(const VnetLaunch& a, cudaStream_t st) {
     constexpr int TM = TileRows<H>::value;
     const size_t smem = smem_floats<H, TM>() * sizeof(float);
-    auto kern = vnet_fwd_bwd_kernel<H, BF16, FWD>;
+    auto kern = FWD ? vnet_forward_kernel<H, BF16> : vnet_fwd_bwd_kernel<H, BF16>;
     static bool configured = false;   // per instantiation; setting it twice is harmless
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
