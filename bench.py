@@ -340,7 +340,7 @@ def run_ours(args, w):
                        "l2": f"inputs larger than L2: replay buffer {replay_bytes / 2**20:.0f} MiB read at "
                              f"random rows every step"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": 4 * args.steps, "clocks": clk, "status": status,
+            "gpu_launches": plan.kernels() * args.steps, "clocks": clk, "status": status,
         }
         print(json.dumps(line))
     ctx.close()

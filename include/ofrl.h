@@ -327,6 +327,14 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
                             float* v_out, float* pi_out, int32_t* argmax_out, float* loss_out,
                             float* norms_out, float* grad_out, void* stream);
 
+/* Kernel launches one ofrl_train_step on this context makes for `rows`
+ * batch rows and n_nets networks writing into `batch` (no counterpart on the
+ * pages: a planning aid for launch accounting and graph capture).  4
+ * (relabel, V, reduce, Adam), or 3 when the reduce and Adam run as one
+ * cooperative launch (its grid fits on the device at once).  Returns 0 for
+ * invalid arguments.  Host only; launches nothing. */
+int32_t ofrl_train_step_kernels(const ofrl_ctx* ctx, const ofrl_batch* batch, int32_t rows, int32_t n_nets);
+
 /* ---- allocation-free variant (no counterpart in the method's pages) ---- */
 
 /* Some callers may not allocate device memory: code whose GPU memory is

@@ -357,6 +357,10 @@ class StepPlan:
         for k in range(self.n_nets):
             self.nets[k].t = self.cn[k].t
 
+    def kernels(self) -> int:
+        """Kernel launches one run() makes (4, or 3 when the reduce and Adam run as one launch)."""
+        return int(self.ctx._lib.ofrl_train_step_kernels(self.ctx.handle, self.bp, self.h.batch, self.n_nets))
+
 
 def target_ema(params, target, polyak: float, stream=None):
     """target = (1 - polyak) target + polyak params, element-wise (Polyak averaging of a target network)."""
@@ -364,6 +368,12 @@ def target_ema(params, target, polyak: float, stream=None):
         raise ValueError("params and target differ in size")
     _abi.check("ofrl_target_ema", _abi.load().ofrl_target_ema(
         _ptr(params, F32, "params"), _ptr(target, F32, "target"), int(params.numel()), polyak, _stream(stream)))
+
+
+def train_step_kernels(ctx: Context, batch: Batch, rows: int, n_nets: int = 1) -> int:
+    """Kernel launches one train_step makes for this batch (4, or 3 when the reduce and Adam run as one launch)."""
+    b = batch.c()
+    return int(ctx._lib.ofrl_train_step_kernels(ctx.handle, C.byref(b), rows, n_nets))
 
 
 def profile_begin(ctx: Context, max_steps: int):

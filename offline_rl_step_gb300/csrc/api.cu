@@ -38,7 +38,7 @@ bool hidden_supported(int h) { return h == 64 || h == 128 || h == 256; }
 
 struct Layout {
     int64_t off_partials, off_tile_loss, off_g0, off_gram, off_scalars, off_counter, off_status, off_img, off_ximg,
-        total;
+        off_barrier, total;
     int32_t max_tiles;
     int64_t P;
 };
@@ -59,6 +59,7 @@ Layout layout_of(const ofrl_vshape* s, int32_t max_batch, int32_t max_nets) {
     L.off_status = take((int64_t)OFRL_STAT_WORDS * 4);
     L.off_img = take(s->hidden == 128 ? (int64_t)max_nets * vnet_tc_image_bytes() : 0);
     L.off_ximg = take(s->hidden == 128 ? (int64_t)L.max_tiles * tc::x_tile_bytes() : 0);
+    L.off_barrier = take(8);
     L.total = o;
     return L;
 }
@@ -235,6 +236,8 @@ ofrl_status ofrl_create(const ofrl_vshape* shape, int32_t max_batch, int32_t max
     ctx->ws.status = reinterpret_cast<int32_t*>(b + L.off_status);
     ctx->ws.img = reinterpret_cast<uint8_t*>(b + L.off_img);
     ctx->ws.ximg = reinterpret_cast<uint8_t*>(b + L.off_ximg);
+    ctx->ws.barrier = reinterpret_cast<unsigned long long*>(b + L.off_barrier);
+    ctx->barrier_arrivals = 0;
     if (cudaMemset(ctx->base, 0, (size_t)L.total) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
         cudaFree(ctx->base);
         delete ctx;
@@ -532,6 +535,29 @@ ofrl_status ofrl_adam_step(ofrl_ctx* ctx, float* p, const float* g, float* m, fl
     return cuda_status(launch_adam(a, st));
 }
 
+int32_t ofrl_train_step_kernels(const ofrl_ctx* ctx, const ofrl_batch* batch, int32_t rows, int32_t n_nets) {
+    if (ctx == nullptr || batch == nullptr || batch->states == nullptr) return 0;
+    if (rows < 1 || rows > ctx->max_batch || n_nets < 1 || n_nets > ctx->max_nets) return 0;
+    VnetLaunch v;
+    std::memset(&v, 0, sizeof(v));
+    v.n_nets = n_nets;
+    v.state_dim = ctx->shape.state_dim;
+    v.hidden = ctx->shape.hidden;
+    v.prec = ctx->shape.prec;
+    v.states = batch->states;
+    v.stride = batch->stride;
+    v.batch = rows;
+    const int tm = vnet_tile_rows(ctx->shape.hidden);
+    ReduceLaunch r;
+    std::memset(&r, 0, sizeof(r));
+    r.n_nets = n_nets;
+    r.P = ctx->n_params;
+    r.n_tiles = (rows + tm - 1) / tm;
+    r.n_parts = vnet_parts(v, r.n_tiles);
+    r.partials = ctx->ws.partials;
+    return reduce_adam_fusable(r) ? 3 : 4;
+}
+
 ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl_her_cfg* her, uint64_t step,
                             const ofrl_batch* batch, const float* q, ofrl_vnet* nets, int32_t n_nets,
                             const ofrl_opt* opt, const float* const* aux_src, int32_t n_aux, float* v_out,
@@ -645,9 +671,6 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
     r.loss_out = loss_out;
     r.sanitize = opt->sanitize_sources;
     r.status = ctx->ws.status;
-    e = launch_reduce_gram(r, st);
-    if (e != cudaSuccess) return OFRL_ECUDA;
-    prof_mark(ctx, 3, st);
 
     // 4. t += 1, then Adam with the safety clip
     AdamLaunch a;
@@ -675,8 +698,20 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
     a.weight_decay = opt->weight_decay;
     a.max_grad_norm = opt->max_grad_norm;
     a.status = ctx->ws.status;
-    e = launch_adam(a, st);
-    if (e != cudaSuccess) return OFRL_ECUDA;
+    // 3 + 4 in one cooperative launch when its grid fits on the device
+    // (a grid barrier between the reduce and Adam), else two launches
+    if (reduce_adam_fusable(r)) {
+        e = launch_reduce_adam(r, a, ctx->ws.barrier, ctx->barrier_arrivals, st);
+        if (e != cudaSuccess) return OFRL_ECUDA;
+        ctx->barrier_arrivals += (uint64_t)reduce_adam_blocks(r);
+        prof_mark(ctx, 3, st);
+    } else {
+        e = launch_reduce_gram(r, st);
+        if (e != cudaSuccess) return OFRL_ECUDA;
+        prof_mark(ctx, 3, st);
+        e = launch_adam(a, st);
+        if (e != cudaSuccess) return OFRL_ECUDA;
+    }
     prof_mark(ctx, 4, st);
     if (ctx->prof_events != nullptr && ctx->prof_count < ctx->prof_max) ctx->prof_count++;
     return OFRL_OK;

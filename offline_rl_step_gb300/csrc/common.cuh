@@ -39,6 +39,7 @@ struct Workspace {
     int32_t* status;      // [OFRL_STAT_WORDS]
     uint8_t* img;         // [max_nets] packed bf16 weight images for the tensor-core kernel
     uint8_t* ximg;        // [max_tiles] bf16 images of the relabelled state tiles
+    unsigned long long* barrier;  // grid-barrier arrival counter of the fused reduce + Adam (only grows)
 };
 
 }  // namespace ofrl
@@ -55,6 +56,7 @@ struct ofrl_ctx {
     void* base;           // the single cudaMalloc of the context
     int64_t bytes;
     ofrl::Workspace ws;
+    uint64_t barrier_arrivals;  // arrivals the launched fused kernels add to ws.barrier
     // measurement hooks: events[step][OFRL_PHASES + 1] while profiling
     cudaEvent_t* prof_events;
     int32_t prof_max;
@@ -145,6 +147,37 @@ inline cudaError_t launch_pdl(void (*kernel)(Arg0, Arg1), dim3 grid, dim3 block,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, a0, a1);
+}
+
+// Launch with programmatic dependent launch and, optionally, thread-block
+// clusters of `cluster` CTAs along x (cluster > 1) or a cooperative launch
+// (every CTA resident at once; the two are exclusive here).
+template <typename... Params, typename... Args>
+inline cudaError_t launch_ex(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             unsigned cluster, bool cooperative, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    unsigned n = 1;
+    if (cooperative) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    } else if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 // launch_pdl with thread-block clusters of `cluster` CTAs along x.
@@ -339,6 +372,13 @@ struct AdamLaunch {
 };
 cudaError_t launch_target_ema(const float* p, float* target, int64_t n, float polyak, cudaStream_t st);
 cudaError_t launch_adam(const AdamLaunch& a, cudaStream_t st);
+// Reduce + Gram + norms and Adam in one cooperative launch (a grid barrier
+// between them): possible when one pass of the reduce grid covers P and the
+// grid fits on the device at once.  barrier_base: arrivals before this launch.
+bool reduce_adam_fusable(const ReduceLaunch& r);
+int reduce_adam_blocks(const ReduceLaunch& r);   // CTAs of that launch
+cudaError_t launch_reduce_adam(const ReduceLaunch& r, const AdamLaunch& a, unsigned long long* barrier,
+                               unsigned long long barrier_base, cudaStream_t st);
 
 struct CombineLaunch {
     int64_t n;

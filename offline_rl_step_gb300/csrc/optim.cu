@@ -18,6 +18,8 @@
 // forms the combined gradient element by element and applies Adam, so the
 // combined gradient is never stored.  Every reduction is in a fixed order.
 
+#include <cstring>
+
 #include "common.cuh"
 #include "step_math.cuh"
 
@@ -50,8 +52,135 @@ __device__ __forceinline__ float4 sum_tiles(const float* __restrict__ pp, int64_
     return make_float4(s0.x + s1.x, s0.y + s1.y, s0.z + s1.z, s0.w + s1.w);
 }
 
+// (j, k) of Gram entry p (gram_index order)
+__device__ __forceinline__ int pair_j(int p) { return p < 4 ? 0 : p < 7 ? 1 : p < 9 ? 2 : 3; }
+__device__ __forceinline__ int pair_k(int p) {
+    return p < 4 ? p : p < 7 ? p - 3 : p < 9 ? p - 5 : 3;
+}
+
+// The tail of the fused reduce + Adam launch (see below).
 template <int EL>
-__global__ void __launch_bounds__(kRedThreads, EL == 8 ? 5 : 4) reduce_gram_kernel(const ReduceLaunch a) {
+__device__ __forceinline__ void fused_norms_adam(const ReduceLaunch& a, const AdamLaunch& d, unsigned long long* bar,
+                                                 unsigned long long bar_target, const float (&gacc)[kGramPairs],
+                                                 const float (&x)[kMaxSrc][4]) {
+    constexpr int kRedElems = 4 * EL;
+    const int tid = threadIdx.x, tx = tid % EL, ty = tid / EL, lane = tid & 31, wid = tid >> 5;
+    const int net = blockIdx.y, G = gridDim.x, nsrc = a.n_src;
+    const int64_t P = a.P;
+    const int64_t i4 = (int64_t)blockIdx.x * kRedElems + 4 * tx;
+    // this lane's weights and moments, read before the barrier (only this
+    // block writes them)
+    float pv[4], mv[4], vv[4];
+    if (ty == 0) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (i4 + e < P) {
+                pv[e] = d.p[net][i4 + e];
+                mv[e] = d.m[net][i4 + e];
+                vv[e] = d.v[net][i4 + e];
+            }
+    }
+    float* gp = a.gram_part + ((int64_t)net * G + blockIdx.x) * kGramPairs;
+    if (wid == 0) {
+#pragma unroll
+        for (int p = 0; p < kGramPairs; ++p) {
+            if (pair_j(p) >= nsrc || pair_k(p) >= nsrc) continue;
+            const float s = warp_sum(gacc[p]);
+            if (lane == 0) gp[p] = s;
+        }
+    }
+    const bool ok = grid_barrier(bar, bar_target, 1000000000ull);
+
+    // totals of the Gram entries present and of the loss, the same fixed
+    // order in every block: lanes stride the blocks, then one butterfly
+    __shared__ float totals[kGramPairs + 1];
+    const float* gall = a.gram_part + (int64_t)net * G * kGramPairs;
+    for (int item = wid; item <= kGramPairs; item += kRedThreads / 32) {
+        const bool need = item == kGramPairs ? a.tile_loss != nullptr
+                                             : pair_j(item) < nsrc && pair_k(item) < nsrc;
+        float v = 0.0f;
+        if (need) {
+            const int n = item == kGramPairs ? a.n_tiles : G;
+            for (int b0 = lane; b0 < n; b0 += 8 * 32) {
+                float u[8];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int b = b0 + 32 * r;
+                    u[r] = b >= n ? 0.0f
+                                  : item == kGramPairs ? __ldcg(a.tile_loss + (int64_t)net * a.net_tile_stride + b)
+                                                       : __ldcg(gall + (int64_t)b * kGramPairs + item);
+                }
+#pragma unroll
+                for (int r = 0; r < 8; ++r) v += u[r];
+            }
+            v = warp_sum(v);
+        }
+        if (lane == 0) totals[item] = v;
+    }
+    __syncthreads();
+    float gram[kGramPairs];
+#pragma unroll
+    for (int p = 0; p < kGramPairs; ++p) gram[p] = totals[p];
+    const NormResult r = finish_norms(gram, totals[kGramPairs], nsrc, a.budget, a.alpha, a.max_grad_norm, a.inv_batch);
+    if (blockIdx.x == 0 && tid == 0) {
+        float* sc = a.scalars + (int64_t)net * kScalars;
+#pragma unroll
+        for (int k = 0; k < kMaxSrc; ++k) {
+            sc[SC_NORM0 + k] = r.nrm[k];
+            sc[SC_COEF0 + k] = r.coef[k];
+        }
+        sc[SC_COMBINED] = r.combined;
+        sc[SC_LOSS] = r.loss;
+        if (a.norms_out != nullptr) {
+#pragma unroll
+            for (int k = 0; k < kMaxSrc; ++k) a.norms_out[net * 5 + k] = r.nrm[k];
+            a.norms_out[net * 5 + 4] = r.combined;
+        }
+        if (a.loss_out != nullptr) a.loss_out[net] = r.loss;
+    }
+
+    // the clipped combination and Adam on this lane's elements (the sources
+    // in x are already the guarded ones when sanitize is on)
+    int bad = 0;
+    if (ty == 0) {
+        const float s = clip_scale(r.combined, d.max_grad_norm);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int64_t i = i4 + e;
+            if (i >= P) continue;
+            float gsum = 0.0f;
+#pragma unroll
+            for (int k = 0; k < kMaxSrc; ++k)
+                if (k < nsrc) gsum = fmaf(r.coef[k], x[k][e], gsum);
+            const float g = s * gsum;
+            float p = pv[e], m = mv[e], v = vv[e];
+            if (adam_element(p, m, v, g, d.beta1, d.beta2, d.eps, d.weight_decay, d.lr[net], d.bc1[net], d.bc2[net])) {
+                if (d.clamp > 0.0f) p = fminf(fmaxf(p, -d.clamp), d.clamp);
+                d.m[net][i] = m;
+                d.v[net][i] = v;
+                d.p[net][i] = p;
+            } else {
+                ++bad;
+            }
+            if (d.target[net] != nullptr) {
+                const float pk = d.polyak[net];
+                d.target[net][i] = (1.0f - pk) * d.target[net][i] + pk * p;
+            }
+        }
+    }
+    if (bad) atomicAdd(d.status + OFRL_STAT_NONFINITE_GRAD, bad);
+    if (!ok && tid == 0) atomicAdd(d.status + OFRL_STAT_TIMEOUT, 1);
+}
+
+// ADAM: one cooperative launch does the reduce and Adam.  One pass of the
+// grid covers P; after the block's Gram partial a grid barrier; then every
+// block forms the totals, norms and coefficients in the same fixed order and
+// applies the clipped combination and Adam to its own elements, which its
+// element lanes still hold.
+template <int EL, bool ADAM>
+__global__ void __launch_bounds__(kRedThreads, ADAM ? 3 : (EL == 8 ? 5 : 4))
+    reduce_gram_kernel(const ReduceLaunch a, const AdamLaunch d, unsigned long long* bar,
+                       unsigned long long bar_target) {
     constexpr int TL = kRedThreads / EL, kRedElems = 4 * EL;
     __shared__ float4 sh[TL][EL + 1];
     __shared__ unsigned int ticket;
@@ -67,10 +196,10 @@ __global__ void __launch_bounds__(kRedThreads, EL == 8 ? 5 : 4) reduce_gram_kern
     float gacc[kGramPairs];
 #pragma unroll
     for (int p = 0; p < kGramPairs; ++p) gacc[p] = 0.0f;
+    float x[kMaxSrc][4];   // (after the loop: this lane's elements, for the fused Adam)
 
     for (int64_t base = (int64_t)blockIdx.x * kRedElems; base < P; base += (int64_t)gridDim.x * kRedElems) {
         const int64_t i4 = base + 4 * tx;
-        float x[kMaxSrc][4];
 #pragma unroll
         for (int k = 0; k < kMaxSrc; ++k)
 #pragma unroll
@@ -124,6 +253,10 @@ __global__ void __launch_bounds__(kRedThreads, EL == 8 ? 5 : 4) reduce_gram_kern
                     for (int k = j; k < kMaxSrc; ++k)
                         gacc[gram_index(j, k)] = fmaf(x[j][e], x[k][e], gacc[gram_index(j, k)]);
         }
+    }
+    if constexpr (ADAM) {
+        fused_norms_adam<EL>(a, d, bar, bar_target, gacc, x);
+        return;
     }
     float* gp = a.gram_part + ((int64_t)net * gridDim.x + blockIdx.x) * kGramPairs;
     // the element lanes (ty == 0) are lanes 0..EL-1 of warp 0; the rest hold zeros.
@@ -317,22 +450,78 @@ int reduce_grid(int64_t P, int el) {
     return (int)(g < kMaxGramBlocks ? (g < 1 ? 1 : g) : kMaxGramBlocks);
 }
 
+template <int EL, bool ADAM>
+cudaError_t configure_reduce() {
+    static cudaError_t state = cudaErrorNotReady;
+    if (state == cudaErrorNotReady) state = set_max_shared_carveout(reduce_gram_kernel<EL, ADAM>);
+    return state;
+}
+
 template <int EL>
 cudaError_t launch_reduce_el(const ReduceLaunch& a, cudaStream_t st) {
-    static bool configured = false;
-    if (!configured) {
-        const cudaError_t e = set_max_shared_carveout(reduce_gram_kernel<EL>);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    const cudaError_t e = configure_reduce<EL, false>();
+    if (e != cudaSuccess) return e;
     const dim3 grid(reduce_grid(a.P, EL), a.n_nets);
-    return launch_pdl(reduce_gram_kernel<EL>, grid, dim3(kRedThreads), 0, st, a);
+    AdamLaunch none;
+    memset(&none, 0, sizeof(none));
+    return launch_ex(reduce_gram_kernel<EL, false>, grid, dim3(kRedThreads), 0, st, 1u, false, a, none,
+                     (unsigned long long*)nullptr, 0ull);
+}
+
+int reduce_el(const ReduceLaunch& a) {
+    const int parts = a.n_parts > 0 ? a.n_parts : a.n_tiles;
+    return a.partials != nullptr && parts <= kManyParts ? 32 : 8;
+}
+
+// CTAs of the fused kernel resident at once on the current device (0
+// without cooperative launch support).
+template <int EL>
+int max_resident_reduce_adam() {
+    static int n = -1;
+    if (n < 0) {
+        n = 0;
+        int dev = 0, coop = 0, sms = 0, per_sm = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop &&
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+            configure_reduce<EL, true>() == cudaSuccess &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reduce_gram_kernel<EL, true>, kRedThreads, 0) ==
+                cudaSuccess)
+            n = per_sm * sms;
+        cudaGetLastError();
+    }
+    return n;
 }
 
 cudaError_t launch_reduce_gram(const ReduceLaunch& a, cudaStream_t st) {
-    const int parts = a.n_parts > 0 ? a.n_parts : a.n_tiles;
-    if (a.partials != nullptr && parts <= kManyParts) return launch_reduce_el<32>(a, st);
-    return launch_reduce_el<8>(a, st);
+    return reduce_el(a) == 32 ? launch_reduce_el<32>(a, st) : launch_reduce_el<8>(a, st);
+}
+
+int reduce_adam_blocks(const ReduceLaunch& r) { return reduce_grid(r.P, reduce_el(r)) * r.n_nets; }
+
+bool reduce_adam_fusable(const ReduceLaunch& r) {
+    if (r.partials == nullptr) return false;
+    const int el = reduce_el(r);
+    const int64_t per_pass = (int64_t)reduce_grid(r.P, el) * 4 * el;
+    if (per_pass < r.P) return false;   // one pass of the grid must cover P
+    const int resident = el == 32 ? max_resident_reduce_adam<32>() : max_resident_reduce_adam<8>();
+    return reduce_adam_blocks(r) <= resident;
+}
+
+cudaError_t launch_reduce_adam(const ReduceLaunch& r, const AdamLaunch& a, unsigned long long* barrier,
+                               unsigned long long barrier_base, cudaStream_t st) {
+    const int el = reduce_el(r);
+    const dim3 grid(reduce_grid(r.P, el), r.n_nets);
+    const unsigned long long target = barrier_base + (unsigned long long)grid.x * grid.y;
+    if (el == 32) {
+        const cudaError_t e = configure_reduce<32, true>();
+        if (e != cudaSuccess) return e;
+        return launch_ex(reduce_gram_kernel<32, true>, grid, dim3(kRedThreads), 0, st, 1u, true, r, a, barrier,
+                         target);
+    }
+    const cudaError_t e = configure_reduce<8, true>();
+    if (e != cudaSuccess) return e;
+    return launch_ex(reduce_gram_kernel<8, true>, grid, dim3(kRedThreads), 0, st, 1u, true, r, a, barrier, target);
 }
 
 cudaError_t launch_adam(const AdamLaunch& a, cudaStream_t st) {

@@ -1,6 +1,7 @@
 // Device arithmetic of the reduce and Adam kernels: turning the Gram matrix
 // of the gradient sources into norms, clip coefficients and the combined
-// norm; one Adam element.
+// norm; one Adam element; a bounded grid barrier for the cooperative launch
+// that does both.
 //
 // Method: "Gradient Stability -- Multi-Task Gradient Isolation + Full
 // Spectral Norm", "Proper design" (each source clipped to its budget
@@ -63,6 +64,40 @@ __device__ __forceinline__ bool adam_element(float& p, float& m, float& v, float
     const float vhat = v / bc2;
     p = p - lr * (mhat / (sqrtf(vhat) + eps) + weight_decay * p);
     return true;
+}
+
+// Grid-wide barrier of a cooperative launch (every CTA resident).  The
+// arrival counter only grows: barrier k of the context's history completes
+// when it reaches `target` = (k + 1) * CTAs, so a CTA that gave up waiting
+// (after limit_ns; returns false) still arrives exactly once and later
+// barriers stay consistent.  All threads of the CTA call it.
+__device__ __forceinline__ bool grid_barrier(unsigned long long* count, unsigned long long target,
+                                             uint64_t limit_ns) {
+    __shared__ int ok_s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(count, 1ull);
+        const volatile unsigned long long* c = count;
+        bool ok = true;
+        if (*c < target) {
+            uint64_t t0;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+            while (*c < target) {
+                __nanosleep(32);
+                uint64_t t;
+                asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+                if (t - t0 > limit_ns) {
+                    ok = false;
+                    break;
+                }
+            }
+        }
+        __threadfence();
+        ok_s = ok ? 1 : 0;
+    }
+    __syncthreads();
+    return ok_s != 0;
 }
 
 }  // namespace ofrl

@@ -148,6 +148,9 @@ class GpuStep:
                     params=[cpu(n.params) for n in self.nets],
                     target=[cpu(n.target) if n.target is not None else None for n in self.nets])
 
+    def kernels(self):
+        return self.ofrl.train_step_kernels(self.ctx, self.batch, self.w.batch, self.w.n_nets)
+
     def close(self):
         self.ctx.close()
 

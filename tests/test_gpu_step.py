@@ -226,3 +226,17 @@ def test_step_with_source_guard_weight_bound_and_target():
         assert st["nonfinite_grad"] == 0, st
     finally:
         g.close()
+
+
+def test_reduce_and_adam_launch_fusion_choice():
+    # the production batch (128 tiles, 32 cluster partials, 182 reduce
+    # blocks) takes the single cooperative reduce + Adam launch; the
+    # H = 256 workload (256 tiles of 64 rows) needs more reduce blocks than
+    # fit at once and keeps two launches
+    need_gpu()
+    for w, expect in ((synth.PROD, 3), (dataclasses.replace(synth.BUDGETED, capacity=1 << 16), 4)):
+        g = GpuStep(w)
+        try:
+            assert g.kernels() == expect, w.name
+        finally:
+            g.close()
