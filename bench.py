@@ -337,6 +337,7 @@ def run_ours(args, w):
             "config": {"workload": w.name, "batch": w.batch, "state_dim": w.state_dim, "hidden": w.hidden,
                        "num_actions": w.num_actions, "n_nets": w.n_nets, "her": f"{w.strategy} {w.her_ratio}",
                        "capacity": w.capacity, "parallelism": f"replicas{world}",
+                       "launch": "direct kernel launches chained by programmatic dependent launch",
                        "l2": f"inputs larger than L2: replay buffer {replay_bytes / 2**20:.0f} MiB read at "
                              f"random rows every step"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,

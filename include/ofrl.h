@@ -335,6 +335,30 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
  * invalid arguments.  Host only; launches nothing. */
 int32_t ofrl_train_step_kernels(const ofrl_ctx* ctx, const ofrl_batch* batch, int32_t rows, int32_t n_nets);
 
+/* ---- the step as a CUDA graph ------------------------------------------
+ * "Phase 2: Multi-Stream Graph Parallelism" runs the trainers' step as a
+ * captured CUDA graph.  ofrl_step_graph_create captures one ofrl_train_step
+ * with these arguments (all of them checked as ofrl_train_step checks them;
+ * nothing runs) and instantiates it.  ofrl_step_graph_launch replays it on
+ * `stream` as the step `step`: the relabel uses `step`; q (device [B, A], or
+ * NULL to keep the previous one) and aux_src (host array of n_nets * n_aux
+ * device pointers, or NULL to keep the previous ones) replace the captured
+ * pointers; each network's t advances by one in the caller's `nets` array
+ * (which must outlive the graph), exactly as ofrl_train_step would.  Every
+ * other buffer is the one given at creation.  One graph launch on the host
+ * per step.  The graph uses the context's workspace: do not interleave its
+ * replays with other calls on the context from another stream.  Profiling
+ * hooks (ofrl_profile_begin) must be off while creating one. */
+typedef struct ofrl_step_graph ofrl_step_graph;
+ofrl_status ofrl_step_graph_create(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl_her_cfg* her,
+                                   const ofrl_batch* batch, const float* q, ofrl_vnet* nets, int32_t n_nets,
+                                   const ofrl_opt* opt, const float* const* aux_src, int32_t n_aux,
+                                   float* v_out, float* pi_out, int32_t* argmax_out, float* loss_out,
+                                   float* norms_out, float* grad_out, ofrl_step_graph** out);
+ofrl_status ofrl_step_graph_launch(ofrl_step_graph* graph, uint64_t step, const float* q,
+                                   const float* const* aux_src, void* stream);
+ofrl_status ofrl_step_graph_destroy(ofrl_step_graph* graph);
+
 /* ---- allocation-free variant (no counterpart in the method's pages) ---- */
 
 /* Some callers may not allocate device memory: code whose GPU memory is

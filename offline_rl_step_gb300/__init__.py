@@ -370,6 +370,67 @@ def target_ema(params, target, polyak: float, stream=None):
         _ptr(params, F32, "params"), _ptr(target, F32, "target"), int(params.numel()), polyak, _stream(stream)))
 
 
+class StepGraph:
+    """train_step captured once as a CUDA graph; launch() replays it as a given step.
+
+    Same semantics as train_step: per launch the step index, and optionally the Q tensor and the auxiliary
+    sources, change; each network's t advances.  Every other tensor is the one given here (keep them alive).
+    One graph launch on the host per step.
+    """
+
+    def __init__(self, ctx: Context, replay: Replay, her: HerConfig, batch: Batch, nets: List[VNet], opt: Opt, q,
+                 aux=None, v_out=None, pi_out=None, argmax_out=None, loss_out=None, norms_out=None, grad_out=None):
+        self.ctx, self.nets = ctx, nets
+        self._keep = [replay, batch, nets, q, aux, v_out, pi_out, argmax_out, loss_out, norms_out, grad_out]
+        self.r, self.h, self.b, self.o = replay.c(), her.c(), batch.c(), opt.c()
+        self.n_nets = len(nets)
+        self.cn = (_abi.VNet * self.n_nets)(*[x.c() for x in nets])
+        self.n_aux = 0 if not aux else len(aux[0])
+        self.aux_arr = (C.c_void_p * max(1, self.n_nets * self.n_aux))()
+        if self.n_aux:
+            for i, t in enumerate(t for per in aux for t in per):
+                self.aux_arr[i] = _ptr(t, F32, "aux").value
+        handle = C.c_void_p()
+        _abi.check("ofrl_step_graph_create", ctx._lib.ofrl_step_graph_create(
+            ctx.handle, C.byref(self.r), C.byref(self.h), C.byref(self.b), _ptr(q, F32, "q"), self.cn, self.n_nets,
+            C.byref(self.o), self.aux_arr if self.n_aux else None, self.n_aux, _ptr(v_out, F32, "v_out"),
+            _ptr(pi_out, F32, "pi_out"), _ptr(argmax_out, I32, "argmax_out"), _ptr(loss_out, F32, "loss_out"),
+            _ptr(norms_out, F32, "norms_out"), _ptr(grad_out, F32, "grad_out"), C.byref(handle)))
+        self.handle = handle
+        self.fn = ctx._lib.ofrl_step_graph_launch
+
+    def launch(self, step: int, q=None, aux=None, stream=None):
+        arr = None
+        if aux is not None:
+            self._keep.append(aux)
+            for i, t in enumerate(t for per in aux for t in per):
+                self.aux_arr[i] = t.data_ptr()
+            arr = self.aux_arr
+        if q is not None:
+            self._keep[3] = q
+        code = self.fn(self.handle, step, C.c_void_p(q.data_ptr()) if q is not None else None, arr,
+                       _stream(stream))
+        if code != _abi.OK:
+            _abi.check("ofrl_step_graph_launch", code)
+        if len(self._keep) > 64:
+            del self._keep[11:-8]
+
+    def sync_t(self):
+        for k in range(self.n_nets):
+            self.nets[k].t = self.cn[k].t
+
+    def close(self):
+        if self.handle:
+            self.ctx._lib.ofrl_step_graph_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 def train_step_kernels(ctx: Context, batch: Batch, rows: int, n_nets: int = 1) -> int:
     """Kernel launches one train_step makes for this batch (4, or 3 when the reduce and Adam run as one launch)."""
     b = batch.c()

@@ -184,12 +184,12 @@ int vnet_parts(const VnetLaunch& v, int n_tiles) {
     return vnet_tc_supported(v) ? n_tiles / vnet_tc_cluster(n_tiles) : n_tiles;
 }
 
-void bias_corrections(float beta1, float beta2, int32_t t, float* bc1, float* bc2) {
+}  // namespace
+
+void ofrl::bias_corrections(float beta1, float beta2, int32_t t, float* bc1, float* bc2) {
     *bc1 = (float)(1.0 - std::pow((double)beta1, (double)t));
     *bc2 = (float)(1.0 - std::pow((double)beta2, (double)t));
 }
-
-}  // namespace
 
 extern "C" {
 

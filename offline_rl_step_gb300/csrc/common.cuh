@@ -372,6 +372,8 @@ struct AdamLaunch {
 };
 cudaError_t launch_target_ema(const float* p, float* target, int64_t n, float polyak, cudaStream_t st);
 cudaError_t launch_adam(const AdamLaunch& a, cudaStream_t st);
+// Adam bias corrections 1 - beta^t, computed in double and rounded to float.
+void bias_corrections(float beta1, float beta2, int32_t t, float* bc1, float* bc2);
 // Reduce + Gram + norms and Adam in one cooperative launch (a grid barrier
 // between them): possible when one pass of the reduce grid covers P and the
 // grid fits on the device at once.  barrier_base: arrivals before this launch.

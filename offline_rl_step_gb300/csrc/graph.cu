@@ -1,0 +1,230 @@
+// The fused train step captured once as a CUDA graph and replayed.
+//
+// Method: "Phase 2: Multi-Stream Graph Parallelism" runs the trainers' step
+// as a captured CUDA graph; here the captured graph is one ofrl_train_step
+// (relabel, V forward/backward, reduce + norms + Adam, with their
+// programmatic dependent launches, cluster and cooperative attributes).  A
+// replay costs one graph launch on the host instead of three or four kernel
+// launches.  What changes from step to step is patched into the
+// instantiated graph's kernel nodes before each replay: the relabel's step
+// index, the V kernel's Q pointer, the auxiliary-source pointers, Adam's bias
+// corrections and the fused kernel's grid-barrier target.  Each node's first
+// arguments are the launch structs the kernels take (HerLaunch; VnetLaunch;
+// ReduceLaunch, AdamLaunch, barrier, target; AdamLaunch), so the fields are
+// patched in copies of the captured arguments.
+
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+#include "../../include/ofrl.h"
+
+struct ofrl_step_graph {
+    ofrl_ctx* ctx;
+    ofrl_vnet* nets;          // caller's array: t advances here
+    int32_t n_nets, n_aux;
+    float beta1, beta2;
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+    cudaGraphNode_t node[4];
+    int n_nodes;              // 3: relabel, V, reduce + Adam; 4: ..., reduce, Adam
+    // the captured arguments of each node (copies patched before a replay)
+    ofrl::HerLaunch her;
+    ofrl::VnetLaunch vnet;
+    std::vector<uint8_t> vnet_args;   // the V kernel's second argument (tensor-core kernel), if any
+    ofrl::ReduceLaunch red;
+    ofrl::AdamLaunch red_adam;
+    unsigned long long* bar;
+    unsigned long long bar_target;
+    ofrl::AdamLaunch adam;
+    uint64_t barrier_arrivals;        // arrivals one replay adds (fused reduce + Adam)
+};
+
+using namespace ofrl;
+
+extern "C" ofrl_status ofrl_step_graph_create(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl_her_cfg* her,
+                                              const ofrl_batch* batch, const float* q, ofrl_vnet* nets,
+                                              int32_t n_nets, const ofrl_opt* opt, const float* const* aux_src,
+                                              int32_t n_aux, float* v_out, float* pi_out, int32_t* argmax_out,
+                                              float* loss_out, float* norms_out, float* grad_out,
+                                              ofrl_step_graph** out) {
+    if (ctx == nullptr || out == nullptr || nets == nullptr || opt == nullptr) return OFRL_EINVAL;
+    if (ctx->prof_events != nullptr) return OFRL_EINVAL;   // no profiling hooks inside a capture
+    *out = nullptr;
+    cudaStream_t st = nullptr;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return OFRL_ECUDA;
+    std::vector<int32_t> t0(n_nets > 0 ? n_nets : 0);
+    for (int k = 0; k < n_nets; ++k) t0[k] = nets[k].t;
+    const uint64_t arrivals0 = ctx->barrier_arrivals;
+
+    // capture one step (every argument check of ofrl_train_step applies)
+    if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        cudaStreamDestroy(st);
+        return OFRL_ECUDA;
+    }
+    const ofrl_status s = ofrl_train_step(ctx, replay, her, 0, batch, q, nets, n_nets, opt, aux_src, n_aux, v_out,
+                                          pi_out, argmax_out, loss_out, norms_out, grad_out, st);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ec = cudaStreamEndCapture(st, &graph);
+    cudaStreamDestroy(st);
+    // the capture launched nothing: t and the barrier count are as before
+    for (int k = 0; k < n_nets; ++k) nets[k].t = t0[k];
+    const uint64_t per_replay = ctx->barrier_arrivals - arrivals0;
+    ctx->barrier_arrivals = arrivals0;
+    if (s != OFRL_OK || ec != cudaSuccess || graph == nullptr) {
+        if (graph) cudaGraphDestroy(graph);
+        return s != OFRL_OK ? s : OFRL_ECUDA;
+    }
+
+    ofrl_step_graph* g = new (std::nothrow) ofrl_step_graph();
+    if (g == nullptr) {
+        cudaGraphDestroy(graph);
+        return OFRL_ECUDA;
+    }
+    g->ctx = ctx;
+    g->nets = nets;
+    g->n_nets = n_nets;
+    g->n_aux = n_aux;
+    g->beta1 = opt->beta1;
+    g->beta2 = opt->beta2;
+    g->graph = graph;
+    g->barrier_arrivals = per_replay;
+    // the kernel nodes, in launch order (a captured stream is a chain)
+    size_t n = 0;
+    cudaGraphGetNodes(graph, nullptr, &n);
+    std::vector<cudaGraphNode_t> nodes(n);
+    bool ok = n >= 3 && n <= 4 && cudaGraphGetNodes(graph, nodes.data(), &n) == cudaSuccess;
+    // order by the chain: the node without dependencies first (the queries
+    // take edge data: programmatic-launch edges carry it)
+    std::vector<cudaGraphNode_t> chain;
+    if (ok) {
+        cudaGraphNode_t cur = nullptr;
+        for (cudaGraphNode_t nd : nodes) {
+            cudaGraphNode_t dep[8];
+            cudaGraphEdgeData edge[8];
+            size_t deps = 8;
+            if (cudaGraphNodeGetDependencies(nd, dep, edge, &deps) != cudaSuccess) ok = false;
+            else if (deps == 0) cur = nd;
+        }
+        while (ok && cur != nullptr && chain.size() < n) {
+            chain.push_back(cur);
+            cudaGraphNode_t next[8];
+            cudaGraphEdgeData edge[8];
+            size_t nd = 8;
+            if (cudaGraphNodeGetDependentNodes(cur, next, edge, &nd) != cudaSuccess || nd > 1) break;
+            cur = nd == 1 ? next[0] : nullptr;
+        }
+        ok = ok && chain.size() == n;
+    }
+    for (size_t i = 0; ok && i < n; ++i) {
+        cudaGraphNodeType ty;
+        ok = cudaGraphNodeGetType(chain[i], &ty) == cudaSuccess && ty == cudaGraphNodeTypeKernel;
+        g->node[i] = chain[i];
+    }
+    g->n_nodes = (int)n;
+    if (ok) {
+        cudaKernelNodeParams p;
+        ok = cudaGraphKernelNodeGetParams(g->node[0], &p) == cudaSuccess;
+        if (ok) std::memcpy(&g->her, p.kernelParams[0], sizeof(HerLaunch));
+        ok = ok && cudaGraphKernelNodeGetParams(g->node[1], &p) == cudaSuccess;
+        if (ok) {
+            std::memcpy(&g->vnet, p.kernelParams[0], sizeof(VnetLaunch));
+            // the tensor-core kernel takes the weight images as a second argument
+            if (vnet_tc_supported(g->vnet)) {
+                g->vnet_args.resize(sizeof(const uint8_t*));
+                std::memcpy(g->vnet_args.data(), p.kernelParams[1], sizeof(const uint8_t*));
+            }
+        }
+        ok = ok && cudaGraphKernelNodeGetParams(g->node[2], &p) == cudaSuccess;
+        if (ok) {
+            std::memcpy(&g->red, p.kernelParams[0], sizeof(ReduceLaunch));
+            std::memcpy(&g->red_adam, p.kernelParams[1], sizeof(AdamLaunch));
+            std::memcpy(&g->bar, p.kernelParams[2], sizeof(g->bar));
+            std::memcpy(&g->bar_target, p.kernelParams[3], sizeof(g->bar_target));
+        }
+        if (ok && n == 4) {
+            ok = cudaGraphKernelNodeGetParams(g->node[3], &p) == cudaSuccess;
+            if (ok) std::memcpy(&g->adam, p.kernelParams[0], sizeof(AdamLaunch));
+        }
+    }
+    ok = ok && cudaGraphInstantiate(&g->exec, graph, 0) == cudaSuccess;
+    cudaGetLastError();   // no error of these queries stays behind for the caller
+    if (!ok) {
+        if (g->exec) cudaGraphExecDestroy(g->exec);
+        cudaGraphDestroy(graph);
+        delete g;
+        return OFRL_EUNSUPPORTED;
+    }
+    *out = g;
+    return OFRL_OK;
+}
+
+namespace {
+
+cudaError_t set_args(ofrl_step_graph* g, int i, void** args) {
+    cudaKernelNodeParams p;
+    cudaError_t e = cudaGraphKernelNodeGetParams(g->node[i], &p);
+    if (e != cudaSuccess) return e;
+    p.kernelParams = args;
+    p.extra = nullptr;
+    return cudaGraphExecKernelNodeSetParams(g->exec, g->node[i], &p);
+}
+
+}  // namespace
+
+extern "C" ofrl_status ofrl_step_graph_launch(ofrl_step_graph* g, uint64_t step, const float* q,
+                                              const float* const* aux_src, void* stream) {
+    if (g == nullptr || step >= (1ull << 32)) return OFRL_EINVAL;
+    if (g->n_aux > 0 && aux_src != nullptr)
+        for (int i = 0; i < g->n_nets * g->n_aux; ++i)
+            if (aux_src[i] == nullptr) return OFRL_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // 1. relabel: the step index
+    g->her.step = step;
+    void* a0[] = {&g->her};
+    cudaError_t e = set_args(g, 0, a0);
+    // 2. V: the Q pointer
+    if (e == cudaSuccess && q != nullptr && q != g->vnet.q) {
+        g->vnet.q = q;
+        void* a1[] = {&g->vnet, g->vnet_args.empty() ? nullptr : g->vnet_args.data()};
+        e = set_args(g, 1, a1);
+    }
+    // 3. reduce (+ Adam): sources, bias corrections, barrier target
+    for (int k = 0; k < g->n_nets; ++k) {
+        const int32_t t = g->nets[k].t + 1;
+        float bc1, bc2;
+        bias_corrections(g->beta1, g->beta2, t, &bc1, &bc2);
+        g->red_adam.bc1[k] = g->adam.bc1[k] = bc1;
+        g->red_adam.bc2[k] = g->adam.bc2[k] = bc2;
+        if (aux_src != nullptr)
+            for (int j = 0; j < g->n_aux; ++j) {
+                const float* src = aux_src[k * g->n_aux + j];
+                g->red.src[k][j + 1] = g->red_adam.src[k][j + 1] = g->adam.src[k][j + 1] = src;
+            }
+    }
+    const unsigned long long base = g->ctx->barrier_arrivals;
+    if (g->barrier_arrivals > 0) g->bar_target = base + g->barrier_arrivals;
+    if (e == cudaSuccess) {
+        void* a2[] = {&g->red, &g->red_adam, &g->bar, &g->bar_target};
+        e = set_args(g, 2, a2);
+    }
+    if (e == cudaSuccess && g->n_nodes == 4) {
+        void* a3[] = {&g->adam};
+        e = set_args(g, 3, a3);
+    }
+    if (e == cudaSuccess) e = cudaGraphLaunch(g->exec, st);
+    if (e != cudaSuccess) return OFRL_ECUDA;
+    g->ctx->barrier_arrivals += g->barrier_arrivals;
+    for (int k = 0; k < g->n_nets; ++k) g->nets[k].t += 1;
+    return OFRL_OK;
+}
+
+extern "C" ofrl_status ofrl_step_graph_destroy(ofrl_step_graph* g) {
+    if (g == nullptr) return OFRL_OK;
+    if (g->exec) cudaGraphExecDestroy(g->exec);
+    if (g->graph) cudaGraphDestroy(g->graph);
+    delete g;
+    return OFRL_OK;
+}

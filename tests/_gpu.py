@@ -110,7 +110,7 @@ def argmax_ok(gpu_am, q, v_ref, beta, margin=1e-3):
 class GpuStep:
     """The fused train step of one workload on the GPU, through the C ABI."""
 
-    def __init__(self, w, weight_clamp_max_abs=0.0, sanitize_sources=False, polyak=None):
+    def __init__(self, w, weight_clamp_max_abs=0.0, sanitize_sources=False, polyak=None, graph=False):
         import offline_rl_step_gb300 as ofrl
         self.ofrl = ofrl
         self.w = w
@@ -133,13 +133,26 @@ class GpuStep:
         self.loss = torch.empty(n, device="cuda")
         self.norms = torch.empty(n, 5, device="cuda")
         self.grad = torch.empty(n, p, device="cuda")
+        self.use_graph = graph
+        self.sg = None
 
     def step(self, k, q, aux=None):
         aux_dev = None if aux is None else [[dev(a) for a in per] for per in aux]
-        self.ofrl.train_step(self.ctx, self.replay, self.her, k, self.batch, dev(q), self.nets, self.opt,
-                             aux=aux_dev, v_out=self.v, pi_out=self.pi, argmax_out=self.am,
-                             loss_out=self.loss, norms_out=self.norms, grad_out=self.grad)
-        torch.cuda.synchronize()
+        qd = dev(q)
+        if self.use_graph:
+            # the step as a replayed CUDA graph (captured at the first step)
+            if self.sg is None:
+                self.sg = self.ofrl.StepGraph(self.ctx, self.replay, self.her, self.batch, self.nets, self.opt, qd,
+                                              aux=aux_dev, v_out=self.v, pi_out=self.pi, argmax_out=self.am,
+                                              loss_out=self.loss, norms_out=self.norms, grad_out=self.grad)
+            self.sg.launch(k, qd, aux_dev)
+            torch.cuda.synchronize()
+            self.sg.sync_t()
+        else:
+            self.ofrl.train_step(self.ctx, self.replay, self.her, k, self.batch, qd, self.nets, self.opt,
+                                 aux=aux_dev, v_out=self.v, pi_out=self.pi, argmax_out=self.am,
+                                 loss_out=self.loss, norms_out=self.norms, grad_out=self.grad)
+            torch.cuda.synchronize()
         cpu = lambda t: t.cpu().numpy()
         return dict(batch={k2: cpu(getattr(self.batch, k2)) for k2 in
                            ("states", "next_states", "actions", "rewards", "dones", "src_idx", "donor_idx")},
@@ -152,6 +165,8 @@ class GpuStep:
         return self.ofrl.train_step_kernels(self.ctx, self.batch, self.w.batch, self.w.n_nets)
 
     def close(self):
+        if self.sg is not None:
+            self.sg.close()
         self.ctx.close()
 
 

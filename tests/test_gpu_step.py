@@ -131,9 +131,9 @@ def _check_step(w, k, got, ref, flagged, nets, p_before, gpu_before, q, strict=F
 
 
 @pytest.mark.parametrize("w", synth.ALL, ids=lambda w: w.name)
-def test_train_step_matches_oracle(w):
+def test_train_step_matches_oracle(w, graph=False):
     need_gpu()
-    g = GpuStep(w)
+    g = GpuStep(w, graph=graph)
     cfg = oracle_cfg(w)
     rep = replay_np(w)
     nets = oracle_nets(w)
@@ -240,3 +240,13 @@ def test_reduce_and_adam_launch_fusion_choice():
             assert g.kernels() == expect, w.name
         finally:
             g.close()
+
+
+@pytest.mark.parametrize("w", [dataclasses.replace(synth.PROD, steps=6),
+                               dataclasses.replace(synth.BUDGETED, batch=1000, capacity=1 << 14, steps=3),
+                               dataclasses.replace(synth.TWIN, steps=3)],
+                         ids=["prod_graph", "budgeted_graph", "twin_graph"])
+def test_step_graph_matches_oracle(w):
+    # the same steps replayed from one captured CUDA graph: the step index,
+    # Q and the auxiliary sources change per replay, t advances
+    test_train_step_matches_oracle(w, graph=True)
