@@ -294,10 +294,11 @@ def run_ours(args, w):
     dominant = max(phase_avg, key=phase_avg.get)
     dur_s = phase_avg[dominant] / 1e3
     sm_mhz = pk.get("sm_max_mhz", 2070.0)
-    if dominant == "vnet" and w.hidden == 128:
-        # tensor-core kernel: bf16 MMAs (three-term split, six products per
+    path = ctx.vnet_path(w.n_nets)
+    if dominant == "vnet" and path in ("tc_fused", "tc_layered"):
+        # tensor-core kernels: bf16 MMAs (three-term split, six products per
         # K-step, for fp32 workloads); algorithmic flops over the measured
-        # sustained bf16 peak (the kernel runs inside a long step)
+        # sustained bf16 peak (the kernels run inside a long step)
         peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
         ach = alg["vnet_flops"] / dur_s / 1e12
         # MMA work as executed: 128-row tiles, S padded to 64, five GEMMs,
@@ -305,9 +306,10 @@ def run_ours(args, w):
         prods = 1 if w.prec == "bf16" else 6
         tiles = -(-w.batch // 128)
         mma = w.n_nets * tiles * prods * 2 * 128 * (2 * w.hidden * 64 + 3 * w.hidden ** 2)
-        roof = {"kernel": "vnet_tc (tcgen05)", "bound": "tensor", "achieved": ach, "peak": peak,
+        kname = "vnet_tc (tcgen05)" if path == "tc_fused" else "vnet_wide fwd + wgrad (tcgen05, TMA)"
+        roof = {"kernel": kname, "bound": "tensor", "achieved": ach, "peak": peak,
                 "unit": "TFLOP/s", "frac": ach / peak,
-                "traffic": NCU_TRAFFIC.get(("vnet_tc (tcgen05)", w.name)),
+                "traffic": NCU_TRAFFIC.get((kname, w.name)),
                 "peak_source": f"bf16_tflops_sustained ({pk_kind})",
                 "mma_tflops_executed": mma / dur_s / 1e12, "mma_frac_executed": mma / dur_s / 1e12 / peak}
     elif dominant == "vnet":
@@ -338,6 +340,7 @@ def run_ours(args, w):
                        "num_actions": w.num_actions, "n_nets": w.n_nets, "her": f"{w.strategy} {w.her_ratio}",
                        "capacity": w.capacity, "parallelism": f"replicas{world}",
                        "launch": "direct kernel launches chained by programmatic dependent launch",
+                       "vnet_path": path,
                        "l2": f"inputs larger than L2: replay buffer {replay_bytes / 2**20:.0f} MiB read at "
                              f"random rows every step"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,

@@ -329,11 +329,35 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
 
 /* Kernel launches one ofrl_train_step on this context makes for `rows`
  * batch rows and n_nets networks writing into `batch` (no counterpart on the
- * pages: a planning aid for launch accounting and graph capture).  4
- * (relabel, V, reduce, Adam), or 3 when the reduce and Adam run as one
- * cooperative launch (its grid fits on the device at once).  Returns 0 for
- * invalid arguments.  Host only; launches nothing. */
+ * pages: a planning aid for launch accounting and graph capture): relabel,
+ * one V kernel (two on the layered tensor-core path), then reduce and Adam
+ * as one cooperative launch when its grid fits on the device at once, else
+ * two.  Returns 0 for invalid arguments.  Host only; launches nothing. */
 int32_t ofrl_train_step_kernels(const ofrl_ctx* ctx, const ofrl_batch* batch, int32_t rows, int32_t n_nets);
+
+/* ---- V forward/backward implementations --------------------------------
+ * The batch x hidden GEMMs of the value network ("GPU IQL + HER Porting
+ * Plan", "CUDA Kernel: iql_value_kernel.cu"; five GEMMs per network and
+ * step) run in one of three ways, all with the same results to fp32
+ * rounding (no counterpart on the pages, which use cuBLAS):
+ *   TC_FUSED   H = 128, S <= 64: one CTA per 128-row tile runs all five
+ *              GEMMs on the tensor cores (tcgen05, accumulators in TMEM);
+ *   TC_LAYERED H = 128 or 256, S < 64: per tile the forward and the
+ *              backward to dz1 on the tensor cores with operands streamed by
+ *              TMA, then the weight gradients split over K-ranges of the
+ *              batch (two kernels);
+ *   CUDA_CORES every H in {64, 128, 256}.
+ * AUTO (the default) takes TC_FUSED for H = 128, TC_LAYERED for H = 256 and
+ * CUDA_CORES otherwise, falling back to CUDA_CORES where a choice does not
+ * apply to a call (e.g. unaligned states in a standalone call).
+ * ofrl_select_vnet_path sets the context's choice: OFRL_EUNSUPPORTED when
+ * the shape (or the driver, for the layered path's tensor maps) does not
+ * allow it, OFRL_EINVAL for an unknown value.  ofrl_vnet_path returns the
+ * implementation a train step of n_nets networks takes (an OFRL_VNET_*
+ * value, never AUTO), or -1 for invalid arguments.  Host only. */
+enum { OFRL_VNET_AUTO = 0, OFRL_VNET_TC_FUSED = 1, OFRL_VNET_TC_LAYERED = 2, OFRL_VNET_CUDA_CORES = 3 };
+ofrl_status ofrl_select_vnet_path(ofrl_ctx* ctx, int32_t path);
+int32_t ofrl_vnet_path(const ofrl_ctx* ctx, int32_t n_nets);
 
 /* ---- the step as a CUDA graph ------------------------------------------
  * "Phase 2: Multi-Stream Graph Parallelism" runs the trainers' step as a

@@ -159,6 +159,10 @@ class Opt:
                         self.beta, b, a, self.weight_clamp_max_abs, 1 if self.sanitize_sources else 0)
 
 
+# V forward/backward implementations (OFRL_VNET_* in ofrl.h)
+VNET_PATHS = {"auto": 0, "tc_fused": 1, "tc_layered": 2, "cuda_cores": 3}
+
+
 class Context:
     """Device workspace for one V-network shape (ofrl_create); the only allocation."""
 
@@ -193,6 +197,18 @@ class Context:
 
     def workspace_bytes(self) -> int:
         return int(self._lib.ofrl_workspace_bytes(C.byref(self.shape), self.max_batch, self.max_nets))
+
+    def select_vnet_path(self, path: str):
+        """Which V forward/backward implementation later calls take: auto, tc_fused, tc_layered, cuda_cores."""
+        _abi.check("ofrl_select_vnet_path", self._lib.ofrl_select_vnet_path(self.handle, VNET_PATHS[path]))
+
+    def vnet_path(self, n_nets: int = 1) -> str:
+        """The implementation a train step of n_nets networks takes on this context."""
+        k = int(self._lib.ofrl_vnet_path(self.handle, n_nets))
+        names = {v: n for n, v in VNET_PATHS.items()}
+        if k not in names:
+            raise ValueError(f"ofrl_vnet_path: invalid arguments (n_nets={n_nets})")
+        return names[k]
 
 
 def her_relabel(ctx: Context, replay: Replay, her: HerConfig, step: int, out: Batch, stream=None):

@@ -70,6 +70,8 @@ SIGNATURES = {
                                     C.POINTER(VNet), C.c_int32, C.POINTER(Opt), C.POINTER(vp), C.c_int32,
                                     vp, vp, vp, vp, vp, vp, vp]),
     "ofrl_train_step_kernels": (C.c_int32, [vp, C.POINTER(Batch), C.c_int32, C.c_int32]),
+    "ofrl_select_vnet_path": (C.c_int32, [vp, C.c_int32]),
+    "ofrl_vnet_path": (C.c_int32, [vp, C.c_int32]),
     "ofrl_step_graph_create": (C.c_int32, [vp, C.POINTER(Replay), C.POINTER(HerCfg), C.POINTER(Batch), vp, vp,
                                            C.c_int32, C.POINTER(Opt), C.POINTER(vp), C.c_int32, vp, vp, vp, vp, vp,
                                            vp, C.POINTER(vp)]),

@@ -38,10 +38,18 @@ bool hidden_supported(int h) { return h == 64 || h == 128 || h == 256; }
 
 struct Layout {
     int64_t off_partials, off_tile_loss, off_g0, off_gram, off_scalars, off_counter, off_status, off_img, off_ximg,
-        off_barrier, total;
+        off_act[3], off_tvec, off_barrier, total;
     int32_t max_tiles;
+    int32_t tiles128;        // 128-row tiles of the tensor-core paths
+    bool layered;            // the layered tensor-core path has its buffers
     int64_t P;
 };
+
+// The tensor-core paths: weight and state-tile images for H = 128 and 256;
+// the layered path's activation images for H = 128 and 256 with S < 64.
+bool tc_images(const ofrl_vshape* s) { return s->hidden == 128 || s->hidden == 256; }
+bool layered_possible(const ofrl_vshape* s) { return tc_images(s) && s->state_dim < tc::KX; }
+int planes_of(const ofrl_vshape* s) { return s->prec == OFRL_PREC_BF16 ? 1 : 3; }
 
 Layout layout_of(const ofrl_vshape* s, int32_t max_batch, int32_t max_nets) {
     Layout L;
@@ -57,8 +65,14 @@ Layout layout_of(const ofrl_vshape* s, int32_t max_batch, int32_t max_nets) {
     L.off_scalars = take((int64_t)max_nets * kScalars * 4);
     L.off_counter = take((int64_t)max_nets * 4);
     L.off_status = take((int64_t)OFRL_STAT_WORDS * 4);
-    L.off_img = take(s->hidden == 128 ? (int64_t)max_nets * vnet_tc_image_bytes() : 0);
-    L.off_ximg = take(s->hidden == 128 ? (int64_t)L.max_tiles * tc::x_tile_bytes() : 0);
+    L.tiles128 = (int32_t)((max_batch + tc::TM - 1) / tc::TM);
+    L.layered = layered_possible(s);
+    L.off_img = take(tc_images(s) ? (int64_t)max_nets * tc::weight_image_bytes(s->hidden) : 0);
+    L.off_ximg = take(tc_images(s) ? (int64_t)L.tiles128 * tc::x_tile_bytes() : 0);
+    for (int k = 0; k < 3; ++k)
+        L.off_act[k] = take(L.layered ? (int64_t)max_nets * L.tiles128 * vnet_wide_act_bytes(s->hidden, planes_of(s))
+                                      : 0);
+    L.off_tvec = take(L.layered ? (int64_t)max_nets * L.tiles128 * vnet_wide_tvec_stride(s->hidden) * 4 : 0);
     L.off_barrier = take(8);
     L.total = o;
     return L;
@@ -163,26 +177,65 @@ void prof_release(ofrl_ctx* ctx) {
     ctx->prof_max = ctx->prof_count = 0;
 }
 
-// V forward/backward: the tensor-core kernel where it applies (hidden 128,
-// 16-byte rows), else the CUDA-core kernel; both write the same partials.
+// The V forward/backward implementation a launch takes: the one the context
+// asks for where it applies, else (PATH_AUTO) the fused tensor-core kernel
+// for hidden 128, the layered one for hidden 256, the CUDA-core kernel
+// otherwise.  Fills the layered path's fields of v.
+int32_t choose_path(const ofrl_ctx* ctx, VnetLaunch& v) {
+    if (ctx->maps != nullptr) {
+        for (int k = 0; k < 3; ++k) v.act[k] = ctx->ws.act[k];
+        v.tvec = ctx->ws.tvec;
+        v.tvec_stride = ctx->tvec_stride;
+        v.act_tiles = ctx->act_tiles;
+        v.maps = ctx->maps;
+        v.n_ranges = vnet_wide_ranges(v, ctx->num_sms);
+        if (v.n_ranges > ctx->max_tiles) v.n_ranges = ctx->max_tiles;
+    }
+    const bool fused = vnet_tc_supported(v), layered = vnet_wide_supported(v);
+    switch (ctx->vnet_path) {
+        case PATH_SIMT: return PATH_SIMT;
+        case PATH_FUSED: return fused ? PATH_FUSED : PATH_SIMT;
+        case PATH_LAYERED: return layered ? PATH_LAYERED : PATH_SIMT;
+        default: return fused ? PATH_FUSED : layered ? PATH_LAYERED : PATH_SIMT;
+    }
+}
+
+// Rows per tile (entries of tile_loss) of the chosen path.
+int path_tile_rows(const VnetLaunch& v) { return v.path == PATH_SIMT ? vnet_tile_rows(v.hidden) : tc::TM; }
+
+// V forward/backward by v.path; all write the same gradient partials.
 // `packed`: the weight images (and v.ximg, if set) were already written.
 cudaError_t launch_vnet(ofrl_ctx* ctx, const VnetLaunch& v, bool packed, cudaStream_t st) {
-    if (vnet_tc_supported(v)) {
+    if (v.path == PATH_FUSED) {
         if (!packed) {
             const cudaError_t e = launch_vnet_tc_pack(v, ctx->ws.img, st);
             if (e != cudaSuccess) return e;
         }
         return launch_vnet_tc(v, ctx->ws.img, st);
     }
+    if (v.path == PATH_LAYERED) {
+        VnetLaunch w = v;
+        if (!packed) {
+            const cudaError_t e = launch_vnet_wide_pack(v, ctx->ws.img, ctx->ws.ximg, st);
+            if (e != cudaSuccess) return e;
+            w.ximg = ctx->ws.ximg;
+        }
+        return launch_vnet_wide(w, ctx->ws.img, st);
+    }
     return launch_vnet_fwd_bwd(v, st);
 }
 
 // Gradient partials per network that launch_vnet leaves for n_tiles tiles:
 // one per tile from the CUDA-core kernel, one per cluster of tiles from the
-// tensor-core kernel.
+// fused tensor-core kernel, one per K-range from the layered one.
 int vnet_parts(const VnetLaunch& v, int n_tiles) {
-    return vnet_tc_supported(v) ? n_tiles / vnet_tc_cluster(n_tiles) : n_tiles;
+    if (v.path == PATH_FUSED) return n_tiles / vnet_tc_cluster(n_tiles);
+    if (v.path == PATH_LAYERED) return v.n_ranges;
+    return n_tiles;
 }
+
+// Kernels a V forward/backward launch takes.
+int vnet_kernels(const VnetLaunch& v) { return v.path == PATH_LAYERED ? 2 : 1; }
 
 }  // namespace
 
@@ -236,12 +289,29 @@ ofrl_status ofrl_create(const ofrl_vshape* shape, int32_t max_batch, int32_t max
     ctx->ws.status = reinterpret_cast<int32_t*>(b + L.off_status);
     ctx->ws.img = reinterpret_cast<uint8_t*>(b + L.off_img);
     ctx->ws.ximg = reinterpret_cast<uint8_t*>(b + L.off_ximg);
+    for (int k = 0; k < 3; ++k) ctx->ws.act[k] = L.layered ? reinterpret_cast<uint8_t*>(b + L.off_act[k]) : nullptr;
+    ctx->ws.tvec = L.layered ? reinterpret_cast<float*>(b + L.off_tvec) : nullptr;
     ctx->ws.barrier = reinterpret_cast<unsigned long long*>(b + L.off_barrier);
     ctx->barrier_arrivals = 0;
+    ctx->vnet_path = PATH_AUTO;
+    ctx->act_tiles = L.tiles128;
+    ctx->tvec_stride = L.layered ? vnet_wide_tvec_stride(shape->hidden) : 0;
+    ctx->maps = nullptr;
     if (cudaMemset(ctx->base, 0, (size_t)L.total) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
         cudaFree(ctx->base);
         delete ctx;
         return OFRL_ECUDA;
+    }
+    // tensor maps over the layered path's buffers; without them (no
+    // tensor-map support in the driver) that path is unavailable
+    if (L.layered) {
+        WideMaps* m = new (std::align_val_t(128), std::nothrow) WideMaps;
+        if (m != nullptr && vnet_wide_maps(m, shape->hidden, planes_of(shape), max_nets, L.tiles128, ctx->ws.act,
+                                           ctx->ws.ximg, L.tiles128, ctx->ws.img) == cudaSuccess)
+            ctx->maps = m;
+        else if (m != nullptr)
+            ::operator delete(m, std::align_val_t(128));
+        cudaGetLastError();
     }
     *out = ctx;
     return OFRL_OK;
@@ -252,6 +322,7 @@ ofrl_status ofrl_destroy(ofrl_ctx* ctx) {
     const cudaError_t e1 = cudaDeviceSynchronize();
     prof_release(ctx);
     const cudaError_t e2 = cudaFree(ctx->base);
+    if (ctx->maps != nullptr) ::operator delete(ctx->maps, std::align_val_t(128));
     delete ctx;
     return (e1 == cudaSuccess && e2 == cudaSuccess) ? OFRL_OK : OFRL_ECUDA;
 }
@@ -374,8 +445,6 @@ ofrl_status ofrl_iql_value_fwd_bwd(ofrl_ctx* ctx, const float* params, const flo
     if (batch < 1 || batch > ctx->max_batch || state_stride < sh.state_dim) return OFRL_EINVAL;
     if (!(tau >= 0.0f && tau <= 1.0f)) return OFRL_EINVAL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int tm = vnet_tile_rows(sh.hidden);
-    const int n_tiles = (batch + tm - 1) / tm;
 
     VnetLaunch v;
     std::memset(&v, 0, sizeof(v));
@@ -397,6 +466,9 @@ ofrl_status ofrl_iql_value_fwd_bwd(ofrl_ctx* ctx, const float* params, const flo
     v.net_partial_stride = (int64_t)ctx->max_tiles * v.part_stride;
     v.net_tile_stride = ctx->max_tiles;
     v.status = ctx->ws.status;
+    v.path = choose_path(ctx, v);
+    const int tm = path_tile_rows(v);
+    const int n_tiles = (batch + tm - 1) / tm;
     cudaError_t e = launch_vnet(ctx, v, false, st);
     if (e != cudaSuccess) return OFRL_ECUDA;
 
@@ -547,7 +619,8 @@ int32_t ofrl_train_step_kernels(const ofrl_ctx* ctx, const ofrl_batch* batch, in
     v.states = batch->states;
     v.stride = batch->stride;
     v.batch = rows;
-    const int tm = vnet_tile_rows(ctx->shape.hidden);
+    v.path = choose_path(ctx, v);
+    const int tm = path_tile_rows(v);
     ReduceLaunch r;
     std::memset(&r, 0, sizeof(r));
     r.n_nets = n_nets;
@@ -555,7 +628,40 @@ int32_t ofrl_train_step_kernels(const ofrl_ctx* ctx, const ofrl_batch* batch, in
     r.n_tiles = (rows + tm - 1) / tm;
     r.n_parts = vnet_parts(v, r.n_tiles);
     r.partials = ctx->ws.partials;
-    return reduce_adam_fusable(r) ? 3 : 4;
+    return 1 + vnet_kernels(v) + (reduce_adam_fusable(r) ? 1 : 2);
+}
+
+ofrl_status ofrl_select_vnet_path(ofrl_ctx* ctx, int32_t path) {
+    ofrl_status s = check_ctx(ctx);
+    if (s != OFRL_OK) return s;
+    const ofrl_vshape& sh = ctx->shape;
+    switch (path) {
+        case OFRL_VNET_AUTO:
+        case OFRL_VNET_CUDA_CORES: break;
+        case OFRL_VNET_TC_FUSED:
+            if (sh.hidden != 128 || sh.state_dim > tc::KX) return OFRL_EUNSUPPORTED;
+            break;
+        case OFRL_VNET_TC_LAYERED:
+            if (ctx->maps == nullptr) return OFRL_EUNSUPPORTED;
+            break;
+        default: return OFRL_EINVAL;
+    }
+    ctx->vnet_path = path;
+    return OFRL_OK;
+}
+
+int32_t ofrl_vnet_path(const ofrl_ctx* ctx, int32_t n_nets) {
+    if (ctx == nullptr || n_nets < 1 || n_nets > ctx->max_nets) return -1;
+    // a train step's batch: 16-byte aligned rows (what ofrl_train_step requires)
+    VnetLaunch v;
+    std::memset(&v, 0, sizeof(v));
+    v.n_nets = n_nets;
+    v.state_dim = ctx->shape.state_dim;
+    v.hidden = ctx->shape.hidden;
+    v.prec = ctx->shape.prec;
+    v.stride = (ctx->shape.state_dim + 3) & ~3;
+    v.batch = ctx->max_batch;
+    return choose_path(ctx, v);
 }
 
 ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl_her_cfg* her, uint64_t step,
@@ -616,7 +722,8 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
     v.net_partial_stride = (int64_t)ctx->max_tiles * v.part_stride;
     v.net_tile_stride = ctx->max_tiles;
     v.status = ctx->ws.status;
-    const bool tc_path = vnet_tc_supported(v);
+    v.path = choose_path(ctx, v);
+    const bool tc_path = v.path == PATH_FUSED || v.path == PATH_LAYERED;
 
     // 1. HER relabel (+ state-tile images and packed weights for the tensor-core kernel)
     prof_mark(ctx, 0, st);
@@ -626,6 +733,7 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
         ha.img_planes = sh.prec == OFRL_PREC_BF16 ? 1 : 3;
         ha.img_rows = (B + tc::TM - 1) / tc::TM * tc::TM;
         ha.wimg = ctx->ws.img;
+        ha.pack_hidden = sh.hidden;
         ha.pack_nets = n_nets;
         for (int k = 0; k < n_nets; ++k) ha.pack_params[k] = nets[k].params;
         v.ximg = ctx->ws.ximg;
@@ -640,7 +748,7 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
     prof_mark(ctx, 2, st);
 
     // 3. primary gradient, Gram matrix, budget coefficients, norms, loss
-    const int tm = vnet_tile_rows(sh.hidden);
+    const int tm = path_tile_rows(v);
     ReduceLaunch r;
     std::memset(&r, 0, sizeof(r));
     r.n_nets = n_nets;

@@ -1,6 +1,7 @@
 // Shared device helpers and the context layout of the ofrl library.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -37,9 +38,33 @@ struct Workspace {
     float* scalars;       // [max_nets][kScalars]
     unsigned int* counter;  // [max_nets] last-block tickets (reset by the last block)
     int32_t* status;      // [OFRL_STAT_WORDS]
-    uint8_t* img;         // [max_nets] packed bf16 weight images for the tensor-core kernel
-    uint8_t* ximg;        // [max_tiles] bf16 images of the relabelled state tiles
+    uint8_t* img;         // [max_nets] packed bf16 weight images for the tensor-core kernels
+    uint8_t* ximg;        // [128-row tiles] bf16 images of the relabelled state tiles
+    uint8_t* act[3];      // layered tensor-core path: h1, dz2, dz1 images [max_nets][128-row tiles]
+    float* tvec;          // layered path: per-tile dW3, db2 column sums and db3 [max_nets][tiles][tvec_stride]
     unsigned long long* barrier;  // grid-barrier arrival counter of the fused reduce + Adam (only grows)
+};
+
+}  // namespace ofrl
+
+namespace ofrl {
+
+// Which V forward/backward implementation a step uses.
+enum VnetPath : int32_t {
+    PATH_AUTO = 0,      // fused tensor-core kernel for H = 128, layered for H = 256, else CUDA cores
+    PATH_FUSED = 1,     // vnet_tc.cu: one CTA per tile does all five GEMMs (H = 128)
+    PATH_LAYERED = 2,   // vnet_wide.cu: per-tile forward/backward, then split-K weight gradients
+    PATH_SIMT = 3,      // vnet_simt.cu: CUDA cores
+};
+
+// Tensor maps of the layered path (5-D: core matrix, chunk, row group,
+// plane, tile or network), each with the box one of its loads uses.
+struct alignas(128) WideMaps {
+    CUtensorMap h1k, dz2k;      // activation K-chunks: all 128 rows x 16 columns
+    CUtensorMap dz2h, dz1h;     // activation MN-chunks: 16 rows x 128 columns (a half of H)
+    CUtensorMap h1n;            // activation MN-chunks: 16 rows x H columns
+    CUtensorMap xk;             // state-image MN-chunks: 16 rows x 64 columns
+    CUtensorMap w2k, w2n;       // W2 image: K-chunks (H rows x 16) and MN-chunks (16 rows x H)
 };
 
 }  // namespace ofrl
@@ -56,6 +81,10 @@ struct ofrl_ctx {
     void* base;           // the single cudaMalloc of the context
     int64_t bytes;
     ofrl::Workspace ws;
+    int32_t vnet_path;          // ofrl::VnetPath requested (PATH_AUTO unless selected)
+    int32_t act_tiles;          // 128-row tiles per network in ws.act / ws.tvec
+    int32_t tvec_stride;
+    ofrl::WideMaps* maps;       // tensor maps of the layered path (null: not available)
     uint64_t barrier_arrivals;  // arrivals the launched fused kernels add to ws.barrier
     // measurement hooks: events[step][OFRL_PHASES + 1] while profiling
     cudaEvent_t* prof_events;
@@ -88,6 +117,23 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+// Column sums over the 32 rows of a warp: v[j] (16 columns per lane) ->
+// lane l returns the sum of column (l >> 1) & 15 (lanes l and l ^ 1 agree).
+__device__ __forceinline__ float colsum16(float (&v)[16]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 16, n = 16; o >= 2; o >>= 1, n >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float keep = up ? v[i + n / 2] : v[i];
+            const float give = up ? v[i] : v[i + n / 2];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, give, o);
+        }
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
 __device__ __forceinline__ int warp_sum_int(int v) {
@@ -269,6 +315,7 @@ struct HerLaunch {
     int32_t pack_nets;
     const float* pack_params[kMaxNets];
     uint8_t* wimg;          // per network: W1 image then W2 image
+    int32_t pack_hidden;    // H of the packed images
     // optional: caller-given sources (e.g. PER-sampled) and importance
     // weights; HER rows get weight 1
     const int32_t* src_in;  // [batch] or null: sources drawn here
@@ -303,6 +350,14 @@ struct VnetLaunch {
     int32_t net_tile_stride;     // floats between networks in tile_loss
     int32_t* status;
     int32_t cluster;             // tensor-core kernel: tiles per partial (set by its launcher)
+    int32_t path;                // VnetPath chosen for this launch (never PATH_AUTO)
+    // layered tensor-core path
+    uint8_t* act[3];             // h1, dz2, dz1 images [n_nets][act_tiles][planes][128 x H]
+    float* tvec;                 // [n_nets][act_tiles][tvec_stride]: dW3 and db2 column sums, db3
+    int32_t tvec_stride;
+    int32_t act_tiles;
+    int32_t n_ranges;            // K-ranges of the weight-gradient kernel (its partials per network)
+    const WideMaps* maps;        // the context's tensor maps (host memory)
     // forward-only launches (launch_vnet_forward): the IQL target inputs
     const float* rewards;        // [B] or null
     const float* dones;          // [B] or null
@@ -319,6 +374,17 @@ int64_t vnet_tc_image_bytes();
 bool vnet_tc_supported(const VnetLaunch& a);
 cudaError_t launch_vnet_tc_pack(const VnetLaunch& a, uint8_t* img, cudaStream_t st);
 cudaError_t launch_vnet_tc(const VnetLaunch& a, const uint8_t* img, cudaStream_t st);
+// Layered tensor-core path (hidden 128 or 256, state_dim < 64): workspace
+// sizes, tensor maps over the context's buffers, weight and state-image
+// packing for standalone calls, and the two kernels.
+bool vnet_wide_supported(const VnetLaunch& a);
+int64_t vnet_wide_act_bytes(int hidden, int planes);     // one 128-row tile of one activation image
+int32_t vnet_wide_tvec_stride(int hidden);
+cudaError_t vnet_wide_maps(WideMaps* m, int hidden, int planes, int n_nets, int act_tiles, uint8_t* const act[3],
+                           uint8_t* ximg, int x_tiles, uint8_t* wimg);
+int vnet_wide_ranges(const VnetLaunch& a, int num_sms);  // partials per network the weight-gradient kernel writes
+cudaError_t launch_vnet_wide_pack(const VnetLaunch& a, uint8_t* wimg, uint8_t* ximg, cudaStream_t st);
+cudaError_t launch_vnet_wide(const VnetLaunch& a, const uint8_t* wimg, cudaStream_t st);
 // Tiles whose gradient partials the tensor-core kernel sums into one (a
 // thread-block cluster): the largest of 4, 2, 1 that divides n_tiles and
 // that the device can schedule.  Its partials count is n_tiles / that.

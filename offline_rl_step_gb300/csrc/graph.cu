@@ -9,9 +9,10 @@
 // instantiated graph's kernel nodes before each replay: the relabel's step
 // index, the V kernel's Q pointer, the auxiliary-source pointers, Adam's bias
 // corrections and the fused kernel's grid-barrier target.  Each node's first
-// arguments are the launch structs the kernels take (HerLaunch; VnetLaunch;
-// ReduceLaunch, AdamLaunch, barrier, target; AdamLaunch), so the fields are
-// patched in copies of the captured arguments.
+// arguments are the launch structs the kernels take (HerLaunch; VnetLaunch
+// (+ the weight images, + the tensor maps of the layered path, whose second
+// kernel reads no Q); ReduceLaunch, AdamLaunch, barrier, target; AdamLaunch),
+// so the fields are patched in copies of the captured arguments.
 
 #include <cmath>
 #include <cstring>
@@ -28,12 +29,14 @@ struct ofrl_step_graph {
     float beta1, beta2;
     cudaGraph_t graph;
     cudaGraphExec_t exec;
-    cudaGraphNode_t node[4];
-    int n_nodes;              // 3: relabel, V, reduce + Adam; 4: ..., reduce, Adam
+    cudaGraphNode_t node[5];
+    int n_nodes;              // relabel, V (1 or 2 kernels), reduce + Adam (1 or 2 kernels)
+    int red_node;             // index of the reduce node
     // the captured arguments of each node (copies patched before a replay)
     ofrl::HerLaunch her;
     ofrl::VnetLaunch vnet;
-    std::vector<uint8_t> vnet_args;   // the V kernel's second argument (tensor-core kernel), if any
+    const uint8_t* vnet_wimg;         // the tensor-core kernels' second argument
+    ofrl::WideMaps* vnet_maps;        // the layered path's third argument (128-byte aligned copy)
     ofrl::ReduceLaunch red;
     ofrl::AdamLaunch red_adam;
     unsigned long long* bar;
@@ -95,7 +98,7 @@ extern "C" ofrl_status ofrl_step_graph_create(ofrl_ctx* ctx, const ofrl_replay* 
     size_t n = 0;
     cudaGraphGetNodes(graph, nullptr, &n);
     std::vector<cudaGraphNode_t> nodes(n);
-    bool ok = n >= 3 && n <= 4 && cudaGraphGetNodes(graph, nodes.data(), &n) == cudaSuccess;
+    bool ok = n >= 3 && n <= 5 && cudaGraphGetNodes(graph, nodes.data(), &n) == cudaSuccess;
     // order by the chain: the node without dependencies first (the queries
     // take edge data: programmatic-launch edges carry it)
     std::vector<cudaGraphNode_t> chain;
@@ -131,21 +134,27 @@ extern "C" ofrl_status ofrl_step_graph_create(ofrl_ctx* ctx, const ofrl_replay* 
         ok = ok && cudaGraphKernelNodeGetParams(g->node[1], &p) == cudaSuccess;
         if (ok) {
             std::memcpy(&g->vnet, p.kernelParams[0], sizeof(VnetLaunch));
-            // the tensor-core kernel takes the weight images as a second argument
-            if (vnet_tc_supported(g->vnet)) {
-                g->vnet_args.resize(sizeof(const uint8_t*));
-                std::memcpy(g->vnet_args.data(), p.kernelParams[1], sizeof(const uint8_t*));
+            // the tensor-core kernels take the weight images as a second
+            // argument, the layered path's first kernel its tensor maps as a third
+            if (g->vnet.path == PATH_FUSED || g->vnet.path == PATH_LAYERED)
+                std::memcpy(&g->vnet_wimg, p.kernelParams[1], sizeof(const uint8_t*));
+            if (g->vnet.path == PATH_LAYERED) {
+                g->vnet_maps = new (std::align_val_t(128), std::nothrow) WideMaps;
+                if (g->vnet_maps == nullptr) ok = false;
+                else std::memcpy(g->vnet_maps, p.kernelParams[2], sizeof(WideMaps));
             }
         }
-        ok = ok && cudaGraphKernelNodeGetParams(g->node[2], &p) == cudaSuccess;
+        g->red_node = g->vnet.path == PATH_LAYERED ? 3 : 2;
+        ok = ok && (int)n >= g->red_node + 1 && (int)n <= g->red_node + 2;
+        ok = ok && cudaGraphKernelNodeGetParams(g->node[g->red_node], &p) == cudaSuccess;
         if (ok) {
             std::memcpy(&g->red, p.kernelParams[0], sizeof(ReduceLaunch));
             std::memcpy(&g->red_adam, p.kernelParams[1], sizeof(AdamLaunch));
             std::memcpy(&g->bar, p.kernelParams[2], sizeof(g->bar));
             std::memcpy(&g->bar_target, p.kernelParams[3], sizeof(g->bar_target));
         }
-        if (ok && n == 4) {
-            ok = cudaGraphKernelNodeGetParams(g->node[3], &p) == cudaSuccess;
+        if (ok && (int)n == g->red_node + 2) {
+            ok = cudaGraphKernelNodeGetParams(g->node[g->red_node + 1], &p) == cudaSuccess;
             if (ok) std::memcpy(&g->adam, p.kernelParams[0], sizeof(AdamLaunch));
         }
     }
@@ -154,6 +163,7 @@ extern "C" ofrl_status ofrl_step_graph_create(ofrl_ctx* ctx, const ofrl_replay* 
     if (!ok) {
         if (g->exec) cudaGraphExecDestroy(g->exec);
         cudaGraphDestroy(graph);
+        if (g->vnet_maps) ::operator delete(g->vnet_maps, std::align_val_t(128));
         delete g;
         return OFRL_EUNSUPPORTED;
     }
@@ -188,7 +198,7 @@ extern "C" ofrl_status ofrl_step_graph_launch(ofrl_step_graph* g, uint64_t step,
     // 2. V: the Q pointer
     if (e == cudaSuccess && q != nullptr && q != g->vnet.q) {
         g->vnet.q = q;
-        void* a1[] = {&g->vnet, g->vnet_args.empty() ? nullptr : g->vnet_args.data()};
+        void* a1[] = {&g->vnet, &g->vnet_wimg, g->vnet_maps};
         e = set_args(g, 1, a1);
     }
     // 3. reduce (+ Adam): sources, bias corrections, barrier target
@@ -208,11 +218,11 @@ extern "C" ofrl_status ofrl_step_graph_launch(ofrl_step_graph* g, uint64_t step,
     if (g->barrier_arrivals > 0) g->bar_target = base + g->barrier_arrivals;
     if (e == cudaSuccess) {
         void* a2[] = {&g->red, &g->red_adam, &g->bar, &g->bar_target};
-        e = set_args(g, 2, a2);
+        e = set_args(g, g->red_node, a2);
     }
-    if (e == cudaSuccess && g->n_nodes == 4) {
+    if (e == cudaSuccess && g->n_nodes == g->red_node + 2) {
         void* a3[] = {&g->adam};
-        e = set_args(g, 3, a3);
+        e = set_args(g, g->red_node + 1, a3);
     }
     if (e == cudaSuccess) e = cudaGraphLaunch(g->exec, st);
     if (e != cudaSuccess) return OFRL_ECUDA;
@@ -225,6 +235,7 @@ extern "C" ofrl_status ofrl_step_graph_destroy(ofrl_step_graph* g) {
     if (g == nullptr) return OFRL_OK;
     if (g->exec) cudaGraphExecDestroy(g->exec);
     if (g->graph) cudaGraphDestroy(g->graph);
+    if (g->vnet_maps) ::operator delete(g->vnet_maps, std::align_val_t(128));
     delete g;
     return OFRL_OK;
 }

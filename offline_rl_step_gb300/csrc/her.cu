@@ -54,10 +54,10 @@ __device__ __forceinline__ int episode_search(const int32_t* __restrict__ ends, 
     return f < len ? lo + f : lo + len;
 }
 
-// Extra blocks of the relabel grid: W1 [H][S] -> [128 x 64] image and
-// W2 [H][H] -> [128 x 128] image of every network, img_planes planes.
+// Extra blocks of the relabel grid: W1 [H][S] -> [H x 64] image and
+// W2 [H][H] -> [H x H] image of every network, img_planes planes.
 __device__ void pack_weights(const HerLaunch& a) {
-    const int S = a.state_dim, H = tc::HH, np = a.img_planes;
+    const int S = a.state_dim, H = a.pack_hidden, np = a.img_planes;
     const Offsets off = offsets_of(S, H);
     const int n1 = H * (tc::KX / 4), n2 = H * (H / 4);      // groups of 4 columns
     const int total = a.pack_nets * (n1 + n2);
@@ -65,19 +65,20 @@ __device__ void pack_weights(const HerLaunch& a) {
          e += a.pack_blocks * blockDim.x) {
         const int net = e / (n1 + n2), f = e % (n1 + n2);
         const float* prm = a.pack_params[net];
-        uint8_t* w1i = a.wimg + (int64_t)net * tc::weight_image_bytes();
-        uint8_t* w2i = w1i + 3 * tc::kPlaneX;
+        uint8_t* w1i = a.wimg + (int64_t)net * tc::weight_image_bytes(H);
+        uint8_t* w2i = w1i + tc::w2_image_offset(H);
+        const uint32_t plane1 = (uint32_t)(H * tc::KX * 2), plane2 = (uint32_t)(H * H * 2);
         float x[4];
         if (f < n1) {
             const int r = f / (tc::KX / 4), c = 4 * (f % (tc::KX / 4));
 #pragma unroll
             for (int j = 0; j < 4; ++j) x[j] = c + j < S ? __ldg(prm + off.w1 + (int64_t)r * S + c + j) : 0.0f;
-            tc::put4(w1i, tc::kPlaneX, np, tc::KX, r, c, x);
+            tc::put4(w1i, plane1, np, tc::KX, r, c, x);
         } else {
             const int g = f - n1, r = g / (H / 4), c = 4 * (g % (H / 4));
 #pragma unroll
             for (int j = 0; j < 4; ++j) x[j] = __ldg(prm + off.w2 + (int64_t)r * H + c + j);
-            tc::put4(w2i, tc::kPlaneH, np, H, r, c, x);
+            tc::put4(w2i, plane2, np, H, r, c, x);
         }
     }
 }
@@ -283,7 +284,8 @@ cudaError_t launch_her_relabel(const HerLaunch& a_in, cudaStream_t st) {
     HerLaunch a = a_in;
     const int rows = a.ximg != nullptr ? a.img_rows : a.batch;
     a.relabel_blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
-    a.pack_blocks = a.wimg != nullptr ? 48 : 0;
+    // the weight images grow with H^2: 48 blocks at H = 128
+    a.pack_blocks = a.wimg != nullptr ? (a.pack_hidden > 128 ? 160 : 48) : 0;
     static bool configured = false;
     if (!configured) {
         const cudaError_t e = set_max_shared_carveout(her_relabel_kernel);

@@ -32,8 +32,11 @@ __host__ __device__ __forceinline__ uint32_t img_off(int r, int c, int C) {
     return (uint32_t)((r >> 3) * (C >> 3) * 128 + (c >> 3) * 128 + (r & 7) * 16 + (c & 7) * 2);
 }
 
-// Bytes of one network's packed weights: W1 image then W2 image, 3 planes.
-__host__ __device__ constexpr int64_t weight_image_bytes() { return 3 * (int64_t)(kPlaneX + kPlaneH); }
+// Bytes of one network's packed weights for hidden width H: the W1 image
+// ([H x 64]) then the W2 image ([H x H]), room for 3 planes each.
+__host__ __device__ constexpr int64_t weight_image_bytes(int H = HH) { return 3 * 2 * (int64_t)H * (KX + H); }
+// Offset of the W2 image inside them.
+__host__ __device__ constexpr int64_t w2_image_offset(int H = HH) { return 3 * 2 * (int64_t)H * KX; }
 // Bytes of one state-tile image (3 planes).
 __host__ __device__ constexpr int64_t x_tile_bytes() { return 3 * (int64_t)kPlaneX; }
 

@@ -151,6 +151,24 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
         : "memory");
 }
 
+// Tiled tensor copy global -> shared of one box of a 5-D tensor map (TMA):
+// `tmap` is the address of a CUtensorMap kernel parameter (__grid_constant__),
+// c0..c4 the box's first coordinates (innermost first; the box shape is part
+// of the map); the box lands densely in shared memory, innermost dimension
+// first, and its bytes are counted on the mbarrier.
+__device__ __forceinline__ void tma_load5(void* dst_smem, const void* tmap, int c0, int c1, int c2, int c3, int c4,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5, %6}], [%7];" ::"r"(smem_u32(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Make this thread's generic-proxy global-memory writes visible to later
+// async-proxy reads (tensor copies) of the same addresses.
+__device__ __forceinline__ void fence_global_to_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
 // Bulk asynchronous copy shared -> global (16-byte aligned, size a multiple
 // of 16), tracked by the issuing thread's bulk group.
 __device__ __forceinline__ void bulk_s2g(void* dst_gmem, const void* src_smem, uint32_t bytes) {

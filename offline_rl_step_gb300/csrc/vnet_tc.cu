@@ -124,23 +124,6 @@ __device__ __forceinline__ void build_x(uint8_t* img, int np, const float* __res
     }
 }
 
-// Column sums over the 32 rows of a warp: v[j] (16 columns per lane) ->
-// lane l returns the sum of column (l >> 1) & 15 (lanes l and l ^ 1 agree).
-__device__ __forceinline__ float colsum16(float (&v)[16]) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int o = 16, n = 16; o >= 2; o >>= 1, n >>= 1) {
-        const bool up = (lane & o) != 0;
-#pragma unroll
-        for (int i = 0; i < n / 2; ++i) {
-            const float keep = up ? v[i + n / 2] : v[i];
-            const float give = up ? v[i] : v[i + n / 2];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, give, o);
-        }
-    }
-    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
-}
-
 // Sum, in rank order, of the value at shared address p in CTAs 0..cn-1 of
 // the cluster (cn <= 8); the loads are all issued before the adds.
 __device__ __forceinline__ float cluster_sum1(const float* p, int cn) {
@@ -189,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     const float* __restrict__ prm = a.params[net];
     const float tau = a.tau[net];
     const uint8_t* w1i = wimg + (int64_t)net * tc::weight_image_bytes();
-    const uint8_t* w2i = w1i + 3 * kPlaneX;
+    const uint8_t* w2i = w1i + tc::w2_image_offset();
     const uint8_t* xi = a.ximg != nullptr ? a.ximg + (int64_t)tile * NP * kPlaneX : nullptr;
     constexpr uint32_t kXBytes = (uint32_t)NP * kPlaneX, kW2Bytes = (uint32_t)NP * kPlaneH;
 
@@ -616,7 +599,7 @@ __global__ void pack_weights_kernel(const VnetLaunch a, uint8_t* __restrict__ im
     const Offsets off = offsets_of(S, HH);
     const float* __restrict__ prm = a.params[net];
     uint8_t* w1i = img + (int64_t)net * tc::weight_image_bytes();
-    uint8_t* w2i = w1i + 3 * kPlaneX;
+    uint8_t* w2i = w1i + tc::w2_image_offset();
     const int n1 = HH * (KX / 4), n2 = HH * (HH / 4);
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n1 + n2; e += gridDim.x * blockDim.x) {
         float x[4];

@@ -110,7 +110,7 @@ def argmax_ok(gpu_am, q, v_ref, beta, margin=1e-3):
 class GpuStep:
     """The fused train step of one workload on the GPU, through the C ABI."""
 
-    def __init__(self, w, weight_clamp_max_abs=0.0, sanitize_sources=False, polyak=None, graph=False):
+    def __init__(self, w, weight_clamp_max_abs=0.0, sanitize_sources=False, polyak=None, graph=False, path=None):
         import offline_rl_step_gb300 as ofrl
         self.ofrl = ofrl
         self.w = w
@@ -119,6 +119,9 @@ class GpuStep:
         self.her = ofrl.HerConfig(w.batch, w.her_count, w.strategy, w.goal_threshold, w.seed)
         self.ctx = ofrl.Context(w.state_dim, w.hidden, w.num_actions, w.prec, max_batch=w.batch,
                                 max_nets=w.n_nets)
+        if path is not None:
+            self.ctx.select_vnet_path(path)
+            assert self.ctx.vnet_path(w.n_nets) == path
         self.params0 = [synth.make_params(w, k) for k in range(w.n_nets)]
         self.nets = [ofrl.VNet.from_params(torch.from_numpy(p), w.taus[k], polyak=polyak)
                      for k, p in enumerate(self.params0)]

@@ -13,7 +13,7 @@ from oracle import iql
 pytestmark = pytest.mark.gpu
 
 
-def _fwd_bwd(s, h, b, tau, prec="fp32", seed=0, stride=None):
+def _fwd_bwd(s, h, b, tau, prec="fp32", seed=0, stride=None, path=None):
     import offline_rl_step_gb300 as ofrl
     need_gpu()
     w = dataclasses.replace(synth.PROD, state_dim=s, hidden=h, net_seeds=(seed + 7,))
@@ -24,6 +24,8 @@ def _fwd_bwd(s, h, b, tau, prec="fp32", seed=0, stride=None):
     x[:, :s] = rng.standard_normal((b, s))
     qt = (rng.standard_normal(b) * 2).astype(np.float32)
     ctx = ofrl.Context(s, h, 5, prec, max_batch=b)
+    if path is not None:
+        ctx.select_vnet_path(path)
     v = torch.empty(b, device="cuda")
     loss = torch.empty(1, device="cuda")
     grad = torch.empty(w.n_params, device="cuda")
@@ -39,6 +41,17 @@ def _fwd_bwd(s, h, b, tau, prec="fp32", seed=0, stride=None):
                                    (50, 256, 16384), (7, 64, 1), (64, 128, 129), (63, 128, 1000)])
 def test_value_fwd_bwd_fp32(s, h, b):
     (v, loss, g), (rv, rl, rg, vu, gu) = _fwd_bwd(s, h, b, 0.7, seed=s + h + b)
+    assert within(v, rv, vu, RTOL, ATOL).all(), "V outside tolerance and fp32 bound"
+    assert_close(loss, rl, what="loss")
+    ok, n_bound, rel = grad_ok(g, rg, gu)
+    assert ok, f"gradient outside tolerance and fp32 bound (norm rel {rel:.3g}, {n_bound} by bound)"
+
+
+@pytest.mark.parametrize("s,h,b,path", [(50, 128, 1000, "tc_layered"), (63, 128, 300, "tc_layered"),
+                                        (1, 256, 129, "tc_layered"), (50, 256, 1000, "cuda_cores")])
+def test_value_fwd_bwd_each_path(s, h, b, path):
+    # the implementations the default choice does not take for these shapes
+    (v, loss, g), (rv, rl, rg, vu, gu) = _fwd_bwd(s, h, b, 0.7, seed=s + h + b, path=path)
     assert within(v, rv, vu, RTOL, ATOL).all(), "V outside tolerance and fp32 bound"
     assert_close(loss, rl, what="loss")
     ok, n_bound, rel = grad_ok(g, rg, gu)

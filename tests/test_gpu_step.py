@@ -131,9 +131,9 @@ def _check_step(w, k, got, ref, flagged, nets, p_before, gpu_before, q, strict=F
 
 
 @pytest.mark.parametrize("w", synth.ALL, ids=lambda w: w.name)
-def test_train_step_matches_oracle(w, graph=False):
+def test_train_step_matches_oracle(w, graph=False, path=None):
     need_gpu()
-    g = GpuStep(w, graph=graph)
+    g = GpuStep(w, graph=graph, path=path)
     cfg = oracle_cfg(w)
     rep = replay_np(w)
     nets = oracle_nets(w)
@@ -169,10 +169,54 @@ def test_train_step_matches_oracle(w, graph=False):
 
 
 def test_ragged_batch_step():
-    # a batch that is not a multiple of the tile rows, H = 256 (64-row tiles)
+    # a batch that is not a multiple of the tile rows, H = 256 (layered
+    # tensor-core path: 8 tiles, the last one ragged)
     need_gpu()
     w = dataclasses.replace(synth.BUDGETED, batch=1000, capacity=1 << 14, steps=2)
     test_train_step_matches_oracle(w)
+
+
+def test_vnet_path_choice():
+    # the default implementation per hidden width, and which choices a shape allows
+    need_gpu()
+    import offline_rl_step_gb300 as ofrl
+    from offline_rl_step_gb300 import _abi
+    want = {64: "cuda_cores", 128: "tc_fused", 256: "tc_layered"}
+    for h, path in want.items():
+        for nets in (1, 2):
+            ctx = ofrl.Context(50, h, 5, "fp32", max_batch=4096, max_nets=nets)
+            try:
+                assert ctx.vnet_path(nets) == path, (h, nets)
+                ctx.select_vnet_path("cuda_cores")
+                assert ctx.vnet_path(nets) == "cuda_cores"
+                for other in ("tc_fused", "tc_layered"):
+                    ok = (other == "tc_fused" and h == 128) or (other == "tc_layered" and h in (128, 256))
+                    if ok:
+                        ctx.select_vnet_path(other)
+                        assert ctx.vnet_path(nets) == other
+                    else:
+                        with pytest.raises(_abi.OfrlError):
+                            ctx.select_vnet_path(other)
+            finally:
+                ctx.close()
+    # a 64-column state leaves no ones column: no layered path
+    ctx = ofrl.Context(64, 256, 5, "fp32", max_batch=1024)
+    try:
+        assert ctx.vnet_path(1) == "cuda_cores"
+    finally:
+        ctx.close()
+
+
+@pytest.mark.parametrize("w, path", [
+    (dataclasses.replace(synth.PROD, batch=2000, capacity=1 << 16, steps=3), "tc_layered"),
+    (dataclasses.replace(synth.TWIN, batch=1000, capacity=1 << 14, steps=3), "tc_layered"),
+    (dataclasses.replace(synth.PROD, batch=1000, capacity=1 << 14, steps=2), "cuda_cores"),
+    (dataclasses.replace(synth.BUDGETED, batch=1000, capacity=1 << 14, steps=2), "cuda_cores"),
+    (dataclasses.replace(synth.BUDGETED, batch=128, capacity=1 << 14, steps=2), "tc_layered"),
+], ids=["prod_layered", "twin_bf16_layered", "prod_cuda_cores", "budgeted_cuda_cores", "budgeted_one_tile"])
+def test_step_on_each_vnet_path(w, path):
+    # every implementation against the oracle (the default ones run in the tests above)
+    test_train_step_matches_oracle(w, path=path)
 
 
 def test_single_row_batch_step():
@@ -231,10 +275,10 @@ def test_step_with_source_guard_weight_bound_and_target():
 def test_reduce_and_adam_launch_fusion_choice():
     # the production batch (128 tiles, 32 cluster partials, 182 reduce
     # blocks) takes the single cooperative reduce + Adam launch; the
-    # H = 256 workload (256 tiles of 64 rows) needs more reduce blocks than
-    # fit at once and keeps two launches
+    # H = 256 workload (two V kernels, more than 64 K-range partials of 79k
+    # parameters) needs more reduce blocks than fit at once and keeps two
     need_gpu()
-    for w, expect in ((synth.PROD, 3), (dataclasses.replace(synth.BUDGETED, capacity=1 << 16), 4)):
+    for w, expect in ((synth.PROD, 3), (dataclasses.replace(synth.BUDGETED, capacity=1 << 16), 5)):
         g = GpuStep(w)
         try:
             assert g.kernels() == expect, w.name
