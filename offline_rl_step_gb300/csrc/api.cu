@@ -61,7 +61,7 @@ Layout layout_of(const ofrl_vshape* s, int32_t max_batch, int32_t max_nets) {
     L.off_partials = take((int64_t)max_nets * L.max_tiles * part_stride_of(L.P) * 4);
     L.off_tile_loss = take((int64_t)max_nets * L.max_tiles * 4);
     L.off_g0 = take((int64_t)max_nets * L.P * 4);
-    L.off_gram = take((int64_t)max_nets * kMaxGramBlocksWs * kGramPairs * 4);
+    L.off_gram = take((int64_t)max_nets * kMaxGramBlocksWs * kGramStride * 4);
     L.off_scalars = take((int64_t)max_nets * kScalars * 4);
     L.off_counter = take((int64_t)max_nets * 4);
     L.off_status = take((int64_t)OFRL_STAT_WORDS * 4);

@@ -13,6 +13,7 @@ namespace ofrl {
 constexpr int kMaxNets = 2;
 constexpr int kMaxSrc = 4;        // primary + up to three auxiliary sources
 constexpr int kGramPairs = 10;    // upper triangle of a 4x4 Gram matrix
+constexpr int kGramStride = 16;   // floats per block's Gram partial (padded: four 16-byte loads)
 constexpr int kScalars = 32;      // per-network scalar slots (see Scalar)
 constexpr int kMaxActions = 16;
 constexpr int kMaxStateDim = 64;
@@ -34,7 +35,7 @@ struct Workspace {
     float* partials;      // [max_nets][max_tiles][P] per-tile gradient partials
     float* tile_loss;     // [max_nets][max_tiles] per-tile sum of w d^2
     float* g0;            // [max_nets][P] primary gradient when the caller gives no buffer
-    float* gram_part;     // [max_nets][max_gram_blocks][kGramPairs]
+    float* gram_part;     // [max_nets][max_gram_blocks][kGramStride]
     float* scalars;       // [max_nets][kScalars]
     unsigned int* counter;  // [max_nets] last-block tickets (reset by the last block)
     int32_t* status;      // [OFRL_STAT_WORDS]
@@ -407,7 +408,7 @@ struct ReduceLaunch {
     float budget[kMaxSrc];
     float alpha[kMaxSrc];
     float max_grad_norm;
-    float* gram_part;            // [n_nets][grid][kGramPairs]
+    float* gram_part;            // [n_nets][grid][kGramStride]
     float* scalars;              // [n_nets][kScalars]
     unsigned int* counter;       // [n_nets]
     float* norms_out;            // [n_nets][5] or null: n_0..n_3, combined

@@ -42,7 +42,7 @@ ScratchLayout scratch_layout(int64_t part_stride, int n_tiles) {
     size_t o = 0;
     L.partials = o; o = up256(o + (size_t)n_tiles * part_stride * sizeof(float));
     L.tile_loss = o; o = up256(o + (size_t)n_tiles * sizeof(float));
-    L.gram = o; o = up256(o + (size_t)kGramBlocks * ofrl::kGramPairs * sizeof(float));
+    L.gram = o; o = up256(o + (size_t)kGramBlocks * ofrl::kGramStride * sizeof(float));
     L.scalars = o; o = up256(o + (size_t)ofrl::kScalars * sizeof(float));
     L.counter = o; o = up256(o + sizeof(unsigned int));
     L.status = o; o = up256(o + OFRL_STAT_WORDS * sizeof(int32_t));

@@ -27,29 +27,33 @@ namespace ofrl {
 namespace {
 
 // A reduce block is EL element lanes (a float4 each) x 256 / EL partial
-// lanes: EL = 8 for many partials (32 partial lanes), EL = 32 for few.
+// lanes: EL = 32 for few partials (8 partial lanes); for many, EL = 64 (4
+// partial lanes, eight loads in flight each) when that grid covers P in one
+// resident pass, else EL = 8 (32 partial lanes).
 constexpr int kRedThreads = 256;
-constexpr int kManyParts = 64;     // more partials than this: EL = 8
+constexpr int kManyParts = 64;     // more partials than this: EL = 64 or 8
 constexpr int kMaxGramBlocks = 2048;
 
+__device__ __forceinline__ void add4(float4& s, const float4& v) {
+    s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+}
+
 // Sum of the partials of element group i4..i4+3 over partials ty, ty + TL,
-// ... (fixed order; independent 16-byte loads in flight).
-template <int TL>
+// ... in that order, U independent 16-byte loads in flight at a time.
+template <int TL, int U>
 __device__ __forceinline__ float4 sum_tiles(const float* __restrict__ pp, int64_t stride, int n_parts, int ty,
                                             int64_t i4) {
-    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
-    int t = ty;
-    for (; t + TL < n_parts; t += 2 * TL) {
-        const float4 a = __ldcg(reinterpret_cast<const float4*>(pp + (int64_t)t * stride + i4));
-        const float4 b = __ldcg(reinterpret_cast<const float4*>(pp + (int64_t)(t + TL) * stride + i4));
-        s0.x += a.x; s0.y += a.y; s0.z += a.z; s0.w += a.w;
-        s1.x += b.x; s1.y += b.y; s1.z += b.z; s1.w += b.w;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int t = ty; t < n_parts; t += U * TL) {
+        float4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            v[u] = t + u * TL < n_parts ? __ldcg(reinterpret_cast<const float4*>(pp + (int64_t)(t + u * TL) * stride + i4))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < U; ++u) add4(acc, v[u]);
     }
-    if (t < n_parts) {
-        const float4 a = __ldcg(reinterpret_cast<const float4*>(pp + (int64_t)t * stride + i4));
-        s0.x += a.x; s0.y += a.y; s0.z += a.z; s0.w += a.w;
-    }
-    return make_float4(s0.x + s1.x, s0.y + s1.y, s0.z + s1.z, s0.w + s1.w);
+    return acc;
 }
 
 // (j, k) of Gram entry p (gram_index order)
@@ -62,7 +66,7 @@ __device__ __forceinline__ int pair_k(int p) {
 template <int EL>
 __device__ __forceinline__ void fused_norms_adam(const ReduceLaunch& a, const AdamLaunch& d, unsigned long long* bar,
                                                  unsigned long long bar_target, const float (&gacc)[kGramPairs],
-                                                 const float (&x)[kMaxSrc][4]) {
+                                                 const float (&x)[kMaxSrc][4], float4* scratch) {
     constexpr int kRedElems = 4 * EL;
     const int tid = threadIdx.x, tx = tid % EL, ty = tid / EL, lane = tid & 31, wid = tid >> 5;
     const int net = blockIdx.y, G = gridDim.x, nsrc = a.n_src;
@@ -80,42 +84,109 @@ __device__ __forceinline__ void fused_norms_adam(const ReduceLaunch& a, const Ad
                 vv[e] = d.v[net][i4 + e];
             }
     }
-    float* gp = a.gram_part + ((int64_t)net * G + blockIdx.x) * kGramPairs;
-    if (wid == 0) {
+    float* gp = a.gram_part + ((int64_t)net * G + blockIdx.x) * kGramStride;
+    if constexpr (EL <= 32) {
+        // the element lanes are lanes 0..EL-1 of warp 0
+        if (wid == 0) {
 #pragma unroll
-        for (int p = 0; p < kGramPairs; ++p) {
-            if (pair_j(p) >= nsrc || pair_k(p) >= nsrc) continue;
-            const float s = warp_sum(gacc[p]);
-            if (lane == 0) gp[p] = s;
+            for (int p = 0; p < kGramPairs; ++p) {
+                if (pair_j(p) >= nsrc || pair_k(p) >= nsrc) continue;
+                const float s = warp_sum(gacc[p]);
+                if (lane == 0) gp[p] = s;
+            }
+        }
+    } else {
+        // the element lanes fill warps 0..EL/32-1: per-warp sums, then in warp order
+        __shared__ float gw[EL / 32][kGramPairs];
+        if (wid < EL / 32) {
+#pragma unroll
+            for (int p = 0; p < kGramPairs; ++p) {
+                const float s = warp_sum(gacc[p]);
+                if (lane == 0) gw[wid][p] = s;
+            }
+        }
+        __syncthreads();
+        if (tid < kGramPairs && pair_j(tid) < nsrc && pair_k(tid) < nsrc) {
+            float s = gw[0][tid];
+#pragma unroll
+            for (int w = 1; w < EL / 32; ++w) s += gw[w][tid];
+            gp[tid] = s;
         }
     }
     const bool ok = grid_barrier(bar, bar_target, 1000000000ull);
 
-    // totals of the Gram entries present and of the loss, the same fixed
-    // order in every block: lanes stride the blocks, then one butterfly
+    // totals of the Gram entries present and of the loss, in the same fixed
+    // order in every block.  Every block reads all G Gram partials.  With one
+    // source: a warp per entry, lanes stride the blocks.  With several, the
+    // entries are read with contiguous 16-byte loads instead (thread t takes
+    // quad t % 4 of partials t / 4, t / 4 + 64, ...; strided 4-byte loads of
+    // the same few lines by every block queue at their L2 slices), lanes of
+    // equal quad combined by shuffles, the warps in order through `scratch`
+    // (the reduce's staging, free by now; no shared memory is added, so a
+    // block still fits beside a tensor-core V CTA).
     __shared__ float totals[kGramPairs + 1];
-    const float* gall = a.gram_part + (int64_t)net * G * kGramPairs;
-    for (int item = wid; item <= kGramPairs; item += kRedThreads / 32) {
-        const bool need = item == kGramPairs ? a.tile_loss != nullptr
-                                             : pair_j(item) < nsrc && pair_k(item) < nsrc;
-        float v = 0.0f;
-        if (need) {
-            const int n = item == kGramPairs ? a.n_tiles : G;
-            for (int b0 = lane; b0 < n; b0 += 8 * 32) {
-                float u[8];
+    if (nsrc <= 1) {
+        const float* gall = a.gram_part + (int64_t)net * G * kGramStride;
+        for (int item = wid; item <= kGramPairs; item += kRedThreads / 32) {
+            const bool need = item == kGramPairs ? a.tile_loss != nullptr
+                                                 : pair_j(item) < nsrc && pair_k(item) < nsrc;
+            float v = 0.0f;
+            if (need) {
+                const int n = item == kGramPairs ? a.n_tiles : G;
+                for (int b0 = lane; b0 < n; b0 += 8 * 32) {
+                    float u[8];
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int b = b0 + 32 * r;
-                    u[r] = b >= n ? 0.0f
-                                  : item == kGramPairs ? __ldcg(a.tile_loss + (int64_t)net * a.net_tile_stride + b)
-                                                       : __ldcg(gall + (int64_t)b * kGramPairs + item);
+                    for (int r = 0; r < 8; ++r) {
+                        const int b = b0 + 32 * r;
+                        u[r] = b >= n ? 0.0f
+                                      : item == kGramPairs ? __ldcg(a.tile_loss + (int64_t)net * a.net_tile_stride + b)
+                                                           : __ldcg(gall + (int64_t)b * kGramStride + item);
+                    }
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) v += u[r];
                 }
-#pragma unroll
-                for (int r = 0; r < 8; ++r) v += u[r];
+                v = warp_sum(v);
             }
-            v = warp_sum(v);
+            if (lane == 0) totals[item] = v;
         }
-        if (lane == 0) totals[item] = v;
+    } else {
+        float4* wq = scratch;                                           // [warps][4]
+        float* wl = reinterpret_cast<float*>(scratch + 4 * (kRedThreads / 32));   // [warps]
+        const float4* g4 = reinterpret_cast<const float4*>(a.gram_part + (int64_t)net * G * kGramStride);
+        const int quad = tid & 3;
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (quad < (kGramPairs + 3) / 4) {
+#pragma unroll 4
+            for (int b = tid >> 2; b < G; b += kRedThreads / 4)
+                add4(s, __ldcg(g4 + (int64_t)b * (kGramStride / 4) + quad));
+        }
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            s.x += __shfl_xor_sync(0xffffffffu, s.x, o);
+            s.y += __shfl_xor_sync(0xffffffffu, s.y, o);
+            s.z += __shfl_xor_sync(0xffffffffu, s.z, o);
+            s.w += __shfl_xor_sync(0xffffffffu, s.w, o);
+        }
+        if (lane < 4) wq[wid * 4 + lane] = s;
+        float l = 0.0f;
+        if (a.tile_loss != nullptr)
+            for (int t = tid; t < a.n_tiles; t += kRedThreads) l += __ldcg(a.tile_loss + (int64_t)net * a.net_tile_stride + t);
+        l = warp_sum(l);
+        if (lane == 0) wl[wid] = l;
+        __syncthreads();
+        if (tid <= kGramPairs) {
+            float v = 0.0f;
+            for (int w = 0; w < kRedThreads / 32; ++w) {
+                if (tid == kGramPairs) {
+                    v += wl[w];
+                } else {
+                    const float4 q4 = wq[w * 4 + (tid >> 2)];
+                    const int c = tid & 3;
+                    v += c == 0 ? q4.x : c == 1 ? q4.y : c == 2 ? q4.z : q4.w;
+                }
+            }
+            totals[tid] = v;
+        }
     }
     __syncthreads();
     float gram[kGramPairs];
@@ -208,7 +279,8 @@ __global__ void __launch_bounds__(kRedThreads, ADAM ? 3 : (EL == 8 ? 5 : 4))
             // partial rows are padded to a multiple of 32 floats: the float4 at
             // i4 < P stays inside the tile's slice
             const float* pp = a.partials + (int64_t)net * a.net_partial_stride;
-            sh[ty][tx] = i4 < P ? sum_tiles<TL>(pp, a.part_stride, n_parts, ty, i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            sh[ty][tx] = i4 < P ? sum_tiles<TL, EL == 64 ? 8 : 2>(pp, a.part_stride, n_parts, ty, i4)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
             __syncthreads();
             if (ty == 0) {
                 float g[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -255,20 +327,44 @@ __global__ void __launch_bounds__(kRedThreads, ADAM ? 3 : (EL == 8 ? 5 : 4))
         }
     }
     if constexpr (ADAM) {
-        fused_norms_adam<EL>(a, d, bar, bar_target, gacc, x);
+        fused_norms_adam<EL>(a, d, bar, bar_target, gacc, x, &sh[0][0]);
         return;
     }
-    float* gp = a.gram_part + ((int64_t)net * gridDim.x + blockIdx.x) * kGramPairs;
-    // the element lanes (ty == 0) are lanes 0..EL-1 of warp 0; the rest hold zeros.
-    // Lane 0 writes the block's Gram partial and alone fences before taking a
-    // ticket: the last block reads nothing else written in this launch.
-    if (wid == 0) {
+    float* gp = a.gram_part + ((int64_t)net * gridDim.x + blockIdx.x) * kGramStride;
+    // the element lanes (ty == 0) are threads 0..EL-1; the rest hold zeros.
+    // Thread 0 writes the block's Gram partial and alone fences before taking
+    // a ticket: the last block reads nothing else written in this launch.
+    if constexpr (EL <= 32) {
+        if (wid == 0) {
 #pragma unroll
-        for (int p = 0; p < kGramPairs; ++p) {
-            const float s = warp_sum(gacc[p]);
-            if (lane == 0) gp[p] = s;
+            for (int p = 0; p < kGramPairs; ++p) {
+                const float s = warp_sum(gacc[p]);
+                if (lane == 0) gp[p] = s;
+            }
+            if (lane == 0) {
+                __threadfence();
+                ticket = atomicAdd(a.counter + net, 1u);
+            }
         }
-        if (lane == 0) {
+    } else {
+        // element lanes in warps 0..EL/32-1: per-warp sums, then in warp order
+        __shared__ float gw[EL / 32][kGramPairs];
+        if (wid < EL / 32) {
+#pragma unroll
+            for (int p = 0; p < kGramPairs; ++p) {
+                const float s = warp_sum(gacc[p]);
+                if (lane == 0) gw[wid][p] = s;
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+#pragma unroll
+            for (int p = 0; p < kGramPairs; ++p) {
+                float s = gw[0][p];
+#pragma unroll
+                for (int w = 1; w < EL / 32; ++w) s += gw[w][p];
+                gp[p] = s;
+            }
             __threadfence();
             ticket = atomicAdd(a.counter + net, 1u);
         }
@@ -286,11 +382,11 @@ __global__ void __launch_bounds__(kRedThreads, ADAM ? 3 : (EL == 8 ? 5 : 4))
     float acc[kGramPairs + 1];
 #pragma unroll
     for (int p = 0; p <= kGramPairs; ++p) acc[p] = 0.0f;
-    const float* gall = a.gram_part + (int64_t)net * gridDim.x * kGramPairs;
+    const float* gall = a.gram_part + (int64_t)net * gridDim.x * kGramStride;
     for (int b = tid; b < (int)gridDim.x; b += kRedThreads) {
         float v[kGramPairs];
 #pragma unroll
-        for (int p = 0; p < kGramPairs; ++p) v[p] = __ldcg(gall + (int64_t)b * kGramPairs + p);
+        for (int p = 0; p < kGramPairs; ++p) v[p] = __ldcg(gall + (int64_t)b * kGramStride + p);
 #pragma unroll
         for (int p = 0; p < kGramPairs; ++p) acc[p] += v[p];
     }
@@ -468,11 +564,6 @@ cudaError_t launch_reduce_el(const ReduceLaunch& a, cudaStream_t st) {
                      (unsigned long long*)nullptr, 0ull);
 }
 
-int reduce_el(const ReduceLaunch& a) {
-    const int parts = a.n_parts > 0 ? a.n_parts : a.n_tiles;
-    return a.partials != nullptr && parts <= kManyParts ? 32 : 8;
-}
-
 // CTAs of the fused kernel resident at once on the current device (0
 // without cooperative launch support).
 template <int EL>
@@ -493,8 +584,21 @@ int max_resident_reduce_adam() {
     return n;
 }
 
+int reduce_el(const ReduceLaunch& a) {
+    const int parts = a.n_parts > 0 ? a.n_parts : a.n_tiles;
+    if (a.partials == nullptr) return 8;
+    if (parts <= kManyParts) return 32;
+    const int g = reduce_grid(a.P, 64);
+    if ((int64_t)g * 4 * 64 >= a.P && g * a.n_nets <= max_resident_reduce_adam<64>()) return 64;
+    return 8;
+}
+
 cudaError_t launch_reduce_gram(const ReduceLaunch& a, cudaStream_t st) {
-    return reduce_el(a) == 32 ? launch_reduce_el<32>(a, st) : launch_reduce_el<8>(a, st);
+    switch (reduce_el(a)) {
+        case 32: return launch_reduce_el<32>(a, st);
+        case 64: return launch_reduce_el<64>(a, st);
+        default: return launch_reduce_el<8>(a, st);
+    }
 }
 
 int reduce_adam_blocks(const ReduceLaunch& r) { return reduce_grid(r.P, reduce_el(r)) * r.n_nets; }
@@ -504,7 +608,9 @@ bool reduce_adam_fusable(const ReduceLaunch& r) {
     const int el = reduce_el(r);
     const int64_t per_pass = (int64_t)reduce_grid(r.P, el) * 4 * el;
     if (per_pass < r.P) return false;   // one pass of the grid must cover P
-    const int resident = el == 32 ? max_resident_reduce_adam<32>() : max_resident_reduce_adam<8>();
+    const int resident = el == 32   ? max_resident_reduce_adam<32>()
+                         : el == 64 ? max_resident_reduce_adam<64>()
+                                    : max_resident_reduce_adam<8>();
     return reduce_adam_blocks(r) <= resident;
 }
 
@@ -517,6 +623,12 @@ cudaError_t launch_reduce_adam(const ReduceLaunch& r, const AdamLaunch& a, unsig
         const cudaError_t e = configure_reduce<32, true>();
         if (e != cudaSuccess) return e;
         return launch_ex(reduce_gram_kernel<32, true>, grid, dim3(kRedThreads), 0, st, 1u, true, r, a, barrier,
+                         target);
+    }
+    if (el == 64) {
+        const cudaError_t e = configure_reduce<64, true>();
+        if (e != cudaSuccess) return e;
+        return launch_ex(reduce_gram_kernel<64, true>, grid, dim3(kRedThreads), 0, st, 1u, true, r, a, barrier,
                          target);
     }
     const cudaError_t e = configure_reduce<8, true>();

@@ -274,14 +274,16 @@ def test_step_with_source_guard_weight_bound_and_target():
 
 def test_reduce_and_adam_launch_fusion_choice():
     # the production batch (128 tiles, 32 cluster partials, 182 reduce
-    # blocks) takes the single cooperative reduce + Adam launch; the
-    # H = 256 workload (two V kernels, more than 64 K-range partials of 79k
-    # parameters) needs more reduce blocks than fit at once and keeps two
+    # blocks) and the H = 256 workload (76 K-range partials of 79k
+    # parameters, or 256 tile partials from the CUDA-core kernel: 64 element
+    # lanes, 310 blocks) take the single cooperative reduce + Adam launch;
+    # the layered path has two V kernels
     need_gpu()
-    for w, expect in ((synth.PROD, 3), (dataclasses.replace(synth.BUDGETED, capacity=1 << 16), 5)):
-        g = GpuStep(w)
+    for w, expect, path in ((synth.PROD, 3, None), (dataclasses.replace(synth.BUDGETED, capacity=1 << 16), 4, None),
+                            (dataclasses.replace(synth.BUDGETED, capacity=1 << 16), 3, "cuda_cores")):
+        g = GpuStep(w, path=path)
         try:
-            assert g.kernels() == expect, w.name
+            assert g.kernels() == expect, (w.name, path)
         finally:
             g.close()
 
