@@ -45,10 +45,14 @@ struct Layout {
     int64_t P;
 };
 
-// The tensor-core paths: weight and state-tile images for H = 128 and 256;
-// the layered path's activation images for H = 128 and 256 with S < 64.
-bool tc_images(const ofrl_vshape* s) { return s->hidden == 128 || s->hidden == 256; }
-bool layered_possible(const ofrl_vshape* s) { return tc_images(s) && s->state_dim < tc::KX; }
+// The tensor-core paths: weight and state-tile images for every H (H = 64
+// padded to 128 units); the layered path's activation images for H = 128 and
+// 256 with S < 64.
+bool tc_images(const ofrl_vshape* s) { return s->hidden == 64 || s->hidden == 128 || s->hidden == 256; }
+int image_width(int hidden) { return hidden < 128 ? 128 : hidden; }
+bool layered_possible(const ofrl_vshape* s) {
+    return (s->hidden == 128 || s->hidden == 256) && s->state_dim < tc::KX;
+}
 int planes_of(const ofrl_vshape* s) { return s->prec == OFRL_PREC_BF16 ? 1 : 3; }
 
 Layout layout_of(const ofrl_vshape* s, int32_t max_batch, int32_t max_nets) {
@@ -67,7 +71,7 @@ Layout layout_of(const ofrl_vshape* s, int32_t max_batch, int32_t max_nets) {
     L.off_status = take((int64_t)OFRL_STAT_WORDS * 4);
     L.tiles128 = (int32_t)((max_batch + tc::TM - 1) / tc::TM);
     L.layered = layered_possible(s);
-    L.off_img = take(tc_images(s) ? (int64_t)max_nets * tc::weight_image_bytes(s->hidden) : 0);
+    L.off_img = take(tc_images(s) ? (int64_t)max_nets * tc::weight_image_bytes(image_width(s->hidden)) : 0);
     L.off_ximg = take(tc_images(s) ? (int64_t)L.tiles128 * tc::x_tile_bytes() : 0);
     for (int k = 0; k < 3; ++k)
         L.off_act[k] = take(L.layered ? (int64_t)max_nets * L.tiles128 * vnet_wide_act_bytes(s->hidden, planes_of(s))
@@ -639,7 +643,7 @@ ofrl_status ofrl_select_vnet_path(ofrl_ctx* ctx, int32_t path) {
         case OFRL_VNET_AUTO:
         case OFRL_VNET_CUDA_CORES: break;
         case OFRL_VNET_TC_FUSED:
-            if (sh.hidden != 128 || sh.state_dim > tc::KX) return OFRL_EUNSUPPORTED;
+            if (sh.hidden > 128 || sh.state_dim > tc::KX) return OFRL_EUNSUPPORTED;
             break;
         case OFRL_VNET_TC_LAYERED:
             if (ctx->maps == nullptr) return OFRL_EUNSUPPORTED;
@@ -734,6 +738,7 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
         ha.img_rows = (B + tc::TM - 1) / tc::TM * tc::TM;
         ha.wimg = ctx->ws.img;
         ha.pack_hidden = sh.hidden;
+        ha.pack_width = v.path == PATH_FUSED ? tc::HH : sh.hidden;
         ha.pack_nets = n_nets;
         for (int k = 0; k < n_nets; ++k) ha.pack_params[k] = nets[k].params;
         v.ximg = ctx->ws.ximg;

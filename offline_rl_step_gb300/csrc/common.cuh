@@ -52,8 +52,8 @@ namespace ofrl {
 
 // Which V forward/backward implementation a step uses.
 enum VnetPath : int32_t {
-    PATH_AUTO = 0,      // fused tensor-core kernel for H = 128, layered for H = 256, else CUDA cores
-    PATH_FUSED = 1,     // vnet_tc.cu: one CTA per tile does all five GEMMs (H = 128)
+    PATH_AUTO = 0,      // fused tensor-core kernel for H <= 128, layered for H = 256, else CUDA cores
+    PATH_FUSED = 1,     // vnet_tc.cu: one CTA per tile does all five GEMMs (H = 128; 64 padded)
     PATH_LAYERED = 2,   // vnet_wide.cu: per-tile forward/backward, then split-K weight gradients
     PATH_SIMT = 3,      // vnet_simt.cu: CUDA cores
 };
@@ -316,7 +316,8 @@ struct HerLaunch {
     int32_t pack_nets;
     const float* pack_params[kMaxNets];
     uint8_t* wimg;          // per network: W1 image then W2 image
-    int32_t pack_hidden;    // H of the packed images
+    int32_t pack_hidden;    // H of the network
+    int32_t pack_width;     // units of the packed images (>= H; the rest zero)
     // optional: caller-given sources (e.g. PER-sampled) and importance
     // weights; HER rows get weight 1
     const int32_t* src_in;  // [batch] or null: sources drawn here

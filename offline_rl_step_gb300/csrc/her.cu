@@ -54,11 +54,12 @@ __device__ __forceinline__ int episode_search(const int32_t* __restrict__ ends, 
     return f < len ? lo + f : lo + len;
 }
 
-// Extra blocks of the relabel grid: W1 [H][S] -> [H x 64] image and
-// W2 [H][H] -> [H x H] image of every network, img_planes planes.
+// Extra blocks of the relabel grid: W1 [H][S] -> [W x 64] image and
+// W2 [H][H] -> [W x W] image of every network (W = pack_width >= H: units
+// past H zero), img_planes planes.
 __device__ void pack_weights(const HerLaunch& a) {
-    const int S = a.state_dim, H = a.pack_hidden, np = a.img_planes;
-    const Offsets off = offsets_of(S, H);
+    const int S = a.state_dim, Hn = a.pack_hidden, H = a.pack_width, np = a.img_planes;
+    const Offsets off = offsets_of(S, Hn);
     const int n1 = H * (tc::KX / 4), n2 = H * (H / 4);      // groups of 4 columns
     const int total = a.pack_nets * (n1 + n2);
     for (int e = (blockIdx.x - a.relabel_blocks) * blockDim.x + threadIdx.x; e < total;
@@ -72,12 +73,13 @@ __device__ void pack_weights(const HerLaunch& a) {
         if (f < n1) {
             const int r = f / (tc::KX / 4), c = 4 * (f % (tc::KX / 4));
 #pragma unroll
-            for (int j = 0; j < 4; ++j) x[j] = c + j < S ? __ldg(prm + off.w1 + (int64_t)r * S + c + j) : 0.0f;
+            for (int j = 0; j < 4; ++j)
+                x[j] = r < Hn && c + j < S ? __ldg(prm + off.w1 + (int64_t)r * S + c + j) : 0.0f;
             tc::put4(w1i, plane1, np, tc::KX, r, c, x);
         } else {
             const int g = f - n1, r = g / (H / 4), c = 4 * (g % (H / 4));
 #pragma unroll
-            for (int j = 0; j < 4; ++j) x[j] = __ldg(prm + off.w2 + (int64_t)r * H + c + j);
+            for (int j = 0; j < 4; ++j) x[j] = r < Hn && c + j < Hn ? __ldg(prm + off.w2 + (int64_t)r * Hn + c + j) : 0.0f;
             tc::put4(w2i, plane2, np, H, r, c, x);
         }
     }
@@ -285,7 +287,7 @@ cudaError_t launch_her_relabel(const HerLaunch& a_in, cudaStream_t st) {
     const int rows = a.ximg != nullptr ? a.img_rows : a.batch;
     a.relabel_blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
     // the weight images grow with H^2: 48 blocks at H = 128
-    a.pack_blocks = a.wimg != nullptr ? (a.pack_hidden > 128 ? 160 : 48) : 0;
+    a.pack_blocks = a.wimg != nullptr ? (a.pack_width > 128 ? 160 : 48) : 0;
     static bool configured = false;
     if (!configured) {
         const cudaError_t e = set_max_shared_carveout(her_relabel_kernel);

@@ -1,6 +1,8 @@
 // IQL value network V(s) forward, expectile loss, policy and backward for one
 // 128-row batch tile per CTA on the 5th-generation tensor cores (tcgen05),
-// hidden width 128.
+// hidden width 128 (64 runs zero-padded to 128 units: padded units have zero
+// weights, biases and output weight, so their activations and gradients are
+// exactly zero, and only the H x H, H x S and H entries are written out).
 //
 // Method: "GPU IQL + HER Porting Plan", "IQL (CPU)" items 1-3 and "CUDA
 // Kernel: iql_value_kernel.cu"; same results as the CUDA-core kernel
@@ -168,7 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     const int tile = blockIdx.x, net = blockIdx.y;
     const int S = a.state_dim, B = a.batch, NA = a.num_actions;
     const int row0 = tile * TM;
-    const Offsets off = offsets_of(S, HH);
+    const int Hn = a.hidden;   // 64 or 128: the weights are zero-padded to 128 units
+    const Offsets off = offsets_of(S, Hn);
     const float* __restrict__ prm = a.params[net];
     const float tau = a.tau[net];
     const uint8_t* w1i = wimg + (int64_t)net * tc::weight_image_bytes();
@@ -192,9 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         umma::bulk_g2s(sm.r1, w1i, kXBytes, &sm.bar_load);
     }
     for (int i = tid; i < HH; i += kThreads) {
-        sm.b1[i] = __ldg(prm + off.b1 + i);
-        sm.b2[i] = __ldg(prm + off.b2 + i);
-        sm.w3[i] = __ldg(prm + off.w3 + i);
+        const bool u = i < Hn;   // padded units: zero bias and output weight, so they stay zero
+        sm.b1[i] = u ? __ldg(prm + off.b1 + i) : 0.0f;
+        sm.b2[i] = u ? __ldg(prm + off.b2 + i) : 0.0f;
+        sm.w3[i] = u ? __ldg(prm + off.w3 + i) : 0.0f;
     }
     const float b3 = __ldg(prm + off.b3);
     // the tile's actions and Q rows (one contiguous block) for the loss and
@@ -518,16 +522,16 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     const int cn = a.cluster;
     float* dst = a.partials + (int64_t)net * a.net_partial_stride + (int64_t)(tile / cn) * a.part_stride;
     if (cn == 1) {
-        // the tile's partial: one 512-byte bulk copy per dW2 row, one for
+        // the tile's partial: one bulk copy per dW2 row (H floats), one for
         // dW1, one per vector (all offsets and sizes multiples of 16 bytes)
         umma::fence_smem_to_async();
         __syncthreads();
-        if (tid < HH) {
-            umma::bulk_s2g(dst + off.w2 + tid * HH, st2 + tid * kStride2, (uint32_t)(HH * 4));
-            if (tid == 0) umma::bulk_s2g(dst + off.w1, st1, (uint32_t)(HH * S * 4));
-            if (tid == 1) umma::bulk_s2g(dst + off.w3, sm.vec[0], (uint32_t)(HH * 4));
-            if (tid == 2) umma::bulk_s2g(dst + off.b2, sm.vec[1], (uint32_t)(HH * 4));
-            if (tid == 3) umma::bulk_s2g(dst + off.b1, sm.vec[2], (uint32_t)(HH * 4));
+        if (tid < Hn) {
+            umma::bulk_s2g(dst + off.w2 + tid * Hn, st2 + tid * kStride2, (uint32_t)(Hn * 4));
+            if (tid == 0) umma::bulk_s2g(dst + off.w1, st1, (uint32_t)(Hn * S * 4));
+            if (tid == 1) umma::bulk_s2g(dst + off.w3, sm.vec[0], (uint32_t)(Hn * 4));
+            if (tid == 2) umma::bulk_s2g(dst + off.b2, sm.vec[1], (uint32_t)(Hn * 4));
+            if (tid == 3) umma::bulk_s2g(dst + off.b1, sm.vec[2], (uint32_t)(Hn * 4));
             if (tid == 4) dst[off.b3] = sm.vb3;
             umma::bulk_commit();
             umma::bulk_wait_read();
@@ -540,12 +544,12 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         // stores that slice of the cluster's partial.
         umma::cluster_sync();
         const int rank = (int)umma::cluster_rank();
-        const int rows = HH / cn, r0 = rank * rows;
+        const int rows = Hn / cn, r0 = rank * rows;
         // one flat list of float4 items: the dW2 rows, then the dW1 rows of
         // the slice; every thread issues the loads of up to kItems items from
         // all cn CTAs before it adds (the loads are latency-bound)
         constexpr int kItems = 3;
-        const int n2 = rows * (HH / 4), n1 = rows * S / 4;
+        const int n2 = rows * (Hn / 4), n1 = rows * S / 4;
         for (int base = tid; base < n2 + n1; base += kItems * kThreads) {
             float4 v[kItems][4];
             uint32_t src[kItems];
@@ -554,9 +558,9 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
             for (int k = 0; k < kItems; ++k) {
                 const int e = base + k * kThreads;
                 if (e < n2) {
-                    const int r = r0 + e / (HH / 4), c = 4 * (e % (HH / 4));
+                    const int r = r0 + e / (Hn / 4), c = 4 * (e % (Hn / 4));
                     src[k] = umma::smem_u32(st2 + r * kStride2 + c);
-                    dp[k] = dst + off.w2 + r * HH + c;
+                    dp[k] = dst + off.w2 + r * Hn + c;
                 } else {
                     const int i = r0 * S + 4 * (e - n2);
                     src[k] = umma::smem_u32(st1 + i);
@@ -591,12 +595,12 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
 }
 
 // Pack W1 ([H][S] -> [128 x 64] image) and W2 ([H][H] -> [128 x 128] image)
-// of every network into NP bf16 planes each (standalone V forward/backward;
-// the fused step packs inside the relabel launch).
+// of every network into NP bf16 planes each, units past H zero (standalone V
+// forward/backward; the fused step packs inside the relabel launch).
 __global__ void pack_weights_kernel(const VnetLaunch a, uint8_t* __restrict__ img, int np) {
     const int net = blockIdx.y;
-    const int S = a.state_dim;
-    const Offsets off = offsets_of(S, HH);
+    const int S = a.state_dim, Hn = a.hidden;
+    const Offsets off = offsets_of(S, Hn);
     const float* __restrict__ prm = a.params[net];
     uint8_t* w1i = img + (int64_t)net * tc::weight_image_bytes();
     uint8_t* w2i = w1i + tc::w2_image_offset();
@@ -606,12 +610,13 @@ __global__ void pack_weights_kernel(const VnetLaunch a, uint8_t* __restrict__ im
         if (e < n1) {
             const int r = e / (KX / 4), c = 4 * (e % (KX / 4));
 #pragma unroll
-            for (int j = 0; j < 4; ++j) x[j] = c + j < S ? __ldg(prm + off.w1 + (int64_t)r * S + c + j) : 0.0f;
+            for (int j = 0; j < 4; ++j)
+                x[j] = r < Hn && c + j < S ? __ldg(prm + off.w1 + (int64_t)r * S + c + j) : 0.0f;
             tc::put4(w1i, kPlaneX, np, KX, r, c, x);
         } else {
             const int f = e - n1, r = f / (HH / 4), c = 4 * (f % (HH / 4));
 #pragma unroll
-            for (int j = 0; j < 4; ++j) x[j] = __ldg(prm + off.w2 + (int64_t)r * HH + c + j);
+            for (int j = 0; j < 4; ++j) x[j] = r < Hn && c + j < Hn ? __ldg(prm + off.w2 + (int64_t)r * Hn + c + j) : 0.0f;
             tc::put4(w2i, kPlaneH, np, HH, r, c, x);
         }
     }
@@ -686,7 +691,7 @@ int vnet_tc_cluster(int n_tiles) {
 }
 
 bool vnet_tc_supported(const VnetLaunch& a) {
-    return a.hidden == HH && a.state_dim <= KX && (a.stride & 3) == 0 &&
+    return (a.hidden == HH || a.hidden == HH / 2) && a.state_dim <= KX && (a.stride & 3) == 0 &&
            (reinterpret_cast<uintptr_t>(a.states) & 15) == 0;
 }
 

@@ -48,7 +48,8 @@ def test_value_fwd_bwd_fp32(s, h, b):
 
 
 @pytest.mark.parametrize("s,h,b,path", [(50, 128, 1000, "tc_layered"), (63, 128, 300, "tc_layered"),
-                                        (1, 256, 129, "tc_layered"), (50, 256, 1000, "cuda_cores")])
+                                        (1, 256, 129, "tc_layered"), (50, 256, 1000, "cuda_cores"),
+                                        (48, 64, 256, "cuda_cores"), (50, 64, 16384, "tc_fused")])
 def test_value_fwd_bwd_each_path(s, h, b, path):
     # the implementations the default choice does not take for these shapes
     (v, loss, g), (rv, rl, rg, vu, gu) = _fwd_bwd(s, h, b, 0.7, seed=s + h + b, path=path)

@@ -181,7 +181,7 @@ def test_vnet_path_choice():
     need_gpu()
     import offline_rl_step_gb300 as ofrl
     from offline_rl_step_gb300 import _abi
-    want = {64: "cuda_cores", 128: "tc_fused", 256: "tc_layered"}
+    want = {64: "tc_fused", 128: "tc_fused", 256: "tc_layered"}
     for h, path in want.items():
         for nets in (1, 2):
             ctx = ofrl.Context(50, h, 5, "fp32", max_batch=4096, max_nets=nets)
@@ -190,7 +190,7 @@ def test_vnet_path_choice():
                 ctx.select_vnet_path("cuda_cores")
                 assert ctx.vnet_path(nets) == "cuda_cores"
                 for other in ("tc_fused", "tc_layered"):
-                    ok = (other == "tc_fused" and h == 128) or (other == "tc_layered" and h in (128, 256))
+                    ok = (other == "tc_fused" and h <= 128) or (other == "tc_layered" and h in (128, 256))
                     if ok:
                         ctx.select_vnet_path(other)
                         assert ctx.vnet_path(nets) == other
@@ -213,7 +213,10 @@ def test_vnet_path_choice():
     (dataclasses.replace(synth.PROD, batch=1000, capacity=1 << 14, steps=2), "cuda_cores"),
     (dataclasses.replace(synth.BUDGETED, batch=1000, capacity=1 << 14, steps=2), "cuda_cores"),
     (dataclasses.replace(synth.BUDGETED, batch=128, capacity=1 << 14, steps=2), "tc_layered"),
-], ids=["prod_layered", "twin_bf16_layered", "prod_cuda_cores", "budgeted_cuda_cores", "budgeted_one_tile"])
+    (dataclasses.replace(synth.TINY, steps=2), "cuda_cores"),
+    (dataclasses.replace(synth.TINY, batch=1000, capacity=1 << 14, steps=2), "tc_fused"),
+], ids=["prod_layered", "twin_bf16_layered", "prod_cuda_cores", "budgeted_cuda_cores", "budgeted_one_tile",
+        "tiny_cuda_cores", "h64_ragged_fused"])
 def test_step_on_each_vnet_path(w, path):
     # every implementation against the oracle (the default ones run in the tests above)
     test_train_step_matches_oracle(w, path=path)
