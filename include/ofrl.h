@@ -319,7 +319,14 @@ ofrl_status ofrl_target_ema(const float* params, float* target, int64_t n, float
  * pi_out [n_nets, B, A], argmax_out [n_nets, B], loss_out [n_nets],
  * norms_out [n_nets, 5] (n_0..n_3 pre-clip source norms, 0 for absent
  * sources, then the combined norm), grad_out [n_nets, P] (the primary
- * gradient g0).  Increments nets[k].t on the host. */
+ * gradient g0).  Increments nets[k].t on the host.
+ * When the previous launch of this context on `stream` was a train step, the
+ * relabel of this step's batch starts while that step's optimizer kernel
+ * still runs (it reads only the replay buffer and writes only the batch;
+ * the V kernel still waits for both).  Writes to the replay buffer in
+ * between by ordinary kernels or copies are ordered as usual; a kernel of
+ * the caller's that lets its dependents launch early (programmatic
+ * dependent launch) must not write the replay buffer right before a step. */
 ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl_her_cfg* her,
                             uint64_t step, const ofrl_batch* batch, const float* q,
                             ofrl_vnet* nets, int32_t n_nets, const ofrl_opt* opt,

@@ -298,6 +298,8 @@ ofrl_status ofrl_create(const ofrl_vshape* shape, int32_t max_batch, int32_t max
     ctx->ws.barrier = reinterpret_cast<unsigned long long*>(b + L.off_barrier);
     ctx->barrier_arrivals = 0;
     ctx->vnet_path = PATH_AUTO;
+    ctx->early_ok = 0;
+    ctx->early_stream = nullptr;
     ctx->act_tiles = L.tiles128;
     ctx->tvec_stride = L.layered ? vnet_wide_tvec_stride(shape->hidden) : 0;
     ctx->maps = nullptr;
@@ -360,6 +362,7 @@ ofrl_status ofrl_her_relabel(ofrl_ctx* ctx, const ofrl_replay* replay, const ofr
     if (s == OFRL_OK) s = check_replay(replay, her);
     if (s == OFRL_OK) s = check_batch(out, replay->state_dim);
     if (s != OFRL_OK) return s;
+    ctx->early_ok = 0;
     if (step >= (1ull << 32)) return OFRL_EINVAL;
     if ((int64_t)her->batch >= (1ll << 31)) return OFRL_EINVAL;
     const HerLaunch a = her_args(ctx, replay, her, step, out);
@@ -373,6 +376,7 @@ ofrl_status ofrl_her_relabel_sources(ofrl_ctx* ctx, const ofrl_replay* replay, c
     if (s == OFRL_OK) s = check_replay(replay, her);
     if (s == OFRL_OK) s = check_batch(out, replay->state_dim);
     if (s != OFRL_OK) return s;
+    ctx->early_ok = 0;
     if (src_idx == nullptr || step >= (1ull << 32)) return OFRL_EINVAL;
     HerLaunch a = her_args(ctx, replay, her, step, out);
     a.src_in = src_idx;
@@ -386,6 +390,7 @@ ofrl_status ofrl_episode_ends_append(ofrl_ctx* ctx, const float* dones, int64_t 
                                      void* stream) {
     ofrl_status s = check_ctx(ctx);
     if (s != OFRL_OK) return s;
+    ctx->early_ok = 0;
     if (n < 0 || first_index < 0 || first_index + (int64_t)n > INT32_MAX || max_episodes < 0) return OFRL_EINVAL;
     if (n > 0 && (!dones || !episode_ends || !num_episodes)) return OFRL_EINVAL;
     return cuda_status(launch_episode_ends_append(dones, first_index, n, episode_ends, num_episodes, max_episodes,
@@ -399,6 +404,7 @@ ofrl_status value_forward(ofrl_ctx* ctx, const float* params, const float* state
                           float* target_out, void* stream) {
     ofrl_status s = check_ctx(ctx);
     if (s != OFRL_OK) return s;
+    ctx->early_ok = 0;
     const ofrl_vshape& sh = ctx->shape;
     if (!params || !states || (!v_out && !target_out)) return OFRL_EINVAL;
     if (batch < 1 || batch > ctx->max_batch || state_stride < sh.state_dim) return OFRL_EINVAL;
@@ -444,6 +450,7 @@ ofrl_status ofrl_iql_value_fwd_bwd(ofrl_ctx* ctx, const float* params, const flo
                                    float* v_out, float* loss_out, float* grad_out, void* stream) {
     ofrl_status s = check_ctx(ctx);
     if (s != OFRL_OK) return s;
+    ctx->early_ok = 0;
     const ofrl_vshape& sh = ctx->shape;
     if (!params || !states || !q_taken || !v_out || !loss_out || !grad_out) return OFRL_EINVAL;
     if (batch < 1 || batch > ctx->max_batch || state_stride < sh.state_dim) return OFRL_EINVAL;
@@ -502,6 +509,7 @@ ofrl_status ofrl_expectile_loss(ofrl_ctx* ctx, const float* q_taken, const float
                                 float tau, float* loss_out, float* dv_out, void* stream) {
     ofrl_status s = check_ctx(ctx);
     if (s != OFRL_OK) return s;
+    ctx->early_ok = 0;
     if (!q_taken || !v || !loss_out || batch < 1) return OFRL_EINVAL;
     if (!(tau >= 0.0f && tau <= 1.0f)) return OFRL_EINVAL;
     return cuda_status(launch_expectile(q_taken, v, batch, tau, loss_out, dv_out,
@@ -513,6 +521,7 @@ ofrl_status ofrl_adv_weighted_policy(ofrl_ctx* ctx, const float* q, const float*
                                      void* stream) {
     ofrl_status s = check_ctx(ctx);
     if (s != OFRL_OK) return s;
+    ctx->early_ok = 0;
     if (!q || !v || !pi_out || batch < 1 || num_actions < 1 || num_actions > kMaxActions) return OFRL_EINVAL;
     if (std::isnan(beta)) return OFRL_EINVAL;
     return cuda_status(launch_policy(q, v, batch, num_actions, beta, pi_out, argmax_out, 0, 1,
@@ -524,6 +533,7 @@ ofrl_status ofrl_budgeted_clip_saxpy(ofrl_ctx* ctx, const float* const* src, con
                                      float* grad_out, float* norms_out, void* stream) {
     ofrl_status s = check_ctx(ctx);
     if (s != OFRL_OK) return s;
+    ctx->early_ok = 0;
     if (!src || !budget_frac || !alpha || !grad_out || n_src < 1 || n_src > kMaxSrc || n < 1) return OFRL_EINVAL;
     if (!(max_grad_norm > 0.0f)) return OFRL_EINVAL;
     for (int k = 0; k < n_src; ++k) {
@@ -569,6 +579,7 @@ ofrl_status ofrl_adam_step(ofrl_ctx* ctx, float* p, const float* g, float* m, fl
     ofrl_status s = check_ctx(ctx);
     if (s == OFRL_OK) s = check_opt(opt);
     if (s != OFRL_OK) return s;
+    ctx->early_ok = 0;
     if (!p || !g || !m || !v || n < 1 || t < 1) return OFRL_EINVAL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     AdamLaunch a;
@@ -732,6 +743,8 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
     // 1. HER relabel (+ state-tile images and packed weights for the tensor-core kernel)
     prof_mark(ctx, 0, st);
     HerLaunch ha = her_args(ctx, replay, her, step, batch);
+    ha.early = ctx->early_ok && ctx->early_stream == stream ? 1 : 0;
+    ctx->early_ok = 0;
     if (tc_path) {
         ha.ximg = ctx->ws.ximg;
         ha.img_planes = sh.prec == OFRL_PREC_BF16 ? 1 : 3;
@@ -827,6 +840,10 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
     }
     prof_mark(ctx, 4, st);
     if (ctx->prof_events != nullptr && ctx->prof_count < ctx->prof_max) ctx->prof_count++;
+    // the step ends with the optimizer kernel, which lets dependents launch
+    // only after its own wait: the next step's relabel may start early
+    ctx->early_ok = 1;
+    ctx->early_stream = stream;
     return OFRL_OK;
 }
 

@@ -83,6 +83,10 @@ struct ofrl_ctx {
     int64_t bytes;
     ofrl::Workspace ws;
     int32_t vnet_path;          // ofrl::VnetPath requested (PATH_AUTO unless selected)
+    // the last launch of this context was the optimizer kernel of a train
+    // step on early_stream: the next step's relabel rows may start early
+    int32_t early_ok;
+    void* early_stream;
     int32_t act_tiles;          // 128-row tiles per network in ws.act / ws.tvec
     int32_t tvec_stride;
     ofrl::WideMaps* maps;       // tensor maps of the layered path (null: not available)
@@ -316,6 +320,7 @@ struct HerLaunch {
     int32_t pack_nets;
     const float* pack_params[kMaxNets];
     uint8_t* wimg;          // per network: W1 image then W2 image
+    int32_t early;          // 1: the row blocks do not wait for the previous kernel (see her_relabel_kernel)
     int32_t pack_hidden;    // H of the network
     int32_t pack_width;     // units of the packed images (>= H; the rest zero)
     // optional: caller-given sources (e.g. PER-sampled) and importance

@@ -73,7 +73,9 @@ extern "C" ofrl_status ofrl_step_graph_create(ofrl_ctx* ctx, const ofrl_replay* 
     const cudaError_t ec = cudaStreamEndCapture(st, &graph);
     cudaStreamDestroy(st);
     // the capture launched nothing: t and the barrier count are as before
+    // (and the captured relabel has no kernel before it in the graph)
     for (int k = 0; k < n_nets; ++k) nets[k].t = t0[k];
+    ctx->early_ok = 0;
     const uint64_t per_replay = ctx->barrier_arrivals - arrivals0;
     ctx->barrier_arrivals = arrivals0;
     if (s != OFRL_OK || ec != cudaSuccess || graph == nullptr) {
@@ -191,6 +193,7 @@ extern "C" ofrl_status ofrl_step_graph_launch(ofrl_step_graph* g, uint64_t step,
         for (int i = 0; i < g->n_nets * g->n_aux; ++i)
             if (aux_src[i] == nullptr) return OFRL_EINVAL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    g->ctx->early_ok = 0;
     // 1. relabel: the step index
     g->her.step = step;
     void* a0[] = {&g->her};

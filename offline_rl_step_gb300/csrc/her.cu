@@ -87,7 +87,13 @@ __device__ void pack_weights(const HerLaunch& a) {
 
 __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerLaunch a) {
     pdl_trigger();
-    pdl_wait();
+    // The weight packing reads what the previous kernel (Adam) wrote.  The
+    // rows read only the replay buffer: with `early` set (the previous kernel
+    // on the stream is the optimizer of a train step, which lets dependents
+    // launch only after everything before it, the V kernel included, has
+    // completed) they run while that kernel still does.  Block 0 waits in
+    // any case, so this grid completes only after the previous one did.
+    if (!a.early || blockIdx.x == 0 || (int)blockIdx.x >= a.relabel_blocks) pdl_wait();
     if ((int)blockIdx.x >= a.relabel_blocks) {
         pack_weights(a);
         return;

@@ -261,8 +261,11 @@ __global__ void __launch_bounds__(kRedThreads, ADAM ? 3 : (EL == 8 ? 5 : 4))
     const int net = blockIdx.y;
     const int64_t P = a.P;
     const int nsrc = a.n_src;
-    pdl_trigger();
+    // dependents launch only once everything before this kernel (the V
+    // kernel reading the batch) has completed: the next step's relabel rows
+    // may then overwrite the batch without waiting for this kernel
     pdl_wait();
+    pdl_trigger();
 
     float gacc[kGramPairs];
 #pragma unroll
@@ -434,8 +437,8 @@ __global__ void __launch_bounds__(kRedThreads, ADAM ? 3 : (EL == 8 ? 5 : 4))
 }
 
 __global__ void __launch_bounds__(256) adam_kernel(const AdamLaunch a) {
+    pdl_wait();      // then dependents (as in reduce_gram_kernel)
     pdl_trigger();
-    pdl_wait();
     const int net = blockIdx.y;
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     float coef[kMaxSrc] = {1.0f, 0.0f, 0.0f, 0.0f};
