@@ -393,8 +393,9 @@ int vnet_wide_ranges(const VnetLaunch& a, int num_sms);  // partials per network
 cudaError_t launch_vnet_wide_pack(const VnetLaunch& a, uint8_t* wimg, uint8_t* ximg, cudaStream_t st);
 cudaError_t launch_vnet_wide(const VnetLaunch& a, const uint8_t* wimg, cudaStream_t st);
 // Tiles whose gradient partials the tensor-core kernel sums into one (a
-// thread-block cluster): the largest of 4, 2, 1 that divides n_tiles and
-// that the device can schedule.  Its partials count is n_tiles / that.
+// thread-block cluster): the smallest of 1, 2, 4 that divides n_tiles, that
+// the device can schedule and that leaves at most 128 partials (else the
+// largest).  Its partials count is n_tiles / that.
 int vnet_tc_cluster(int n_tiles);
 
 struct ReduceLaunch {

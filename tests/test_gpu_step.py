@@ -215,8 +215,9 @@ def test_vnet_path_choice():
     (dataclasses.replace(synth.BUDGETED, batch=128, capacity=1 << 14, steps=2), "tc_layered"),
     (dataclasses.replace(synth.TINY, steps=2), "cuda_cores"),
     (dataclasses.replace(synth.TINY, batch=1000, capacity=1 << 14, steps=2), "tc_fused"),
+    (dataclasses.replace(synth.PROD, batch=32768, steps=2), "tc_fused"),
 ], ids=["prod_layered", "twin_bf16_layered", "prod_cuda_cores", "budgeted_cuda_cores", "budgeted_one_tile",
-        "tiny_cuda_cores", "h64_ragged_fused"])
+        "tiny_cuda_cores", "h64_ragged_fused", "prod_256_tiles_cluster2"])
 def test_step_on_each_vnet_path(w, path):
     # every implementation against the oracle (the default ones run in the tests above)
     test_train_step_matches_oracle(w, path=path)
@@ -276,11 +277,10 @@ def test_step_with_source_guard_weight_bound_and_target():
 
 
 def test_reduce_and_adam_launch_fusion_choice():
-    # the production batch (128 tiles, 32 cluster partials, 182 reduce
-    # blocks) and the H = 256 workload (76 K-range partials of 79k
-    # parameters, or 256 tile partials from the CUDA-core kernel: 64 element
-    # lanes, 310 blocks) take the single cooperative reduce + Adam launch;
-    # the layered path has two V kernels
+    # the production batch (128 tile partials: 64 element lanes, 91 blocks)
+    # and the H = 256 workload (76 K-range partials of 79k parameters, or 256
+    # tile partials from the CUDA-core kernel: 310 blocks) take the single
+    # cooperative reduce + Adam launch; the layered path has two V kernels
     need_gpu()
     for w, expect, path in ((synth.PROD, 3, None), (dataclasses.replace(synth.BUDGETED, capacity=1 << 16), 4, None),
                             (dataclasses.replace(synth.BUDGETED, capacity=1 << 16), 3, "cuda_cores")):
