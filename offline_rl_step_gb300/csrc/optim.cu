@@ -27,11 +27,13 @@ namespace ofrl {
 namespace {
 
 // A reduce block is EL element lanes (a float4 each) x 256 / EL partial
-// lanes: EL = 32 for few partials (8 partial lanes); for many, EL = 64 (4
-// partial lanes, eight loads in flight each) when that grid covers P in one
-// resident pass, else EL = 8 (32 partial lanes).
+// lanes, each with eight loads in flight: EL = 32 (8 partial lanes), or for
+// many partials EL = 64 when only that grid covers P in one resident pass
+// (the reduce and Adam then run as one launch), else EL = 8 (32 partial
+// lanes, two launches).
 constexpr int kRedThreads = 256;
-constexpr int kManyParts = 64;     // more partials than this: EL = 64 or 8
+constexpr int kManyParts = 64;     // more partials than this: EL = 32 or 64 (fused), else 8
+constexpr int kRedUnroll = 8;      // partial loads in flight per thread
 constexpr int kMaxGramBlocks = 2048;
 
 __device__ __forceinline__ void add4(float4& s, const float4& v) {
@@ -249,7 +251,7 @@ __device__ __forceinline__ void fused_norms_adam(const ReduceLaunch& a, const Ad
 // applies the clipped combination and Adam to its own elements, which its
 // element lanes still hold.
 template <int EL, bool ADAM>
-__global__ void __launch_bounds__(kRedThreads, ADAM ? 3 : (EL == 8 ? 5 : 4))
+__global__ void __launch_bounds__(kRedThreads, ADAM ? 3 : 4)
     reduce_gram_kernel(const ReduceLaunch a, const AdamLaunch d, unsigned long long* bar,
                        unsigned long long bar_target) {
     constexpr int TL = kRedThreads / EL, kRedElems = 4 * EL;
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(kRedThreads, ADAM ? 3 : (EL == 8 ? 5 : 4))
             // partial rows are padded to a multiple of 32 floats: the float4 at
             // i4 < P stays inside the tile's slice
             const float* pp = a.partials + (int64_t)net * a.net_partial_stride;
-            sh[ty][tx] = i4 < P ? sum_tiles<TL, EL == 64 ? 8 : 2>(pp, a.part_stride, n_parts, ty, i4)
+            sh[ty][tx] = i4 < P ? sum_tiles<TL, kRedUnroll>(pp, a.part_stride, n_parts, ty, i4)
                                 : make_float4(0.f, 0.f, 0.f, 0.f);
             __syncthreads();
             if (ty == 0) {
@@ -587,12 +589,22 @@ int max_resident_reduce_adam() {
     return n;
 }
 
+// One pass of the EL-lane grid covers P and fits on the device at once.
+template <int EL>
+bool fits_one_pass(const ReduceLaunch& a) {
+    const int g = reduce_grid(a.P, EL);
+    return (int64_t)g * 4 * EL >= a.P && g * a.n_nets <= max_resident_reduce_adam<EL>();
+}
+
 int reduce_el(const ReduceLaunch& a) {
     const int parts = a.n_parts > 0 ? a.n_parts : a.n_tiles;
     if (a.partials == nullptr) return 8;
     if (parts <= kManyParts) return 32;
-    const int g = reduce_grid(a.P, 64);
-    if ((int64_t)g * 4 * 64 >= a.P && g * a.n_nets <= max_resident_reduce_adam<64>()) return 64;
+    // many partials: 32 element lanes (8 partial lanes), else 64, when that
+    // grid fits one pass (measured with 128 partials: 33.9 us a step at 32
+    // lanes, 34.9 at 64, 35.2 at 16, whose grid is twice as large)
+    if (fits_one_pass<32>(a)) return 32;
+    if (fits_one_pass<64>(a)) return 64;
     return 8;
 }
 
