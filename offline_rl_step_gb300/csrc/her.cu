@@ -91,15 +91,19 @@ __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerL
     // rows read only the replay buffer: with `early` set (the previous kernel
     // on the stream is the optimizer of a train step, which lets dependents
     // launch only after everything before it, the V kernel included, has
-    // completed) they run while that kernel still does.  Block 0 waits in
-    // any case, so this grid completes only after the previous one did.
-    if (!a.early || blockIdx.x == 0 || (int)blockIdx.x >= a.relabel_blocks) pdl_wait();
-    if ((int)blockIdx.x >= a.relabel_blocks) {
+    // completed) they run while that kernel still does.  The last row block
+    // waits in any case, so this grid completes only after the previous one
+    // did.
+    const int rb = a.relabel_blocks;
+    if (!a.early || (int)blockIdx.x >= rb - 1) pdl_wait();
+    if ((int)blockIdx.x >= rb) {
         pack_weights(a);
         return;
     }
     const int sub = threadIdx.x & (kLanesPerRow - 1);
-    const int row_raw = blockIdx.x * kRowsPerBlock + threadIdx.x / kLanesPerRow;
+    // blocks in reverse row order: the HER rows (the last rows, with the
+    // longest chain of dependent loads) are dispatched first
+    const int row_raw = (rb - 1 - (int)blockIdx.x) * kRowsPerBlock + threadIdx.x / kLanesPerRow;
     const bool live = row_raw < a.batch;
     if (a.ximg != nullptr && row_raw >= a.batch && row_raw < a.img_rows) {
         // the last tile's rows past the batch: zero image rows
