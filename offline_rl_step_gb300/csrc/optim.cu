@@ -74,17 +74,17 @@ __device__ __forceinline__ void fused_norms_adam(const ReduceLaunch& a, const Ad
     const int net = blockIdx.y, G = gridDim.x, nsrc = a.n_src;
     const int64_t P = a.P;
     const int64_t i4 = (int64_t)blockIdx.x * kRedElems + 4 * tx;
-    // this lane's weights and moments, read before the barrier (only this
-    // block writes them)
-    float pv[4], mv[4], vv[4];
-    if (ty == 0) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if (i4 + e < P) {
-                pv[e] = d.p[net][i4 + e];
-                mv[e] = d.m[net][i4 + e];
-                vv[e] = d.v[net][i4 + e];
-            }
+    // Adam runs one element per thread (threads 0 .. 4 EL - 1): this
+    // thread's weight, moments and target, read before the barrier (only
+    // this block writes them)
+    const int64_t ie = (int64_t)blockIdx.x * kRedElems + tid;
+    const bool has_e = tid < kRedElems && ie < P;
+    float pe = 0.0f, me = 0.0f, ve = 0.0f, te = 0.0f;
+    if (has_e) {
+        pe = d.p[net][ie];
+        me = d.m[net][ie];
+        ve = d.v[net][ie];
+        if (d.target[net] != nullptr) te = d.target[net][ie];
     }
     float* gp = a.gram_part + ((int64_t)net * G + blockIdx.x) * kGramStride;
     if constexpr (EL <= 32) {
@@ -212,36 +212,43 @@ __device__ __forceinline__ void fused_norms_adam(const ReduceLaunch& a, const Ad
         if (a.loss_out != nullptr) a.loss_out[net] = r.loss;
     }
 
-    // the clipped combination and Adam on this lane's elements (the sources
-    // in x are already the guarded ones when sanitize is on)
-    int bad = 0;
+    // the clipped combination and Adam, one element per thread: the element
+    // lanes hand their sources (already guarded when sanitize is on) over
+    // through `scratch` (free since the totals; it holds kMaxSrc x 4 EL floats)
+    float* xs = reinterpret_cast<float*>(scratch);
     if (ty == 0) {
+#pragma unroll
+        for (int k = 0; k < kMaxSrc; ++k)
+            if (k < nsrc) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) xs[k * kRedElems + 4 * tx + e] = x[k][e];
+            }
+    }
+    __syncthreads();
+    int bad = 0;
+    if (has_e) {
         const float s = clip_scale(r.combined, d.max_grad_norm);
+        float gsum = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int64_t i = i4 + e;
-            if (i >= P) continue;
-            float gsum = 0.0f;
-#pragma unroll
-            for (int k = 0; k < kMaxSrc; ++k)
-                if (k < nsrc) gsum = fmaf(r.coef[k], x[k][e], gsum);
-            const float g = s * gsum;
-            float p = pv[e], m = mv[e], v = vv[e];
-            if (adam_element(p, m, v, g, d.beta1, d.beta2, d.eps, d.weight_decay, d.lr[net], d.bc1[net], d.bc2[net])) {
-                if (d.clamp > 0.0f) p = fminf(fmaxf(p, -d.clamp), d.clamp);
-                d.m[net][i] = m;
-                d.v[net][i] = v;
-                d.p[net][i] = p;
-            } else {
-                ++bad;
-            }
-            if (d.target[net] != nullptr) {
-                const float pk = d.polyak[net];
-                d.target[net][i] = (1.0f - pk) * d.target[net][i] + pk * p;
-            }
+        for (int k = 0; k < kMaxSrc; ++k)
+            if (k < nsrc) gsum = fmaf(r.coef[k], xs[k * kRedElems + tid], gsum);
+        const float g = s * gsum;
+        float p = pe, m = me, v = ve;
+        if (adam_element(p, m, v, g, d.beta1, d.beta2, d.eps, d.weight_decay, d.lr[net], d.bc1[net], d.bc2[net])) {
+            if (d.clamp > 0.0f) p = fminf(fmaxf(p, -d.clamp), d.clamp);
+            d.m[net][ie] = m;
+            d.v[net][ie] = v;
+            d.p[net][ie] = p;
+        } else {
+            bad = 1;
+        }
+        if (d.target[net] != nullptr) {
+            const float pk = d.polyak[net];
+            d.target[net][ie] = (1.0f - pk) * te + pk * p;
         }
     }
-    if (bad) atomicAdd(d.status + OFRL_STAT_NONFINITE_GRAD, bad);
+    bad = __syncthreads_count(bad);
+    if (bad && tid == 0) atomicAdd(d.status + OFRL_STAT_NONFINITE_GRAD, bad);
     if (!ok && tid == 0) atomicAdd(d.status + OFRL_STAT_TIMEOUT, 1);
 }
 
