@@ -7,6 +7,10 @@
  * ----------------------------------------
  *  - Pointers named in a comment as "device" are CUDA device pointers
  *    (or managed memory) on the current device; the caller owns every buffer.
+ *    ofrl_train_step's q, loss_out and norms_out may also point into
+ *    page-locked host memory (cudaHostAlloc / cudaHostRegister): the kernels
+ *    then read Q and write the loss and norms in place over the host link
+ *    (NVLink-C2C on Grace-Blackwell) instead of copies on the stream.
  *    The context owns only its workspace (gradient partials, reduction
  *    scratch, the status word), sized once at ofrl_create.  No call after
  *    ofrl_create allocates.
@@ -389,6 +393,27 @@ ofrl_status ofrl_step_graph_create(ofrl_ctx* ctx, const ofrl_replay* replay, con
 ofrl_status ofrl_step_graph_launch(ofrl_step_graph* graph, uint64_t step, const float* q,
                                    const float* const* aux_src, void* stream);
 ofrl_status ofrl_step_graph_destroy(ofrl_step_graph* graph);
+
+/* The step graph with its host I/O inside (no counterpart on the pages): as
+ * ofrl_step_graph_create, plus a copy of q_host (pinned host [B, A]) into
+ * the device q before the kernels and copies of loss_out and norms_out into
+ * loss_host ([n_nets]) and norms_host ([n_nets, 5]) after them, as nodes of
+ * the graph; any of the three may be NULL (no copy).  Host buffers must be
+ * page-locked (cudaHostAlloc / cudaHostRegister).  ofrl_step_graph_launch_io
+ * replays it as step `step` with this step's host buffers (NULL keeps the
+ * previous one): one graph launch does the copy-in, the step and the
+ * copy-out.  The results are in the host buffers once `stream` has reached
+ * the launch (synchronise or wait on an event).  ofrl_step_graph_destroy
+ * releases it. */
+ofrl_status ofrl_step_graph_create_io(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl_her_cfg* her,
+                                      const ofrl_batch* batch, float* q, ofrl_vnet* nets, int32_t n_nets,
+                                      const ofrl_opt* opt, const float* const* aux_src, int32_t n_aux,
+                                      float* v_out, float* pi_out, int32_t* argmax_out, float* loss_out,
+                                      float* norms_out, float* grad_out, const float* q_host, float* loss_host,
+                                      float* norms_host, ofrl_step_graph** out);
+ofrl_status ofrl_step_graph_launch_io(ofrl_step_graph* graph, uint64_t step, const float* q_host,
+                                      const float* const* aux_src, float* loss_host, float* norms_host,
+                                      void* stream);
 
 /* ---- allocation-free variant (no counterpart in the method's pages) ---- */
 

@@ -35,15 +35,28 @@ def n_params(state_dim: int, hidden: int) -> int:
     return hidden * state_dim + hidden + hidden * hidden + hidden + hidden + 1
 
 
-def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
+def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor", host_ok=False):
+    """Address of a CUDA tensor; with host_ok also of a pinned CPU tensor (page-locked host memory the
+    kernels read or write in place over the host link)."""
     if t is None:
         return None
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise TypeError(f"{name} must be a CUDA tensor")
+    if not isinstance(t, torch.Tensor) or not (t.is_cuda or (host_ok and t.is_pinned())):
+        raise TypeError(f"{name} must be a CUDA tensor" + (" or a pinned CPU tensor" if host_ok else ""))
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    return C.c_void_p(t.data_ptr())
+
+
+def _host_ptr(t: Optional[torch.Tensor], name="tensor"):
+    """A page-locked float32 CPU tensor (the graph's host copies need pinned memory)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_pinned():
+        raise TypeError(f"{name} must be a pinned CPU tensor")
+    if t.dtype != F32 or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous float32 tensor")
     return C.c_void_p(t.data_ptr())
 
 
@@ -327,10 +340,10 @@ def train_step(ctx: Context, replay: Replay, her: HerConfig, step: int, batch: B
         flat = [_ptr(t, F32, "aux").value for per in aux for t in per]
         aux_arr = (C.c_void_p * len(flat))(*flat)
     _abi.check("ofrl_train_step", ctx._lib.ofrl_train_step(
-        ctx.handle, C.byref(r), C.byref(h), step, C.byref(b), _ptr(q, F32, "q"), cn, n_nets, C.byref(o),
+        ctx.handle, C.byref(r), C.byref(h), step, C.byref(b), _ptr(q, F32, "q", host_ok=True), cn, n_nets, C.byref(o),
         aux_arr, n_aux, _ptr(v_out, F32, "v_out"), _ptr(pi_out, F32, "pi_out"),
-        _ptr(argmax_out, I32, "argmax_out"), _ptr(loss_out, F32, "loss_out"),
-        _ptr(norms_out, F32, "norms_out"), _ptr(grad_out, F32, "grad_out"), _stream(stream)))
+        _ptr(argmax_out, I32, "argmax_out"), _ptr(loss_out, F32, "loss_out", host_ok=True),
+        _ptr(norms_out, F32, "norms_out", host_ok=True), _ptr(grad_out, F32, "grad_out"), _stream(stream)))
     for k in range(n_nets):
         nets[k].t = cn[k].t
 
@@ -353,8 +366,8 @@ class StepPlan:
         self.cn = (_abi.VNet * self.n_nets)(*[x.c() for x in nets])
         self.n_aux = n_aux
         self.aux_arr = (C.c_void_p * max(1, self.n_nets * n_aux))()
-        self.outs = [_ptr(v_out, F32), _ptr(pi_out, F32), _ptr(argmax_out, I32), _ptr(loss_out, F32),
-                     _ptr(norms_out, F32), _ptr(grad_out, F32)]
+        self.outs = [_ptr(v_out, F32), _ptr(pi_out, F32), _ptr(argmax_out, I32), _ptr(loss_out, F32, host_ok=True),
+                     _ptr(norms_out, F32, host_ok=True), _ptr(grad_out, F32)]
         self.fn = ctx._lib.ofrl_train_step
         self.rp, self.hp, self.bp, self.op = C.byref(self.r), C.byref(self.h), C.byref(self.b), C.byref(self.o)
 
@@ -372,6 +385,11 @@ class StepPlan:
     def sync_t(self):
         for k in range(self.n_nets):
             self.nets[k].t = self.cn[k].t
+
+    def reload_t(self):
+        """Take each network's t from the VNet objects (after steps made by other means, e.g. a StepGraph)."""
+        for k in range(self.n_nets):
+            self.cn[k].t = self.nets[k].t
 
     def kernels(self) -> int:
         """Kernel launches one run() makes (4, or 3 when the reduce and Adam run as one launch)."""
@@ -395,9 +413,13 @@ class StepGraph:
     """
 
     def __init__(self, ctx: Context, replay: Replay, her: HerConfig, batch: Batch, nets: List[VNet], opt: Opt, q,
-                 aux=None, v_out=None, pi_out=None, argmax_out=None, loss_out=None, norms_out=None, grad_out=None):
+                 aux=None, v_out=None, pi_out=None, argmax_out=None, loss_out=None, norms_out=None, grad_out=None,
+                 q_host=None, loss_host=None, norms_host=None):
+        """q_host / loss_host / norms_host (pinned CPU tensors): the graph also copies Q in from q_host and the
+        loss and norms out to loss_host / norms_host; replay it with launch_io."""
         self.ctx, self.nets = ctx, nets
-        self._keep = [replay, batch, nets, q, aux, v_out, pi_out, argmax_out, loss_out, norms_out, grad_out]
+        self._keep = [replay, batch, nets, q, aux, v_out, pi_out, argmax_out, loss_out, norms_out, grad_out,
+                      q_host, loss_host, norms_host]
         self.r, self.h, self.b, self.o = replay.c(), her.c(), batch.c(), opt.c()
         self.n_nets = len(nets)
         self.cn = (_abi.VNet * self.n_nets)(*[x.c() for x in nets])
@@ -407,13 +429,38 @@ class StepGraph:
             for i, t in enumerate(t for per in aux for t in per):
                 self.aux_arr[i] = _ptr(t, F32, "aux").value
         handle = C.c_void_p()
-        _abi.check("ofrl_step_graph_create", ctx._lib.ofrl_step_graph_create(
-            ctx.handle, C.byref(self.r), C.byref(self.h), C.byref(self.b), _ptr(q, F32, "q"), self.cn, self.n_nets,
-            C.byref(self.o), self.aux_arr if self.n_aux else None, self.n_aux, _ptr(v_out, F32, "v_out"),
-            _ptr(pi_out, F32, "pi_out"), _ptr(argmax_out, I32, "argmax_out"), _ptr(loss_out, F32, "loss_out"),
-            _ptr(norms_out, F32, "norms_out"), _ptr(grad_out, F32, "grad_out"), C.byref(handle)))
+        args = (ctx.handle, C.byref(self.r), C.byref(self.h), C.byref(self.b), _ptr(q, F32, "q"), self.cn,
+                self.n_nets, C.byref(self.o), self.aux_arr if self.n_aux else None, self.n_aux,
+                _ptr(v_out, F32, "v_out"), _ptr(pi_out, F32, "pi_out"), _ptr(argmax_out, I32, "argmax_out"),
+                _ptr(loss_out, F32, "loss_out"), _ptr(norms_out, F32, "norms_out"), _ptr(grad_out, F32, "grad_out"))
+        self.io = q_host is not None or loss_host is not None or norms_host is not None
+        if self.io:
+            _abi.check("ofrl_step_graph_create_io", ctx._lib.ofrl_step_graph_create_io(
+                *args, _host_ptr(q_host, "q_host"), _host_ptr(loss_host, "loss_host"),
+                _host_ptr(norms_host, "norms_host"), C.byref(handle)))
+        else:
+            _abi.check("ofrl_step_graph_create", ctx._lib.ofrl_step_graph_create(*args, C.byref(handle)))
         self.handle = handle
         self.fn = ctx._lib.ofrl_step_graph_launch
+        self.fn_io = ctx._lib.ofrl_step_graph_launch_io
+
+    def launch_io(self, step: int, q_host=None, aux=None, loss_host=None, norms_host=None, stream=None):
+        """Replay as step `step` with this step's host buffers (pinned CPU tensors; None keeps the previous)."""
+        arr = None
+        if aux is not None:
+            self._keep.append(aux)
+            for i, t in enumerate(t for per in aux for t in per):
+                self.aux_arr[i] = t.data_ptr()
+            arr = self.aux_arr
+        for t in (q_host, loss_host, norms_host):
+            if t is not None:
+                self._keep.append(t)
+        code = self.fn_io(self.handle, step, _host_ptr(q_host, "q_host"), arr, _host_ptr(loss_host, "loss_host"),
+                          _host_ptr(norms_host, "norms_host"), _stream(stream))
+        if code != _abi.OK:
+            _abi.check("ofrl_step_graph_launch_io", code)
+        if len(self._keep) > 64:
+            del self._keep[14:-8]
 
     def launch(self, step: int, q=None, aux=None, stream=None):
         arr = None
@@ -429,7 +476,7 @@ class StepGraph:
         if code != _abi.OK:
             _abi.check("ofrl_step_graph_launch", code)
         if len(self._keep) > 64:
-            del self._keep[11:-8]
+            del self._keep[14:-8]
 
     def sync_t(self):
         for k in range(self.n_nets):

@@ -77,6 +77,10 @@ SIGNATURES = {
                                            vp, C.POINTER(vp)]),
     "ofrl_step_graph_launch": (C.c_int32, [vp, C.c_uint64, vp, C.POINTER(vp), vp]),
     "ofrl_step_graph_destroy": (C.c_int32, [vp]),
+    "ofrl_step_graph_create_io": (C.c_int32, [vp, C.POINTER(Replay), C.POINTER(HerCfg), C.POINTER(Batch), vp, vp,
+                                              C.c_int32, C.POINTER(Opt), C.POINTER(vp), C.c_int32, vp, vp, vp, vp,
+                                              vp, vp, vp, vp, vp, C.POINTER(vp)]),
+    "ofrl_step_graph_launch_io": (C.c_int32, [vp, C.c_uint64, vp, C.POINTER(vp), vp, vp, vp]),
     "ofrl_noalloc_max_batch": (C.c_int64, [C.POINTER(VShape)]),
     "ofrl_iql_value_fwd_bwd_noalloc": (C.c_int32, [C.POINTER(VShape), vp, vp, C.c_int32, C.c_int32, vp, C.c_float,
                                                    vp, vp, vp, vp]),

@@ -30,7 +30,14 @@ struct ofrl_step_graph {
     cudaGraph_t graph;
     cudaGraphExec_t exec;
     cudaGraphNode_t node[5];
-    int n_nodes;              // relabel, V (1 or 2 kernels), reduce + Adam (1 or 2 kernels)
+    int n_nodes;              // kernels: relabel, V (1 or 2), reduce + Adam (1 or 2)
+    // host I/O (ofrl_step_graph_create_io): Q copied in before the kernels,
+    // loss and norms copied out after them (null nodes when not asked for)
+    cudaGraphNode_t h2d_q, d2h_loss, d2h_norms;
+    void* q_dev;
+    const void* loss_dev;
+    const void* norms_dev;
+    size_t q_bytes, loss_bytes, norms_bytes;
     int red_node;             // index of the reduce node
     // the captured arguments of each node (copies patched before a replay)
     ofrl::HerLaunch her;
@@ -47,15 +54,21 @@ struct ofrl_step_graph {
 
 using namespace ofrl;
 
-extern "C" ofrl_status ofrl_step_graph_create(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl_her_cfg* her,
-                                              const ofrl_batch* batch, const float* q, ofrl_vnet* nets,
-                                              int32_t n_nets, const ofrl_opt* opt, const float* const* aux_src,
-                                              int32_t n_aux, float* v_out, float* pi_out, int32_t* argmax_out,
-                                              float* loss_out, float* norms_out, float* grad_out,
-                                              ofrl_step_graph** out) {
+namespace {
+
+ofrl_status create_graph(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl_her_cfg* her, const ofrl_batch* batch,
+                         const float* q, ofrl_vnet* nets, int32_t n_nets, const ofrl_opt* opt,
+                         const float* const* aux_src, int32_t n_aux, float* v_out, float* pi_out,
+                         int32_t* argmax_out, float* loss_out, float* norms_out, float* grad_out,
+                         const float* q_host, float* loss_host, float* norms_host, ofrl_step_graph** out) {
     if (ctx == nullptr || out == nullptr || nets == nullptr || opt == nullptr) return OFRL_EINVAL;
     if (ctx->prof_events != nullptr) return OFRL_EINVAL;   // no profiling hooks inside a capture
+    if ((q_host != nullptr && q == nullptr) || (loss_host != nullptr && loss_out == nullptr) ||
+        (norms_host != nullptr && norms_out == nullptr) || her == nullptr)
+        return OFRL_EINVAL;
     *out = nullptr;
+    const size_t q_bytes = (size_t)her->batch * ctx->shape.num_actions * sizeof(float);
+    const size_t loss_bytes = (size_t)n_nets * sizeof(float), norms_bytes = (size_t)n_nets * 5 * sizeof(float);
     cudaStream_t st = nullptr;
     if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return OFRL_ECUDA;
     std::vector<int32_t> t0(n_nets > 0 ? n_nets : 0);
@@ -67,8 +80,18 @@ extern "C" ofrl_status ofrl_step_graph_create(ofrl_ctx* ctx, const ofrl_replay* 
         cudaStreamDestroy(st);
         return OFRL_ECUDA;
     }
-    const ofrl_status s = ofrl_train_step(ctx, replay, her, 0, batch, q, nets, n_nets, opt, aux_src, n_aux, v_out,
-                                          pi_out, argmax_out, loss_out, norms_out, grad_out, st);
+    cudaError_t ecp = cudaSuccess;
+    if (q_host != nullptr)
+        ecp = cudaMemcpyAsync(const_cast<float*>(q), q_host, q_bytes, cudaMemcpyHostToDevice, st);
+    ofrl_status s = ecp == cudaSuccess ? ofrl_train_step(ctx, replay, her, 0, batch, q, nets, n_nets, opt, aux_src,
+                                                         n_aux, v_out, pi_out, argmax_out, loss_out, norms_out,
+                                                         grad_out, st)
+                                       : OFRL_ECUDA;
+    if (s == OFRL_OK && loss_host != nullptr)
+        ecp = cudaMemcpyAsync(loss_host, loss_out, loss_bytes, cudaMemcpyDeviceToHost, st);
+    if (s == OFRL_OK && ecp == cudaSuccess && norms_host != nullptr)
+        ecp = cudaMemcpyAsync(norms_host, norms_out, norms_bytes, cudaMemcpyDeviceToHost, st);
+    if (s == OFRL_OK && ecp != cudaSuccess) s = OFRL_ECUDA;
     cudaGraph_t graph = nullptr;
     const cudaError_t ec = cudaStreamEndCapture(st, &graph);
     cudaStreamDestroy(st);
@@ -96,11 +119,19 @@ extern "C" ofrl_status ofrl_step_graph_create(ofrl_ctx* ctx, const ofrl_replay* 
     g->beta2 = opt->beta2;
     g->graph = graph;
     g->barrier_arrivals = per_replay;
-    // the kernel nodes, in launch order (a captured stream is a chain)
+    g->q_dev = const_cast<float*>(q);
+    g->loss_dev = loss_out;
+    g->norms_dev = norms_out;
+    g->q_bytes = q_bytes;
+    g->loss_bytes = loss_bytes;
+    g->norms_bytes = norms_bytes;
+    // the nodes in launch order (a captured stream is a chain): the Q copy,
+    // the kernels, the loss and norms copies
+    const int n_io = (q_host ? 1 : 0) + (loss_host ? 1 : 0) + (norms_host ? 1 : 0);
     size_t n = 0;
     cudaGraphGetNodes(graph, nullptr, &n);
     std::vector<cudaGraphNode_t> nodes(n);
-    bool ok = n >= 3 && n <= 5 && cudaGraphGetNodes(graph, nodes.data(), &n) == cudaSuccess;
+    bool ok = (int)n >= 3 + n_io && (int)n <= 5 + n_io && cudaGraphGetNodes(graph, nodes.data(), &n) == cudaSuccess;
     // order by the chain: the node without dependencies first (the queries
     // take edge data: programmatic-launch edges carry it)
     std::vector<cudaGraphNode_t> chain;
@@ -123,10 +154,23 @@ extern "C" ofrl_status ofrl_step_graph_create(ofrl_ctx* ctx, const ofrl_replay* 
         }
         ok = ok && chain.size() == n;
     }
-    for (size_t i = 0; ok && i < n; ++i) {
-        cudaGraphNodeType ty;
-        ok = cudaGraphNodeGetType(chain[i], &ty) == cudaSuccess && ty == cudaGraphNodeTypeKernel;
-        g->node[i] = chain[i];
+    {
+        size_t i = 0;
+        if (ok && q_host != nullptr) g->h2d_q = chain[i++];
+        const size_t kend = n - (loss_host ? 1 : 0) - (norms_host ? 1 : 0);
+        int nk = 0;
+        for (; ok && i < kend; ++i) {
+            cudaGraphNodeType ty;
+            ok = cudaGraphNodeGetType(chain[i], &ty) == cudaSuccess && ty == cudaGraphNodeTypeKernel;
+            g->node[nk++] = chain[i];
+        }
+        if (ok && loss_host != nullptr) g->d2h_loss = chain[i++];
+        if (ok && norms_host != nullptr) g->d2h_norms = chain[i++];
+        for (cudaGraphNode_t io : {g->h2d_q, g->d2h_loss, g->d2h_norms}) {
+            cudaGraphNodeType ty;
+            if (ok && io != nullptr) ok = cudaGraphNodeGetType(io, &ty) == cudaSuccess && ty == cudaGraphNodeTypeMemcpy;
+        }
+        n = (size_t)nk;
     }
     g->n_nodes = (int)n;
     if (ok) {
@@ -173,8 +217,6 @@ extern "C" ofrl_status ofrl_step_graph_create(ofrl_ctx* ctx, const ofrl_replay* 
     return OFRL_OK;
 }
 
-namespace {
-
 cudaError_t set_args(ofrl_step_graph* g, int i, void** args) {
     cudaKernelNodeParams p;
     cudaError_t e = cudaGraphKernelNodeGetParams(g->node[i], &p);
@@ -184,10 +226,8 @@ cudaError_t set_args(ofrl_step_graph* g, int i, void** args) {
     return cudaGraphExecKernelNodeSetParams(g->exec, g->node[i], &p);
 }
 
-}  // namespace
-
-extern "C" ofrl_status ofrl_step_graph_launch(ofrl_step_graph* g, uint64_t step, const float* q,
-                                              const float* const* aux_src, void* stream) {
+ofrl_status launch_graph(ofrl_step_graph* g, uint64_t step, const float* q, const float* const* aux_src,
+                         const float* q_host, float* loss_host, float* norms_host, void* stream) {
     if (g == nullptr || step >= (1ull << 32)) return OFRL_EINVAL;
     if (g->n_aux > 0 && aux_src != nullptr)
         for (int i = 0; i < g->n_nets * g->n_aux; ++i)
@@ -227,11 +267,54 @@ extern "C" ofrl_status ofrl_step_graph_launch(ofrl_step_graph* g, uint64_t step,
         void* a3[] = {&g->adam};
         e = set_args(g, g->red_node + 1, a3);
     }
+    // 4. host I/O: this step's host buffers
+    if (e == cudaSuccess && g->h2d_q != nullptr && q_host != nullptr)
+        e = cudaGraphExecMemcpyNodeSetParams1D(g->exec, g->h2d_q, g->q_dev, q_host, g->q_bytes,
+                                               cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && g->d2h_loss != nullptr && loss_host != nullptr)
+        e = cudaGraphExecMemcpyNodeSetParams1D(g->exec, g->d2h_loss, loss_host, g->loss_dev, g->loss_bytes,
+                                               cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && g->d2h_norms != nullptr && norms_host != nullptr)
+        e = cudaGraphExecMemcpyNodeSetParams1D(g->exec, g->d2h_norms, norms_host, g->norms_dev, g->norms_bytes,
+                                               cudaMemcpyDeviceToHost);
     if (e == cudaSuccess) e = cudaGraphLaunch(g->exec, st);
     if (e != cudaSuccess) return OFRL_ECUDA;
     g->ctx->barrier_arrivals += g->barrier_arrivals;
     for (int k = 0; k < g->n_nets; ++k) g->nets[k].t += 1;
     return OFRL_OK;
+}
+
+}  // namespace
+
+extern "C" ofrl_status ofrl_step_graph_create(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl_her_cfg* her,
+                                              const ofrl_batch* batch, const float* q, ofrl_vnet* nets,
+                                              int32_t n_nets, const ofrl_opt* opt, const float* const* aux_src,
+                                              int32_t n_aux, float* v_out, float* pi_out, int32_t* argmax_out,
+                                              float* loss_out, float* norms_out, float* grad_out,
+                                              ofrl_step_graph** out) {
+    return create_graph(ctx, replay, her, batch, q, nets, n_nets, opt, aux_src, n_aux, v_out, pi_out, argmax_out,
+                        loss_out, norms_out, grad_out, nullptr, nullptr, nullptr, out);
+}
+
+extern "C" ofrl_status ofrl_step_graph_create_io(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl_her_cfg* her,
+                                                 const ofrl_batch* batch, float* q, ofrl_vnet* nets, int32_t n_nets,
+                                                 const ofrl_opt* opt, const float* const* aux_src, int32_t n_aux,
+                                                 float* v_out, float* pi_out, int32_t* argmax_out, float* loss_out,
+                                                 float* norms_out, float* grad_out, const float* q_host,
+                                                 float* loss_host, float* norms_host, ofrl_step_graph** out) {
+    return create_graph(ctx, replay, her, batch, q, nets, n_nets, opt, aux_src, n_aux, v_out, pi_out, argmax_out,
+                        loss_out, norms_out, grad_out, q_host, loss_host, norms_host, out);
+}
+
+extern "C" ofrl_status ofrl_step_graph_launch(ofrl_step_graph* g, uint64_t step, const float* q,
+                                              const float* const* aux_src, void* stream) {
+    return launch_graph(g, step, q, aux_src, nullptr, nullptr, nullptr, stream);
+}
+
+extern "C" ofrl_status ofrl_step_graph_launch_io(ofrl_step_graph* g, uint64_t step, const float* q_host,
+                                                 const float* const* aux_src, float* loss_host, float* norms_host,
+                                                 void* stream) {
+    return launch_graph(g, step, nullptr, aux_src, q_host, loss_host, norms_host, stream);
 }
 
 extern "C" ofrl_status ofrl_step_graph_destroy(ofrl_step_graph* g) {

@@ -110,7 +110,8 @@ def argmax_ok(gpu_am, q, v_ref, beta, margin=1e-3):
 class GpuStep:
     """The fused train step of one workload on the GPU, through the C ABI."""
 
-    def __init__(self, w, weight_clamp_max_abs=0.0, sanitize_sources=False, polyak=None, graph=False, path=None):
+    def __init__(self, w, weight_clamp_max_abs=0.0, sanitize_sources=False, polyak=None, graph=False, path=None,
+                 host_io=False):
         import offline_rl_step_gb300 as ofrl
         self.ofrl = ofrl
         self.w = w
@@ -133,15 +134,37 @@ class GpuStep:
         self.v = torch.empty(n, b, device="cuda")
         self.pi = torch.empty(n, b, a, device="cuda")
         self.am = torch.empty(n, b, dtype=torch.int32, device="cuda")
-        self.loss = torch.empty(n, device="cuda")
-        self.norms = torch.empty(n, 5, device="cuda")
+        # host_io: Q read in place from pinned host memory, loss and norms
+        # written in place into pinned host memory by the kernels
+        self.host_io = host_io
+        self.loss = torch.empty(n, pin_memory=True) if host_io else torch.empty(n, device="cuda")
+        self.norms = torch.empty(n, 5, pin_memory=True) if host_io else torch.empty(n, 5, device="cuda")
         self.grad = torch.empty(n, p, device="cuda")
         self.use_graph = graph
         self.sg = None
 
     def step(self, k, q, aux=None):
         aux_dev = None if aux is None else [[dev(a) for a in per] for per in aux]
-        qd = dev(q)
+        if self.use_graph == "io":
+            # the graph with its host I/O: Q copied in from pinned host memory,
+            # loss and norms copied out to pinned host memory, one launch
+            qh = torch.from_numpy(np.ascontiguousarray(q)).pin_memory()
+            if self.sg is None:
+                self.qd = torch.empty(qh.shape, device="cuda")
+                self.loss_h = torch.empty(self.w.n_nets, pin_memory=True)
+                self.norms_h = torch.empty(self.w.n_nets, 5, pin_memory=True)
+                self.sg = self.ofrl.StepGraph(self.ctx, self.replay, self.her, self.batch, self.nets, self.opt,
+                                              self.qd, aux=aux_dev, v_out=self.v, pi_out=self.pi, argmax_out=self.am,
+                                              loss_out=self.loss, norms_out=self.norms, grad_out=self.grad,
+                                              q_host=qh, loss_host=self.loss_h, norms_host=self.norms_h)
+            self.sg.launch_io(k, qh, aux_dev, self.loss_h, self.norms_h)
+            torch.cuda.synchronize()
+            self.sg.sync_t()
+            # the host copies are the device results, bit for bit
+            assert np.array_equal(self.loss_h.numpy(), self.loss.cpu().numpy())
+            assert np.array_equal(self.norms_h.numpy(), self.norms.cpu().numpy())
+            return self._results()
+        qd = torch.from_numpy(np.ascontiguousarray(q)).pin_memory() if self.host_io else dev(q)
         if self.use_graph:
             # the step as a replayed CUDA graph (captured at the first step)
             if self.sg is None:
@@ -156,6 +179,9 @@ class GpuStep:
                                  aux=aux_dev, v_out=self.v, pi_out=self.pi, argmax_out=self.am,
                                  loss_out=self.loss, norms_out=self.norms, grad_out=self.grad)
             torch.cuda.synchronize()
+        return self._results()
+
+    def _results(self):
         cpu = lambda t: t.cpu().numpy()
         return dict(batch={k2: cpu(getattr(self.batch, k2)) for k2 in
                            ("states", "next_states", "actions", "rewards", "dones", "src_idx", "donor_idx")},

@@ -131,9 +131,9 @@ def _check_step(w, k, got, ref, flagged, nets, p_before, gpu_before, q, strict=F
 
 
 @pytest.mark.parametrize("w", synth.ALL, ids=lambda w: w.name)
-def test_train_step_matches_oracle(w, graph=False, path=None):
+def test_train_step_matches_oracle(w, graph=False, path=None, host_io=False):
     need_gpu()
-    g = GpuStep(w, graph=graph, path=path)
+    g = GpuStep(w, graph=graph, path=path, host_io=host_io)
     cfg = oracle_cfg(w)
     rep = replay_np(w)
     nets = oracle_nets(w)
@@ -299,3 +299,22 @@ def test_step_graph_matches_oracle(w):
     # the same steps replayed from one captured CUDA graph: the step index,
     # Q and the auxiliary sources change per replay, t advances
     test_train_step_matches_oracle(w, graph=True)
+
+
+@pytest.mark.parametrize("w", [dataclasses.replace(synth.PROD, steps=4),
+                               dataclasses.replace(synth.BUDGETED, batch=1000, capacity=1 << 14, steps=3)],
+                         ids=["prod_graph_io", "budgeted_graph_io"])
+def test_step_graph_host_io_matches_oracle(w):
+    # the graph with its host I/O: each replay copies a fresh pinned host Q in
+    # and the loss and norms out (equal to the device results bit for bit)
+    test_train_step_matches_oracle(w, graph="io")
+
+
+@pytest.mark.parametrize("w", [dataclasses.replace(synth.PROD, steps=4),
+                               dataclasses.replace(synth.BUDGETED, batch=1000, capacity=1 << 14, steps=3),
+                               dataclasses.replace(synth.TINY, steps=3)],
+                         ids=["prod_host_buffers", "budgeted_host_buffers", "tiny_host_buffers"])
+def test_train_step_with_host_buffers_matches_oracle(w):
+    # Q read in place from pinned host memory, loss and norms written in
+    # place into pinned host memory by the kernels
+    test_train_step_matches_oracle(w, host_io=True)
