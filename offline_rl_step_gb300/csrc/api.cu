@@ -230,10 +230,10 @@ cudaError_t launch_vnet(ofrl_ctx* ctx, const VnetLaunch& v, bool packed, cudaStr
 }
 
 // Gradient partials per network that launch_vnet leaves for n_tiles tiles:
-// one per tile from the CUDA-core kernel, one per cluster of tiles from the
-// fused tensor-core kernel, one per K-range from the layered one.
+// one per tile from the CUDA-core kernel, one per CTA from the fused
+// tensor-core kernel, one per K-range from the layered one.
 int vnet_parts(const VnetLaunch& v, int n_tiles) {
-    if (v.path == PATH_FUSED) return n_tiles / vnet_tc_cluster(n_tiles);
+    if (v.path == PATH_FUSED) return vnet_tc_ctas(n_tiles, v.n_nets);
     if (v.path == PATH_LAYERED) return v.n_ranges;
     return n_tiles;
 }

@@ -231,27 +231,6 @@ inline cudaError_t launch_ex(void (*kernel)(Params...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// launch_pdl with thread-block clusters of `cluster` CTAs along x.
-template <typename Arg0, typename Arg1>
-inline cudaError_t launch_pdl_cluster(void (*kernel)(Arg0, Arg1), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                                      unsigned cluster, Arg0 a0, Arg1 a1) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = cluster;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kernel, a0, a1);
-}
-
 inline int64_t n_params_of(int s, int h) {
     return (int64_t)h * s + h + (int64_t)h * h + h + h + 1;
 }
@@ -356,7 +335,6 @@ struct VnetLaunch {
     int64_t net_partial_stride;  // floats between networks in partials
     int32_t net_tile_stride;     // floats between networks in tile_loss
     int32_t* status;
-    int32_t cluster;             // tensor-core kernel: tiles per partial (set by its launcher)
     int32_t path;                // VnetPath chosen for this launch (never PATH_AUTO)
     // layered tensor-core path
     uint8_t* act[3];             // h1, dz2, dz1 images [n_nets][act_tiles][planes][128 x H]
@@ -392,11 +370,10 @@ cudaError_t vnet_wide_maps(WideMaps* m, int hidden, int planes, int n_nets, int 
 int vnet_wide_ranges(const VnetLaunch& a, int num_sms);  // partials per network the weight-gradient kernel writes
 cudaError_t launch_vnet_wide_pack(const VnetLaunch& a, uint8_t* wimg, uint8_t* ximg, cudaStream_t st);
 cudaError_t launch_vnet_wide(const VnetLaunch& a, const uint8_t* wimg, cudaStream_t st);
-// Tiles whose gradient partials the tensor-core kernel sums into one (a
-// thread-block cluster): the smallest of 1, 2, 4 that divides n_tiles, that
-// the device can schedule and that leaves at most 128 partials (else the
-// largest).  Its partials count is n_tiles / that.
-int vnet_tc_cluster(int n_tiles);
+// CTAs per network of the fused tensor-core kernel (its gradient partials
+// per network): one wave of one CTA per SM, each CTA running an equal share
+// of the n_tiles tiles back to back.
+int vnet_tc_ctas(int n_tiles, int n_nets);
 
 struct ReduceLaunch {
     int n_nets;

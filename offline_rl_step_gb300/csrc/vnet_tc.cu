@@ -71,14 +71,16 @@ __device__ __forceinline__ uint64_t desc_mn(const uint8_t* plane, int C, int ks)
 }
 
 // Issue one GEMM (all K-steps, all split terms) from one thread.
+// accumulate: add to what D holds (else the first product overwrites it).
 template <int NP>
 __device__ __forceinline__ void gemm(uint32_t d_tmem, const uint8_t* a, uint32_t a_plane, int a_cols, bool a_mn,
-                                     const uint8_t* b, uint32_t b_plane, int b_cols, bool b_mn, int ksteps, int n) {
+                                     const uint8_t* b, uint32_t b_plane, int b_cols, bool b_mn, int ksteps, int n,
+                                     bool accumulate = false) {
     const uint32_t idesc = umma::instr_desc(umma::kTypeBF16, a_mn, b_mn, TM, n);
     constexpr int nt = NP == 3 ? 6 : 1;
     constexpr int ta[6] = {2, 1, 0, 1, 0, 0};   // smallest products first
     constexpr int tb[6] = {0, 1, 2, 0, 1, 0};
-    uint32_t acc = 0;
+    uint32_t acc = accumulate ? 1u : 0u;
     for (int ks = 0; ks < ksteps; ++ks) {
 #pragma unroll
         for (int t = 0; t < nt; ++t) {
@@ -126,21 +128,6 @@ __device__ __forceinline__ void build_x(uint8_t* img, int np, const float* __res
     }
 }
 
-// Sum, in rank order, of the value at shared address p in CTAs 0..cn-1 of
-// the cluster (cn <= 8); the loads are all issued before the adds.
-__device__ __forceinline__ float cluster_sum1(const float* p, int cn) {
-    const uint32_t a = umma::smem_u32(p);
-    float v[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        if (k < cn) v[k] = umma::ld_cluster1(umma::cluster_map(a, (uint32_t)k));
-    float s = v[0];
-#pragma unroll
-    for (int k = 1; k < 8; ++k)
-        if (k < cn) s += v[k];
-    return s;
-}
-
 struct TcSmem {
     uint8_t r0[kRegion];
     uint8_t r1[kRegion];
@@ -148,11 +135,11 @@ struct TcSmem {
     float vsum[4][TM];
     float red[3][kEpiWarps][32];   // per epilogue warp column sums: dW3, db2, db1
     float lred[2][4];           // per lane-quarter warp of column group 0: loss, db3
-    __align__(16) float vec[3][HH];   // this tile's dW3, db2, db1
+    __align__(16) float vec[3][HH];   // this CTA's dW3, db2, db1 over its tiles
     float qt[TM * kMaxActions];       // the tile's Q rows [row][action] (or q_taken [row])
     int32_t act[TM];                  // the tile's actions
     float vrow[TM];                   // V of each row
-    float vb3;                  // this tile's db3
+    float vb3;                  // this CTA's db3 over its tiles
     uint64_t bar_mma, bar_load;
     uint32_t tmem_slot;
 };
@@ -167,16 +154,15 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     const int ew = warp - 1, et = tid - 32;     // epilogue warp / thread index
     const int q = warp & 3, cg = (warp - 1) >> 2;   // TMEM lane quarter, column group (32 columns)
     const int row = 32 * q + lane;              // tile row / accumulator lane of this thread
-    const int tile = blockIdx.x, net = blockIdx.y;
+    const int net = blockIdx.y;
     const int S = a.state_dim, B = a.batch, NA = a.num_actions;
-    const int row0 = tile * TM;
+    const int n_tiles = (B + TM - 1) / TM;
     const int Hn = a.hidden;   // 64 or 128: the weights are zero-padded to 128 units
     const Offsets off = offsets_of(S, Hn);
     const float* __restrict__ prm = a.params[net];
     const float tau = a.tau[net];
     const uint8_t* w1i = wimg + (int64_t)net * tc::weight_image_bytes();
     const uint8_t* w2i = w1i + tc::w2_image_offset();
-    const uint8_t* xi = a.ximg != nullptr ? a.ximg + (int64_t)tile * NP * kPlaneX : nullptr;
     constexpr uint32_t kXBytes = (uint32_t)NP * kPlaneX, kW2Bytes = (uint32_t)NP * kPlaneH;
 
     if (tid == 0) {
@@ -187,36 +173,16 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     if (warp == 0) umma::tmem_alloc(&sm.tmem_slot, kTmemCols);
     pdl_trigger();
     pdl_wait();
-    // ---- stage 1: X image -> R0, W1 image -> R1 (issued first; the loads
-    // below overlap it) ----
-    if (tid == 0) {
-        umma::mbar_expect_tx(&sm.bar_load, (xi ? kXBytes : 0u) + kXBytes);
-        if (xi) umma::bulk_g2s(sm.r0, xi, kXBytes, &sm.bar_load);
-        umma::bulk_g2s(sm.r1, w1i, kXBytes, &sm.bar_load);
-    }
     for (int i = tid; i < HH; i += kThreads) {
         const bool u = i < Hn;   // padded units: zero bias and output weight, so they stay zero
         sm.b1[i] = u ? __ldg(prm + off.b1 + i) : 0.0f;
         sm.b2[i] = u ? __ldg(prm + off.b2 + i) : 0.0f;
         sm.w3[i] = u ? __ldg(prm + off.w3 + i) : 0.0f;
+        sm.vec[0][i] = sm.vec[1][i] = sm.vec[2][i] = 0.0f;
     }
+    if (tid == 0) sm.vb3 = 0.0f;
     const float b3 = __ldg(prm + off.b3);
-    // the tile's actions and Q rows (one contiguous block) for the loss and
-    // the policy, read long before they are needed
-    {
-        const int nrow = B - row0 < TM ? B - row0 : TM;
-        if (a.q != nullptr) {
-            for (int e = tid; e < nrow * NA; e += kThreads) sm.qt[e] = __ldg(a.q + (int64_t)row0 * NA + e);
-            for (int e = tid; e < nrow; e += kThreads) sm.act[e] = __ldg(a.actions + row0 + e);
-        } else {
-            for (int e = tid; e < nrow; e += kThreads) sm.qt[e] = __ldg(a.q_taken + row0 + e);
-        }
-    }
-    umma::fence_before_sync();
-    __syncthreads();
-    umma::fence_after_sync();
-    const uint32_t tmem = sm.tmem_slot;
-    const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);   // this warp's lane quarter
+    uint32_t tmem = 0, tq = 0;
     uint32_t ph_mma = 0, ph_load = 0;
     bool ok = true;
     auto wait_mma = [&]() {
@@ -229,266 +195,297 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         ph_load ^= 1u;
     };
 
-    if (!xi) build_x(sm.r0, NP, a.states, a.stride, row0, B, S);
-    umma::fence_smem_to_async();
-    __syncthreads();
-    wait_load();
-    // ---- G1: z1 = X . W1^T ----
-    if (tid == 0) {
+    // Tiles blockIdx.x, blockIdx.x + gridDim.x, ...: the weight-gradient
+    // accumulators (dW2, dW1 in TMEM; dW3, db2, db1, db3 in shared memory)
+    // run over all of them; one partial per CTA at the end.
+    for (int tile = blockIdx.x, it = 0; tile < n_tiles; tile += gridDim.x, ++it) {
+        const int row0 = tile * TM;
+        const uint8_t* xi = a.ximg != nullptr ? a.ximg + (int64_t)tile * NP * kPlaneX : nullptr;
+        // ---- stage 1: X image -> R0, W1 image -> R1 (issued first; the loads
+        // below overlap it; the previous tile's G5 has finished reading them) ----
+        if (tid == 0) {
+            umma::mbar_expect_tx(&sm.bar_load, (xi ? kXBytes : 0u) + kXBytes);
+            if (xi) umma::bulk_g2s(sm.r0, xi, kXBytes, &sm.bar_load);
+            umma::bulk_g2s(sm.r1, w1i, kXBytes, &sm.bar_load);
+        }
+        // the tile's actions and Q rows (one contiguous block) for the loss and
+        // the policy, read long before they are needed
+        {
+            const int nrow = B - row0 < TM ? B - row0 : TM;
+            if (a.q != nullptr) {
+                for (int e = tid; e < nrow * NA; e += kThreads) sm.qt[e] = __ldg(a.q + (int64_t)row0 * NA + e);
+                for (int e = tid; e < nrow; e += kThreads) sm.act[e] = __ldg(a.actions + row0 + e);
+            } else {
+                for (int e = tid; e < nrow; e += kThreads) sm.qt[e] = __ldg(a.q_taken + row0 + e);
+            }
+        }
+        umma::fence_before_sync();
+        __syncthreads();
         umma::fence_after_sync();
-        gemm<NP>(tmem + TM_Z1, sm.r0, kPlaneX, KX, false, sm.r1, kPlaneX, KX, false, KX / 16, HH);
-        umma::commit(&sm.bar_mma);
-    }
-    wait_mma();
-    // W1 is no longer read: the W2 image streams into R1 during epilogue 1
-    if (tid == 0) {
-        umma::mbar_expect_tx(&sm.bar_load, kW2Bytes);
-        umma::bulk_g2s(sm.r1, w2i, kW2Bytes, &sm.bar_load);
-    }
+        tmem = sm.tmem_slot;
+        tq = tmem + ((uint32_t)(32 * q) << 16);   // this warp's lane quarter
 
-    // ---- epilogue 1: h1 = relu(z1 + b1) -> R0; ReLU mask bits kept ----
-    uint32_t mask1 = 0;
-    if (epi) {
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            const int c0 = cg * 32 + cc * 16;
-            float v[16];
-            umma::tmem_ld16(tq + TM_Z1 + (uint32_t)c0, v);
-            umma::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float z = v[j] + sm.b1[c0 + j];
-                v[j] = z < 0.0f ? 0.0f : z;
-                if (v[j] > 0.0f) mask1 |= 1u << (cc * 16 + j);
-            }
-            store16<NP>(sm.r0, row, c0, v);
+        if (!xi) build_x(sm.r0, NP, a.states, a.stride, row0, B, S);
+        umma::fence_smem_to_async();
+        __syncthreads();
+        wait_load();
+        // ---- G1: z1 = X . W1^T ----
+        if (tid == 0) {
+            umma::fence_after_sync();
+            gemm<NP>(tmem + TM_Z1, sm.r0, kPlaneX, KX, false, sm.r1, kPlaneX, KX, false, KX / 16, HH);
+            umma::commit(&sm.bar_mma);
         }
-    }
-    umma::fence_smem_to_async();
-    umma::fence_before_sync();
-    __syncthreads();
-    wait_load();
-    // ---- G2: z2 = h1 . W2^T ----
-    if (tid == 0) {
-        umma::fence_after_sync();
-        gemm<NP>(tmem + TM_Z2, sm.r0, kPlaneH, HH, false, sm.r1, kPlaneH, HH, false, HH / 16, HH);
-        umma::commit(&sm.bar_mma);
-    }
-    wait_mma();
+        wait_mma();
+        // W1 is no longer read: the W2 image streams into R1 during epilogue 1
+        if (tid == 0) {
+            umma::mbar_expect_tx(&sm.bar_load, kW2Bytes);
+            umma::bulk_g2s(sm.r1, w2i, kW2Bytes, &sm.bar_load);
+        }
 
-    // ---- epilogue 2: V, loss, dV, policy, dz2 -> R1, dW3 / db2 / db3 ----
-    // z2 is read from TMEM twice (for V, then for dz2) instead of being kept
-    // in registers across the row reduction.
-    if (epi) {
-        float vp = 0.0f;
+        // ---- epilogue 1: h1 = relu(z1 + b1) -> R0; ReLU mask bits kept ----
+        uint32_t mask1 = 0;
+        if (epi) {
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            const int c0 = cg * 32 + cc * 16;
-            float v[16];
-            umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, v);
-            umma::tmem_ld_wait();
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c0 = cg * 32 + cc * 16;
+                float v[16];
+                umma::tmem_ld16(tq + TM_Z1 + (uint32_t)c0, v);
+                umma::tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float z = v[j] + sm.b2[c0 + j];
-                vp = fmaf(z < 0.0f ? 0.0f : z, sm.w3[c0 + j], vp);
+                for (int j = 0; j < 16; ++j) {
+                    const float z = v[j] + sm.b1[c0 + j];
+                    v[j] = z < 0.0f ? 0.0f : z;
+                    if (v[j] > 0.0f) mask1 |= 1u << (cc * 16 + j);
+                }
+                store16<NP>(sm.r0, row, c0, v);
             }
         }
-        sm.vsum[cg][row] = vp;
-    }
-    __syncthreads();
-    const float V = ((sm.vsum[0][row] + sm.vsum[1][row]) + (sm.vsum[2][row] + sm.vsum[3][row])) + b3;
-    const int b = row0 + row;
-    float dv = 0.0f, lossp = 0.0f;
-    if (epi && b < B) {
-        float qv;
-        if (a.q != nullptr) {
-            int act = sm.act[row];
-            if (act < 0 || act >= NA) {
-                if (cg == 0) atomicAdd(a.status + OFRL_STAT_BAD_ACTION, 1);
-                act = 0;
-            }
-            qv = sm.qt[row * NA + act];
-        } else {
-            qv = sm.qt[row];
+        umma::fence_smem_to_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        wait_load();
+        // ---- G2: z2 = h1 . W2^T ----
+        if (tid == 0) {
+            umma::fence_after_sync();
+            gemm<NP>(tmem + TM_Z2, sm.r0, kPlaneH, HH, false, sm.r1, kPlaneH, HH, false, HH / 16, HH);
+            umma::commit(&sm.bar_mma);
         }
-        const float d = qv - V;
-        const float w = d >= 0.0f ? tau : 1.0f - tau;
-        lossp = w * d * d;
-        dv = (-2.0f * w * d) / (float)B;
-        if (cg == 0 && a.v_out != nullptr) a.v_out[(int64_t)net * B + b] = V;
-    }
-    if (epi && cg == 0) sm.vrow[row] = V;
-    // dz2 -> R1 (what G3 and G4 need); the column sums and the loss partial
-    // are computed while G3 runs, the policy while G4 runs
-    if (epi) {
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            const int c0 = cg * 32 + cc * 16;
-            float g[16];
-            umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, g);
-            umma::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float z = g[j] + sm.b2[c0 + j];
-                g[j] = z > 0.0f ? dv * sm.w3[c0 + j] : 0.0f;
-            }
-            store16<NP>(sm.r1, row, c0, g);
-        }
-    }
-    umma::fence_smem_to_async();
-    umma::fence_before_sync();
-    __syncthreads();
-    // ---- G3: dW2 = dz2^T . h1 ----
-    if (tid == 0) {
-        umma::fence_after_sync();
-        gemm<NP>(tmem + TM_DW2, sm.r1, kPlaneH, HH, true, sm.r0, kPlaneH, HH, true, TM / 16, HH);
-        umma::commit(&sm.bar_mma);
-    }
-    if (epi && cg == 0) {
-        const float ls = warp_sum(lossp), ds = warp_sum(dv);
-        if (lane == 0) { sm.lred[0][q] = ls; sm.lred[1][q] = ds; }
-    }
-    wait_mma();
-    // ---- stage 3: W2 image -> R0 (h1 is no longer read) ----
-    if (tid == 0) {
-        umma::mbar_expect_tx(&sm.bar_load, kW2Bytes);
-        umma::bulk_g2s(sm.r0, w2i, kW2Bytes, &sm.bar_load);
-    }
-    // column sums for dW3 and db2 while W2 arrives (no MMA runs: TMEM reads
-    // and shuffles beside a running GEMM slow both)
-    if (epi) {
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            const int c0 = cg * 32 + cc * 16;
-            float g[16], hw[16];
-            umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, g);
-            umma::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float z = g[j] + sm.b2[c0 + j];
-                g[j] = z > 0.0f ? dv * sm.w3[c0 + j] : 0.0f;
-                hw[j] = dv * (z < 0.0f ? 0.0f : z);
-            }
-            const float s3 = colsum16(hw);
-            const float s2 = colsum16(g);
-            if ((lane & 1) == 0) {
-                sm.red[0][ew][cc * 16 + ((lane >> 1) & 15)] = s3;
-                sm.red[1][ew][cc * 16 + ((lane >> 1) & 15)] = s2;
-            }
-        }
-    }
-    __syncthreads();
-    // dW3, db2, db3 and the loss partial of the tile (fixed order over warps)
-    for (int c = et; c >= 0 && c < HH; c += kThreads) {
-        const int g = c >> 5, cl = c & 31;
-        float s3 = 0.0f, s2 = 0.0f;
-        for (int qq = 0; qq < 4; ++qq) { s3 += sm.red[0][g * 4 + qq][cl]; s2 += sm.red[1][g * 4 + qq][cl]; }
-        sm.vec[0][c] = s3;
-        sm.vec[1][c] = s2;
-    }
-    if (et == 0) {
-        const float l = (sm.lred[0][0] + sm.lred[0][1]) + (sm.lred[0][2] + sm.lred[0][3]);
-        const float d3 = (sm.lred[1][0] + sm.lred[1][1]) + (sm.lred[1][2] + sm.lred[1][3]);
-        a.tile_loss[(int64_t)net * a.net_tile_stride + tile] = l;
-        sm.vb3 = d3;
-    }
-    wait_load();
-    // ---- G4: dh1 = dz2 . W2 ----
-    if (tid == 0) {
-        umma::fence_after_sync();
-        gemm<NP>(tmem + TM_Z1, sm.r1, kPlaneH, HH, false, sm.r0, kPlaneH, HH, true, HH / 16, HH);
-        umma::commit(&sm.bar_mma);
-    }
-    // the policy while G4 runs: four threads per row (lanes 4r .. 4r + 3 of
-    // a warp), each over actions j, j + 4, ...; max / argmax (lowest index on
-    // ties) and the sum of exponentials combined over the four lanes
-    if (epi && a.pi_out != nullptr) {
-        const int pr = et >> 2, j = et & 3;
-        const int pb = row0 + pr;
-        const bool prow = pb < B;
-        const float Vp = sm.vrow[pr];
-        const float* qr = sm.qt + pr * NA;
-        float zmax = -INFINITY, amax = -INFINITY;
-        int best = NA;
-        if (prow)
-            for (int k = j; k < NA; k += 4) {
-                const float adv = fminf(fmaxf(qr[k] - Vp, -10.0f), 10.0f);
-                if (adv > amax) { amax = adv; best = k; }
-                zmax = fmaxf(zmax, a.beta * adv);
-            }
-#pragma unroll
-        for (int o = 1; o < 4; o <<= 1) {
-            const float oa = __shfl_xor_sync(0xffffffffu, amax, o);
-            const int ob = __shfl_xor_sync(0xffffffffu, best, o);
-            if (oa > amax || (oa == amax && ob < best)) { amax = oa; best = ob; }
-            zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
-        }
-        float sum = 0.0f;
-        if (prow)
-            for (int k = j; k < NA; k += 4) sum += expf(a.beta * fminf(fmaxf(qr[k] - Vp, -10.0f), 10.0f) - zmax);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        if (prow) {
-            float* po = a.pi_out + ((int64_t)net * B + pb) * NA;
-            for (int k = j; k < NA; k += 4)
-                po[k] = expf(a.beta * fminf(fmaxf(qr[k] - Vp, -10.0f), 10.0f) - zmax) / sum;
-            if (j == 0 && a.argmax_out != nullptr) a.argmax_out[(int64_t)net * B + pb] = best < NA ? best : 0;
-        }
-    }
-    wait_mma();
-    // dz2 is no longer read: the X image streams into R1 during epilogue 4
-    if (tid == 0 && xi) {
-        umma::mbar_expect_tx(&sm.bar_load, kXBytes);
-        umma::bulk_g2s(sm.r1, xi, kXBytes, &sm.bar_load);
-    }
+        wait_mma();
 
-    // ---- epilogue 4: dz1 = dh1 * 1[z1 > 0] -> R0; db1 ----
-    if (epi) {
+        // ---- epilogue 2: V, loss, dV, policy, dz2 -> R1, dW3 / db2 / db3 ----
+        // z2 is read from TMEM twice (for V, then for dz2) instead of being kept
+        // in registers across the row reduction.
+        if (epi) {
+            float vp = 0.0f;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            const int c0 = cg * 32 + cc * 16;
-            float v[16];
-            umma::tmem_ld16(tq + TM_Z1 + (uint32_t)c0, v);
-            umma::tmem_ld_wait();
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c0 = cg * 32 + cc * 16;
+                float v[16];
+                umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, v);
+                umma::tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = ((mask1 >> (cc * 16 + j)) & 1u) ? v[j] : 0.0f;
-            store16<NP>(sm.r0, row, c0, v);
+                for (int j = 0; j < 16; ++j) {
+                    const float z = v[j] + sm.b2[c0 + j];
+                    vp = fmaf(z < 0.0f ? 0.0f : z, sm.w3[c0 + j], vp);
+                }
+            }
+            sm.vsum[cg][row] = vp;
         }
-    }
-    if (!xi) build_x(sm.r1, NP, a.states, a.stride, row0, B, S);
-    umma::fence_smem_to_async();
-    umma::fence_before_sync();
-    __syncthreads();
-    if (xi) wait_load();
-    // ---- G5: dW1 = dz1^T . X ----
-    if (tid == 0) {
-        umma::fence_after_sync();
-        gemm<NP>(tmem + TM_DW1, sm.r0, kPlaneH, HH, true, sm.r1, kPlaneX, KX, true, TM / 16, KX);
-        umma::commit(&sm.bar_mma);
-    }
-    // db1: with S < 64 G5 yields it in its last column (the ones column of
-    // the state-tile image); else column sums while G5 runs
-    if (epi && !tc::ones_column(KX - 1, S)) {
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            const int c0 = cg * 32 + cc * 16;
-            float v[16];
-            umma::tmem_ld16(tq + TM_Z1 + (uint32_t)c0, v);
-            umma::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = ((mask1 >> (cc * 16 + j)) & 1u) ? v[j] : 0.0f;
-            const float s1 = colsum16(v);
-            if ((lane & 1) == 0) sm.red[2][ew][cc * 16 + ((lane >> 1) & 15)] = s1;
+        __syncthreads();
+        const float V = ((sm.vsum[0][row] + sm.vsum[1][row]) + (sm.vsum[2][row] + sm.vsum[3][row])) + b3;
+        const int b = row0 + row;
+        float dv = 0.0f, lossp = 0.0f;
+        if (epi && b < B) {
+            float qv;
+            if (a.q != nullptr) {
+                int act = sm.act[row];
+                if (act < 0 || act >= NA) {
+                    if (cg == 0) atomicAdd(a.status + OFRL_STAT_BAD_ACTION, 1);
+                    act = 0;
+                }
+                qv = sm.qt[row * NA + act];
+            } else {
+                qv = sm.qt[row];
+            }
+            const float d = qv - V;
+            const float w = d >= 0.0f ? tau : 1.0f - tau;
+            lossp = w * d * d;
+            dv = (-2.0f * w * d) / (float)B;
+            if (cg == 0 && a.v_out != nullptr) a.v_out[(int64_t)net * B + b] = V;
         }
-    }
-    __syncthreads();
-    for (int c = et; c >= 0 && c < HH; c += kThreads) {
-        const int g = c >> 5, cl = c & 31;
-        float s1 = 0.0f;
-        for (int qq = 0; qq < 4; ++qq) s1 += sm.red[2][g * 4 + qq][cl];
-        if (!tc::ones_column(KX - 1, S)) sm.vec[2][c] = s1;
-    }
-    wait_mma();
+        if (epi && cg == 0) sm.vrow[row] = V;
+        // dz2 -> R1 (what G3 and G4 need); the column sums and the loss partial
+        // are computed while G3 runs, the policy while G4 runs
+        if (epi) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c0 = cg * 32 + cc * 16;
+                float g[16];
+                umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, g);
+                umma::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float z = g[j] + sm.b2[c0 + j];
+                    g[j] = z > 0.0f ? dv * sm.w3[c0 + j] : 0.0f;
+                }
+                store16<NP>(sm.r1, row, c0, g);
+            }
+        }
+        umma::fence_smem_to_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        // ---- G3: dW2 = dz2^T . h1 ----
+        if (tid == 0) {
+            umma::fence_after_sync();
+            gemm<NP>(tmem + TM_DW2, sm.r1, kPlaneH, HH, true, sm.r0, kPlaneH, HH, true, TM / 16, HH, it > 0);
+            umma::commit(&sm.bar_mma);
+        }
+        if (epi && cg == 0) {
+            const float ls = warp_sum(lossp), ds = warp_sum(dv);
+            if (lane == 0) { sm.lred[0][q] = ls; sm.lred[1][q] = ds; }
+        }
+        wait_mma();
+        // ---- stage 3: W2 image -> R0 (h1 is no longer read) ----
+        if (tid == 0) {
+            umma::mbar_expect_tx(&sm.bar_load, kW2Bytes);
+            umma::bulk_g2s(sm.r0, w2i, kW2Bytes, &sm.bar_load);
+        }
+        // column sums for dW3 and db2 while W2 arrives (no MMA runs: TMEM reads
+        // and shuffles beside a running GEMM slow both)
+        if (epi) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c0 = cg * 32 + cc * 16;
+                float g[16], hw[16];
+                umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, g);
+                umma::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float z = g[j] + sm.b2[c0 + j];
+                    g[j] = z > 0.0f ? dv * sm.w3[c0 + j] : 0.0f;
+                    hw[j] = dv * (z < 0.0f ? 0.0f : z);
+                }
+                const float s3 = colsum16(hw);
+                const float s2 = colsum16(g);
+                if ((lane & 1) == 0) {
+                    sm.red[0][ew][cc * 16 + ((lane >> 1) & 15)] = s3;
+                    sm.red[1][ew][cc * 16 + ((lane >> 1) & 15)] = s2;
+                }
+            }
+        }
+        __syncthreads();
+        // dW3, db2, db3 and the loss partial of the tile (fixed order over warps)
+        for (int c = et; c >= 0 && c < HH; c += kThreads) {
+            const int g = c >> 5, cl = c & 31;
+            float s3 = 0.0f, s2 = 0.0f;
+            for (int qq = 0; qq < 4; ++qq) { s3 += sm.red[0][g * 4 + qq][cl]; s2 += sm.red[1][g * 4 + qq][cl]; }
+            sm.vec[0][c] += s3;
+            sm.vec[1][c] += s2;
+        }
+        if (et == 0) {
+            const float l = (sm.lred[0][0] + sm.lred[0][1]) + (sm.lred[0][2] + sm.lred[0][3]);
+            const float d3 = (sm.lred[1][0] + sm.lred[1][1]) + (sm.lred[1][2] + sm.lred[1][3]);
+            a.tile_loss[(int64_t)net * a.net_tile_stride + tile] = l;
+            sm.vb3 += d3;
+        }
+        wait_load();
+        // ---- G4: dh1 = dz2 . W2 ----
+        if (tid == 0) {
+            umma::fence_after_sync();
+            gemm<NP>(tmem + TM_Z1, sm.r1, kPlaneH, HH, false, sm.r0, kPlaneH, HH, true, HH / 16, HH);
+            umma::commit(&sm.bar_mma);
+        }
+        // the policy while G4 runs: four threads per row (lanes 4r .. 4r + 3 of
+        // a warp), each over actions j, j + 4, ...; max / argmax (lowest index on
+        // ties) and the sum of exponentials combined over the four lanes
+        if (epi && a.pi_out != nullptr) {
+            const int pr = et >> 2, j = et & 3;
+            const int pb = row0 + pr;
+            const bool prow = pb < B;
+            const float Vp = sm.vrow[pr];
+            const float* qr = sm.qt + pr * NA;
+            float zmax = -INFINITY, amax = -INFINITY;
+            int best = NA;
+            if (prow)
+                for (int k = j; k < NA; k += 4) {
+                    const float adv = fminf(fmaxf(qr[k] - Vp, -10.0f), 10.0f);
+                    if (adv > amax) { amax = adv; best = k; }
+                    zmax = fmaxf(zmax, a.beta * adv);
+                }
+#pragma unroll
+            for (int o = 1; o < 4; o <<= 1) {
+                const float oa = __shfl_xor_sync(0xffffffffu, amax, o);
+                const int ob = __shfl_xor_sync(0xffffffffu, best, o);
+                if (oa > amax || (oa == amax && ob < best)) { amax = oa; best = ob; }
+                zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
+            }
+            float sum = 0.0f;
+            if (prow)
+                for (int k = j; k < NA; k += 4) sum += expf(a.beta * fminf(fmaxf(qr[k] - Vp, -10.0f), 10.0f) - zmax);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            if (prow) {
+                float* po = a.pi_out + ((int64_t)net * B + pb) * NA;
+                for (int k = j; k < NA; k += 4)
+                    po[k] = expf(a.beta * fminf(fmaxf(qr[k] - Vp, -10.0f), 10.0f) - zmax) / sum;
+                if (j == 0 && a.argmax_out != nullptr) a.argmax_out[(int64_t)net * B + pb] = best < NA ? best : 0;
+            }
+        }
+        wait_mma();
+        // dz2 is no longer read: the X image streams into R1 during epilogue 4
+        if (tid == 0 && xi) {
+            umma::mbar_expect_tx(&sm.bar_load, kXBytes);
+            umma::bulk_g2s(sm.r1, xi, kXBytes, &sm.bar_load);
+        }
+
+        // ---- epilogue 4: dz1 = dh1 * 1[z1 > 0] -> R0; db1 ----
+        if (epi) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c0 = cg * 32 + cc * 16;
+                float v[16];
+                umma::tmem_ld16(tq + TM_Z1 + (uint32_t)c0, v);
+                umma::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = ((mask1 >> (cc * 16 + j)) & 1u) ? v[j] : 0.0f;
+                store16<NP>(sm.r0, row, c0, v);
+            }
+        }
+        if (!xi) build_x(sm.r1, NP, a.states, a.stride, row0, B, S);
+        umma::fence_smem_to_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        if (xi) wait_load();
+        // ---- G5: dW1 = dz1^T . X ----
+        if (tid == 0) {
+            umma::fence_after_sync();
+            gemm<NP>(tmem + TM_DW1, sm.r0, kPlaneH, HH, true, sm.r1, kPlaneX, KX, true, TM / 16, KX, it > 0);
+            umma::commit(&sm.bar_mma);
+        }
+        // db1: with S < 64 G5 yields it in its last column (the ones column of
+        // the state-tile image); else column sums while G5 runs
+        if (epi && !tc::ones_column(KX - 1, S)) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c0 = cg * 32 + cc * 16;
+                float v[16];
+                umma::tmem_ld16(tq + TM_Z1 + (uint32_t)c0, v);
+                umma::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = ((mask1 >> (cc * 16 + j)) & 1u) ? v[j] : 0.0f;
+                const float s1 = colsum16(v);
+                if ((lane & 1) == 0) sm.red[2][ew][cc * 16 + ((lane >> 1) & 15)] = s1;
+            }
+        }
+        __syncthreads();
+        for (int c = et; c >= 0 && c < HH; c += kThreads) {
+            const int g = c >> 5, cl = c & 31;
+            float s1 = 0.0f;
+            for (int qq = 0; qq < 4; ++qq) s1 += sm.red[2][g * 4 + qq][cl];
+            if (!tc::ones_column(KX - 1, S)) sm.vec[2][c] += s1;
+        }
+        wait_mma();
+    }   // tiles
 
     // ---- dW2 (lane = output unit, 128 columns) and dW1 (lane = unit, 64 columns) ----
     // Staged in shared memory (R0, R1 are free now): dW2 rows at a padded
@@ -519,74 +516,20 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         if (c0 + 15 == KX - 1 && tc::ones_column(KX - 1, S)) sm.vec[2][row] = v[15];
     }
 
-    const int cn = a.cluster;
-    float* dst = a.partials + (int64_t)net * a.net_partial_stride + (int64_t)(tile / cn) * a.part_stride;
-    if (cn == 1) {
-        // the tile's partial: one bulk copy per dW2 row (H floats), one for
-        // dW1, one per vector (all offsets and sizes multiples of 16 bytes)
-        umma::fence_smem_to_async();
-        __syncthreads();
-        if (tid < Hn) {
-            umma::bulk_s2g(dst + off.w2 + tid * Hn, st2 + tid * kStride2, (uint32_t)(Hn * 4));
-            if (tid == 0) umma::bulk_s2g(dst + off.w1, st1, (uint32_t)(Hn * S * 4));
-            if (tid == 1) umma::bulk_s2g(dst + off.w3, sm.vec[0], (uint32_t)(Hn * 4));
-            if (tid == 2) umma::bulk_s2g(dst + off.b2, sm.vec[1], (uint32_t)(Hn * 4));
-            if (tid == 3) umma::bulk_s2g(dst + off.b1, sm.vec[2], (uint32_t)(Hn * 4));
-            if (tid == 4) dst[off.b3] = sm.vb3;
-            umma::bulk_commit();
-            umma::bulk_wait_read();
-        }
-    } else {
-        // sum of the cluster's tiles: CTA `rank` of a cluster of cn adds rows
-        // [rank * HH / cn, (rank + 1) * HH / cn) of dW2 and dW1 and the same
-        // entries of dW3, db2, db1 over the cluster's CTAs in rank order,
-        // reading their staging through distributed shared memory, and
-        // stores that slice of the cluster's partial.
-        umma::cluster_sync();
-        const int rank = (int)umma::cluster_rank();
-        const int rows = Hn / cn, r0 = rank * rows;
-        // one flat list of float4 items: the dW2 rows, then the dW1 rows of
-        // the slice; every thread issues the loads of up to kItems items from
-        // all cn CTAs before it adds (the loads are latency-bound)
-        constexpr int kItems = 3;
-        const int n2 = rows * (Hn / 4), n1 = rows * S / 4;
-        for (int base = tid; base < n2 + n1; base += kItems * kThreads) {
-            float4 v[kItems][4];
-            uint32_t src[kItems];
-            float* dp[kItems];
-#pragma unroll
-            for (int k = 0; k < kItems; ++k) {
-                const int e = base + k * kThreads;
-                if (e < n2) {
-                    const int r = r0 + e / (Hn / 4), c = 4 * (e % (Hn / 4));
-                    src[k] = umma::smem_u32(st2 + r * kStride2 + c);
-                    dp[k] = dst + off.w2 + r * Hn + c;
-                } else {
-                    const int i = r0 * S + 4 * (e - n2);
-                    src[k] = umma::smem_u32(st1 + i);
-                    dp[k] = dst + off.w1 + i;
-                }
-#pragma unroll
-                for (int rk = 0; rk < 4; ++rk)
-                    if (e < n2 + n1 && rk < cn) v[k][rk] = umma::ld_cluster4(umma::cluster_map(src[k], (uint32_t)rk));
-            }
-#pragma unroll
-            for (int k = 0; k < kItems; ++k) {
-                if (base + k * kThreads >= n2 + n1) continue;
-                float4 t = v[k][0];
-#pragma unroll
-                for (int rk = 1; rk < 4; ++rk)
-                    if (rk < cn) { t.x += v[k][rk].x; t.y += v[k][rk].y; t.z += v[k][rk].z; t.w += v[k][rk].w; }
-                *reinterpret_cast<float4*>(dp[k]) = t;
-            }
-        }
-        for (int e = tid; e < 3 * rows; e += kThreads) {
-            const int k = e / rows, c = r0 + e % rows;
-            dst[(k == 0 ? off.w3 : k == 1 ? off.b2 : off.b1) + c] = cluster_sum1(&sm.vec[k][c], cn);
-        }
-        if (rank == 0 && tid == 0) dst[off.b3] = cluster_sum1(&sm.vb3, cn);
-        // no CTA leaves (and frees its shared memory) while a peer still reads it
-        umma::cluster_sync();
+    // this CTA's partial: one bulk copy per dW2 row (H floats), one for dW1,
+    // one per vector (all offsets and sizes multiples of 16 bytes)
+    float* dst = a.partials + (int64_t)net * a.net_partial_stride + (int64_t)blockIdx.x * a.part_stride;
+    umma::fence_smem_to_async();
+    __syncthreads();
+    if (tid < Hn) {
+        umma::bulk_s2g(dst + off.w2 + tid * Hn, st2 + tid * kStride2, (uint32_t)(Hn * 4));
+        if (tid == 0) umma::bulk_s2g(dst + off.w1, st1, (uint32_t)(Hn * S * 4));
+        if (tid == 1) umma::bulk_s2g(dst + off.w3, sm.vec[0], (uint32_t)(Hn * 4));
+        if (tid == 2) umma::bulk_s2g(dst + off.b2, sm.vec[1], (uint32_t)(Hn * 4));
+        if (tid == 3) umma::bulk_s2g(dst + off.b1, sm.vec[2], (uint32_t)(Hn * 4));
+        if (tid == 4) dst[off.b3] = sm.vb3;
+        umma::bulk_commit();
+        umma::bulk_wait_read();
     }
     if (!ok && tid == 0) atomicAdd(a.status + OFRL_STAT_TIMEOUT, 1);
     umma::fence_before_sync();
@@ -633,39 +576,16 @@ cudaError_t configure_np() {
     return state;
 }
 
-// Largest cluster (4, 2, 1) of 1-CTA-per-SM tiles the device schedules.
-// Clusters of 8 such CTAs do not all fit at once on a 152-SM part (the grid
-// then runs in two waves), and the summation through distributed shared
-// memory costs as much as it saves in the reduction beyond 4.
-constexpr int kMaxCluster = 4;
-constexpr int kMaxPartials = 128;   // partials per network the reduce reads well in one pass
-int max_cluster() {
-    static int best = 0;
-    if (best == 0) {
-        best = 1;
-        if (configure_np<3>() == cudaSuccess && configure_np<1>() == cudaSuccess) {
-            for (int c = kMaxCluster; c >= 2; c >>= 1) {
-                cudaLaunchConfig_t cfg = {};
-                cfg.gridDim = dim3((unsigned)c, 1, 1);
-                cfg.blockDim = dim3(kThreads, 1, 1);
-                cfg.dynamicSmemBytes = sizeof(TcSmem);
-                cudaLaunchAttribute attr[1];
-                attr[0].id = cudaLaunchAttributeClusterDimension;
-                attr[0].val.clusterDim.x = (unsigned)c;
-                attr[0].val.clusterDim.y = 1;
-                attr[0].val.clusterDim.z = 1;
-                cfg.attrs = attr;
-                cfg.numAttrs = 1;
-                int n = 0;
-                if (cudaOccupancyMaxActiveClusters(&n, vnet_tc_kernel<3>, &cfg) == cudaSuccess && n > 0) {
-                    best = c;
-                    break;
-                }
-                cudaGetLastError();
-            }
-        }
+int num_sms() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                       cudaSuccess)
+            n = 1;
+        cudaGetLastError();
     }
-    return best;
+    return n;
 }
 
 template <int NP>
@@ -673,32 +593,21 @@ cudaError_t launch_np(const VnetLaunch& a, const uint8_t* wimg, cudaStream_t st)
     const cudaError_t e = configure_np<NP>();
     if (e != cudaSuccess) return e;
     const int n_tiles = (a.batch + TM - 1) / TM;
-    VnetLaunch c = a;
-    c.cluster = vnet_tc_cluster(n_tiles);
-    const dim3 grid((unsigned)n_tiles, a.n_nets);
-    return launch_pdl_cluster(vnet_tc_kernel<NP>, grid, dim3(kThreads), sizeof(TcSmem), st, (unsigned)c.cluster, c,
-                              wimg);
+    const dim3 grid((unsigned)vnet_tc_ctas(n_tiles, a.n_nets), a.n_nets);
+    return launch_pdl(vnet_tc_kernel<NP>, grid, dim3(kThreads), sizeof(TcSmem), st, a, wimg);
 }
 
 }  // namespace
 
 int64_t vnet_tc_image_bytes() { return tc::weight_image_bytes(); }
 
-int vnet_tc_cluster(int n_tiles) {
-    // the smallest cluster that leaves at most kMaxPartials partials: each
-    // CTA then writes its tile's partial with bulk copies and skips the
-    // exchange through distributed shared memory, which costs a CTA more
-    // than the reduce spends on the extra partials up to that count (128
-    // tiles: 35.0 us a step unclustered against 37.1 in clusters of 4; 512
-    // tiles: 121.3 us in clusters of 4 against 126.3 unclustered)
-    const int m = max_cluster();
-    int best = 1;
-    for (int c = 1; c <= m; c <<= 1) {
-        if (n_tiles % c != 0) continue;
-        best = c;
-        if (n_tiles / c <= kMaxPartials) break;
-    }
-    return best;
+int vnet_tc_ctas(int n_tiles, int n_nets) {
+    // one wave of one CTA per SM, the tiles spread evenly: with more tiles
+    // than that, each CTA runs ceil(tiles / CTAs) of them back to back and
+    // writes one partial (512 tiles: 128 CTAs of 4 tiles)
+    const int per_net = num_sms() / (n_nets > 0 ? n_nets : 1) > 0 ? num_sms() / (n_nets > 0 ? n_nets : 1) : 1;
+    const int per_cta = (n_tiles + per_net - 1) / per_net;
+    return (n_tiles + per_cta - 1) / per_cta;
 }
 
 bool vnet_tc_supported(const VnetLaunch& a) {

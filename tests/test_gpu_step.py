@@ -217,7 +217,7 @@ def test_vnet_path_choice():
     (dataclasses.replace(synth.TINY, batch=1000, capacity=1 << 14, steps=2), "tc_fused"),
     (dataclasses.replace(synth.PROD, batch=32768, steps=2), "tc_fused"),
 ], ids=["prod_layered", "twin_bf16_layered", "prod_cuda_cores", "budgeted_cuda_cores", "budgeted_one_tile",
-        "tiny_cuda_cores", "h64_ragged_fused", "prod_256_tiles_cluster2"])
+        "tiny_cuda_cores", "h64_ragged_fused", "prod_256_tiles_two_per_cta"])
 def test_step_on_each_vnet_path(w, path):
     # every implementation against the oracle (the default ones run in the tests above)
     test_train_step_matches_oracle(w, path=path)
