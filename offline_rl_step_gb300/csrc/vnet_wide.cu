@@ -92,6 +92,7 @@ struct SmemA {
     int32_t act[TM];
     float vrow[TM];
     uint64_t full[kStagesA], empty[kStagesA], bar_mma, bar_load;
+    uint64_t piece[2][4];   // round p of the h1 / dz2 pieces written (one arrival per epilogue warp)
     uint32_t tmem_slot;
 };
 
@@ -167,11 +168,29 @@ __device__ __forceinline__ void load_x(SmemA<H, NP>& sm, const WideMaps& mp, int
     umma::tma_load5(sm.ring + s * G::kStageA, G4 ? &mp.dz2k : &mp.h1k, 0, 2 * j, 0, 0, nt, &sm.full[s]);
 }
 
+// The i-th K-chunk a streamed GEMM consumes: the epilogue writes the
+// activation in rounds, round p holding piece p (16 columns) of every column
+// group (H / 4 columns each), so chunk order follows the rounds and a GEMM
+// starts on the first round while the epilogue writes the next.
+template <int H>
+__device__ __forceinline__ int chunk_of(int i) { return (i % 4) * (H / 64) + i / 4; }
+
+// Thread 0 of kernel A: the activation part of the i-th chunk once its
+// round of pieces is written.
+template <int H, int NP, bool G4>
+__device__ __forceinline__ bool load_x_when_written(SmemA<H, NP>& sm, const WideMaps& mp, int s, int i, int nt,
+                                                    bool ok) {
+    ok = wait_bar(&sm.piece[G4 ? 1 : 0][i / 4], 0u, ok);
+    load_x<H, NP, G4>(sm, mp, s, chunk_of<H>(i), nt);
+    return ok;
+}
+
 // Thread 0 of kernel A: one streamed GEMM (G2 or G4) over the chunks
 // n0 .. n0 + kChunks - 1 of the stage ring (chunk n uses stage n % S for the
-// (n / S)-th time).  Chunks n0 .. n0 + S - 1 were loaded before; every later
-// chunk goes into the stage of the chunk before it as soon as that chunk's
-// MMAs are done, so one issued chunk always waits in the queue.
+// (n / S)-th time), K-chunks in chunk_of order.  Chunks n0 .. n0 + S - 1
+// were loaded before; every later chunk goes into the stage of the chunk
+// before it as soon as that chunk's MMAs are done, so one issued chunk
+// always waits in the queue.
 template <int H, int NP, bool G4>
 __device__ __forceinline__ bool run_gemm(SmemA<H, NP>& sm, const WideMaps& mp, int n0, uint32_t d_tmem, int net,
                                          int nt, bool ok) {
@@ -198,8 +217,8 @@ __device__ __forceinline__ bool run_gemm(SmemA<H, NP>& sm, const WideMaps& mp, i
         if (j >= 1 && j - 1 + S < G::kChunks) {
             const int p = n - 1, sp = p % S;
             ok = wait_bar(&sm.empty[sp], (uint32_t)(p / S) & 1u, ok);
-            load_w<H, NP, G4>(sm, mp, sp, j - 1 + S, net);
-            load_x<H, NP, G4>(sm, mp, sp, j - 1 + S, nt);
+            load_w<H, NP, G4>(sm, mp, sp, chunk_of<H>(j - 1 + S), net);
+            ok = load_x_when_written<H, NP, G4>(sm, mp, sp, j - 1 + S, nt, ok);
         }
     }
     return ok;
@@ -239,6 +258,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma::mbar_init(&sm.bar_mma, 1);
         umma::mbar_init(&sm.bar_load, 1);
+        for (int r = 0; r < 4; ++r) {
+            umma::mbar_init(&sm.piece[0][r], kEpiWarps);
+            umma::mbar_init(&sm.piece[1][r], kEpiWarps);
+        }
         umma::fence_mbar_init();
     }
     if (warp == 0) umma::tmem_alloc(&sm.tmem_slot, kTmemCols);
@@ -297,8 +320,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma::commit(&sm.bar_mma);
     }
     wait_mma();
-    if (tid == 0)
-        for (int j = 0; j < S; ++j) load_w<H, NP, false>(sm, mp, j, j, net);
+    // ---- G2: z2 = h1 . W2^T, streamed; each K-chunk as soon as its round of
+    // h1 pieces is written; then the first W2 MN-chunks of G4 ----
+    if (tid == 0) {
+        for (int j = 0; j < S; ++j) load_w<H, NP, false>(sm, mp, j, chunk_of<H>(j), net);
+        for (int j = 0; j < S; ++j) ok = load_x_when_written<H, NP, false>(sm, mp, j, j, nt, ok);
+        ok = run_gemm<H, NP, false>(sm, mp, 0, tmem + TM_Z2, net, nt, ok);
+        umma::commit(&sm.bar_mma);
+        for (int j = 0; j < S; ++j) {
+            const int n = K + j, s = n % S;
+            ok = wait_bar(&sm.empty[s], (uint32_t)((n - S) / S) & 1u, ok);
+            load_w<H, NP, true>(sm, mp, s, chunk_of<H>(j), net);
+        }
+        // ---- G4: dh1 = dz2 . W2, streamed the same way behind the dz2 pieces ----
+        for (int j = 0; j < S; ++j) ok = load_x_when_written<H, NP, true>(sm, mp, (K + j) % S, j, nt, ok);
+        ok = run_gemm<H, NP, true>(sm, mp, K, tmem + TM_Z1, net, nt, ok);
+        umma::commit(&sm.bar_mma);
+    }
 
     // ---- epilogue 1: h1 = relu(z1 + b1) -> global image; ReLU mask kept ----
     uint64_t mask1 = 0;
@@ -316,20 +354,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (v[j] > 0.0f) mask1 |= 1ull << (16 * p + j);
             }
             store16_global<NP>(h1g, G::kActPlane, H, row, c0, v);
-        }
-        umma::fence_global_to_async();
-    }
-    umma::fence_before_sync();
-    __syncthreads();
-    // ---- G2: z2 = h1 . W2^T, streamed; then the first W2 MN-chunks of G4 ----
-    if (tid == 0) {
-        for (int j = 0; j < S; ++j) load_x<H, NP, false>(sm, mp, j, j, nt);
-        ok = run_gemm<H, NP, false>(sm, mp, 0, tmem + TM_Z2, net, nt, ok);
-        umma::commit(&sm.bar_mma);
-        for (int j = 0; j < S; ++j) {
-            const int n = K + j, s = n % S;
-            ok = wait_bar(&sm.empty[s], (uint32_t)((n - S) / S) & 1u, ok);
-            load_w<H, NP, true>(sm, mp, s, j, net);
+            // round p written by this warp: visible to the tensor copies,
+            // this warp's TMEM reads of z1 ordered before G4 overwrites it
+            umma::fence_global_to_async();
+            umma::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) umma::mbar_arrive(&sm.piece[0][p]);
         }
     }
 
@@ -386,6 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 hw[j] = dv * (z < 0.0f ? 0.0f : z);
             }
             store16_global<NP>(dz2g, G::kActPlane, H, row, c0, g);
+            umma::fence_global_to_async();
+            __syncwarp();
+            if (lane == 0) umma::mbar_arrive(&sm.piece[1][p]);   // round p of dz2 written by this warp
             const float s3 = colsum16(hw);
             const float s2 = colsum16(g);
             if ((lane & 1) == 0) {
@@ -393,20 +426,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sm.red[1][ew][16 * p + ((lane >> 1) & 15)] = s2;
             }
         }
-        umma::fence_global_to_async();
         if (cg == 0) {
             const float ls = warp_sum(lossp), ds = warp_sum(dv);
             if (lane == 0) { sm.lred[0][q] = ls; sm.lred[1][q] = ds; }
         }
-    }
-    umma::fence_before_sync();
-    __syncthreads();
-    // ---- G4: dh1 = dz2 . W2, streamed ----
-    if (tid == 0) {
-        umma::fence_after_sync();
-        for (int j = 0; j < S; ++j) load_x<H, NP, true>(sm, mp, (K + j) % S, j, nt);
-        ok = run_gemm<H, NP, true>(sm, mp, K, tmem + TM_Z1, net, nt, ok);
-        umma::commit(&sm.bar_mma);
+        epi_sync();
     }
     if (epi) {
         // the tile's vectors (fixed order over the four lane-quarter warps)
