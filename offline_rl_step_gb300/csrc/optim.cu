@@ -40,6 +40,18 @@ __device__ __forceinline__ void add4(float4& s, const float4& v) {
     s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
 }
 
+// 16-byte load of a gradient partial, read once: evict_first in L2.
+__device__ __forceinline__ float4 ld_last(const float* p) {
+    float4 v;
+    asm volatile(
+        "{\n\t.reg .b64 pol;\n\t"
+        "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+        "ld.global.cg.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], pol;\n\t}"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "l"(p));
+    return v;
+}
+
 // Sum of the partials of element group i4..i4+3 over partials ty, ty + TL,
 // ... in that order, U independent 16-byte loads in flight at a time.
 template <int TL, int U>
@@ -50,8 +62,7 @@ __device__ __forceinline__ float4 sum_tiles(const float* __restrict__ pp, int64_
         float4 v[U];
 #pragma unroll
         for (int u = 0; u < U; ++u)
-            v[u] = t + u * TL < n_parts ? __ldcg(reinterpret_cast<const float4*>(pp + (int64_t)(t + u * TL) * stride + i4))
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[u] = t + u * TL < n_parts ? ld_last(pp + (int64_t)(t + u * TL) * stride + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int u = 0; u < U; ++u) add4(acc, v[u]);
     }

@@ -171,6 +171,38 @@ __device__ __forceinline__ void tma_load5(void* dst_smem, const void* tmap, int 
         : "memory");
 }
 
+// L2 eviction priorities (createpolicy): evict_last for lines that a later
+// kernel of the step reads back (activation images, gradient partials),
+// evict_first for lines read for the last time.
+__device__ __forceinline__ uint64_t l2_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 16-byte global store under an L2 policy.
+__device__ __forceinline__ void st16_hint(void* p, const uint4& v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
+// tma_load5 under an L2 policy.
+__device__ __forceinline__ void tma_load5_hint(void* dst_smem, const void* tmap, int c0, int c1, int c2, int c3,
+                                               int c4, uint64_t* bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar)),
+        "l"(pol)
+        : "memory");
+}
+
 // Make this thread's generic-proxy global-memory writes visible to later
 // async-proxy reads (tensor copies) of the same addresses.
 __device__ __forceinline__ void fence_global_to_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
@@ -180,6 +212,12 @@ __device__ __forceinline__ void fence_global_to_async() { asm volatile("fence.pr
 __device__ __forceinline__ void bulk_s2g(void* dst_gmem, const void* src_smem, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst_gmem),
                  "r"(smem_u32(src_smem)), "r"(bytes)
+                 : "memory");
+}
+// bulk_s2g under an L2 policy.
+__device__ __forceinline__ void bulk_s2g_hint(void* dst_gmem, const void* src_smem, uint32_t bytes, uint64_t pol) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst_gmem),
+                 "r"(smem_u32(src_smem)), "r"(bytes), "l"(pol)
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }

@@ -137,7 +137,7 @@ __host__ __device__ constexpr int term_b(int t) { return t == 2 ? 2 : (t == 1 ||
 // with C columns (NP planes of `plane` bytes).
 template <int NP>
 __device__ __forceinline__ void store16_global(uint8_t* img, uint32_t plane, int C, int r, int c0,
-                                               const float (&v)[16]) {
+                                               const float (&v)[16], uint64_t pol) {
     uint32_t t[NP][8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -147,8 +147,8 @@ __device__ __forceinline__ void store16_global(uint8_t* img, uint32_t plane, int
     const uint32_t o0 = tc::img_off(r, c0, C), o1 = tc::img_off(r, c0 + 8, C);
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
-        *reinterpret_cast<uint4*>(img + (uint32_t)p * plane + o0) = make_uint4(t[p][0], t[p][1], t[p][2], t[p][3]);
-        *reinterpret_cast<uint4*>(img + (uint32_t)p * plane + o1) = make_uint4(t[p][4], t[p][5], t[p][6], t[p][7]);
+        umma::st16_hint(img + (uint32_t)p * plane + o0, make_uint4(t[p][0], t[p][1], t[p][2], t[p][3]), pol);
+        umma::st16_hint(img + (uint32_t)p * plane + o1, make_uint4(t[p][4], t[p][5], t[p][6], t[p][7]), pol);
     }
 }
 
@@ -165,7 +165,8 @@ __device__ __forceinline__ void load_w(SmemA<H, NP>& sm, const WideMaps& mp, int
 template <int H, int NP, bool G4>
 __device__ __forceinline__ void load_x(SmemA<H, NP>& sm, const WideMaps& mp, int s, int j, int nt) {
     using G = Geo<H, NP>;
-    umma::tma_load5(sm.ring + s * G::kStageA, G4 ? &mp.dz2k : &mp.h1k, 0, 2 * j, 0, 0, nt, &sm.full[s]);
+    umma::tma_load5_hint(sm.ring + s * G::kStageA, G4 ? &mp.dz2k : &mp.h1k, 0, 2 * j, 0, 0, nt, &sm.full[s],
+                         umma::l2_evict_last());
 }
 
 // The i-th K-chunk a streamed GEMM consumes: the epilogue writes the
@@ -249,6 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* h1g = a.act[0] + (int64_t)nt * NP * G::kActPlane;
     uint8_t* dz2g = a.act[1] + (int64_t)nt * NP * G::kActPlane;
     uint8_t* dz1g = a.act[2] + (int64_t)nt * NP * G::kActPlane;
+    // the images stay in L2 for this kernel's streamed GEMMs and kernel B
+    const uint64_t keep = umma::l2_evict_last();
     uint8_t* ring = sm.ring;
 
     if (tid == 0) {
@@ -353,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 v[j] = z < 0.0f ? 0.0f : z;
                 if (v[j] > 0.0f) mask1 |= 1ull << (16 * p + j);
             }
-            store16_global<NP>(h1g, G::kActPlane, H, row, c0, v);
+            store16_global<NP>(h1g, G::kActPlane, H, row, c0, v, keep);
             // round p written by this warp: visible to the tensor copies,
             // this warp's TMEM reads of z1 ordered before G4 overwrites it
             umma::fence_global_to_async();
@@ -415,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 g[j] = z > 0.0f ? dv * sm.w3[c0 + j] : 0.0f;
                 hw[j] = dv * (z < 0.0f ? 0.0f : z);
             }
-            store16_global<NP>(dz2g, G::kActPlane, H, row, c0, g);
+            store16_global<NP>(dz2g, G::kActPlane, H, row, c0, g, keep);
             umma::fence_global_to_async();
             __syncwarp();
             if (lane == 0) umma::mbar_arrive(&sm.piece[1][p]);   // round p of dz2 written by this warp
@@ -494,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = ((mask1 >> (16 * p + j)) & 1ull) ? v[j] : 0.0f;
-            store16_global<NP>(dz1g, G::kActPlane, H, row, c0, v);
+            store16_global<NP>(dz1g, G::kActPlane, H, row, c0, v, keep);
         }
         umma::fence_global_to_async();
     }
@@ -511,9 +514,10 @@ __device__ __forceinline__ void load_step(SmemB<H, NP>& sm, const WideMaps& mp, 
     const int tile = g / kWaysPerTile, rg = 2 * (g % kWaysPerTile), nt = nt0 + tile;
     uint8_t* st = sm.ring + s * G::kStageB;
     umma::mbar_expect_tx(&sm.full[s], G::kStageB);
-    umma::tma_load5(st, &mp.dz2h, 0, 16 * h, rg, 0, nt, &sm.full[s]);
+    const uint64_t last = umma::l2_evict_first();
+    umma::tma_load5_hint(st, &mp.dz2h, 0, 16 * h, rg, 0, nt, &sm.full[s], last);
     umma::tma_load5(st + G::kOffB2, &mp.h1n, 0, 0, rg, 0, nt, &sm.full[s]);
-    umma::tma_load5(st + G::kOffA1, &mp.dz1h, 0, 16 * h, rg, 0, nt, &sm.full[s]);
+    umma::tma_load5_hint(st + G::kOffA1, &mp.dz1h, 0, 16 * h, rg, 0, nt, &sm.full[s], last);
     umma::tma_load5(st + G::kOffB1, &mp.xk, 0, 0, rg, 0, tile, &sm.full[s]);
 }
 
@@ -637,8 +641,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid < 128 + 5) {
         const float* st2 = reinterpret_cast<const float*>(sm.ring);
         const float* st1 = st2 + 128 * G::kStride2;
-        if (tid < 128) umma::bulk_s2g(dst + off.w2 + (int64_t)(128 * h + tid) * H, st2 + tid * G::kStride2, H * 4);
-        if (tid == 128) umma::bulk_s2g(dst + off.w1 + (int64_t)128 * h * S_, st1, (uint32_t)(128 * S_ * 4));
+        const uint64_t keep = umma::l2_evict_last();
+        if (tid < 128)
+            umma::bulk_s2g_hint(dst + off.w2 + (int64_t)(128 * h + tid) * H, st2 + tid * G::kStride2, H * 4, keep);
+        if (tid == 128) umma::bulk_s2g_hint(dst + off.w1 + (int64_t)128 * h * S_, st1, (uint32_t)(128 * S_ * 4), keep);
         if (tid == 129) umma::bulk_s2g(dst + off.w3 + 128 * h, sm.vec[0], 512);
         if (tid == 130) umma::bulk_s2g(dst + off.b2 + 128 * h, sm.vec[1], 512);
         if (tid == 131) umma::bulk_s2g(dst + off.b1 + 128 * h, sm.vec[2], 512);
