@@ -49,7 +49,7 @@ def test_relabel_full_size(w):
 
 
 @pytest.mark.parametrize("strategy", ["final", "future", "random"])
-@pytest.mark.parametrize("batch", [1, 15, 17, 1000])
+@pytest.mark.parametrize("batch", [1, 15, 17, 1000, 40001])   # 40001: the 16-rows-per-warp kernel, ragged
 def test_relabel_ragged_batches(strategy, batch):
     w = dataclasses.replace(synth.TINY, strategy=strategy, ep_len=(5, 40), capacity=3000)
     _run(w, step=11, batch=batch)
