@@ -223,6 +223,17 @@ def test_step_on_each_vnet_path(w, path):
     test_train_step_matches_oracle(w, path=path)
 
 
+@pytest.mark.parametrize("w", [
+    dataclasses.replace(synth.PROD, state_dim=64, num_actions=16, batch=1000, capacity=1 << 14, steps=2),
+    dataclasses.replace(synth.PROD, state_dim=63, hidden=256, num_actions=16, batch=300, capacity=1 << 14, steps=2),
+    dataclasses.replace(synth.TINY, state_dim=64, num_actions=1, batch=700, capacity=1 << 14, steps=2),
+], ids=["s64_a16_h128", "s63_a16_h256", "s64_a1_h64"])
+def test_step_at_shape_limits(w):
+    # the largest state (no ones column in the state-tile image: db1 from
+    # column sums), the most and the fewest actions, hidden 256 with S = 63
+    test_train_step_matches_oracle(w)
+
+
 def test_single_row_batch_step():
     need_gpu()
     w = dataclasses.replace(synth.TINY, batch=1, her_ratio=1.0, steps=2)
