@@ -8,9 +8,11 @@
  *  - Pointers named in a comment as "device" are CUDA device pointers
  *    (or managed memory) on the current device; the caller owns every buffer.
  *    ofrl_train_step's q, loss_out and norms_out may also point into
- *    page-locked host memory (cudaHostAlloc / cudaHostRegister): the kernels
- *    then read Q and write the loss and norms in place over the host link
- *    (NVLink-C2C on Grace-Blackwell) instead of copies on the stream.
+ *    page-locked host memory (cudaHostAlloc / cudaHostRegister): the
+ *    relabel launch then copies Q over the host link (NVLink-C2C on
+ *    Grace-Blackwell) into the workspace while the previous step's
+ *    optimizer kernel still runs, and the optimizer writes the loss and
+ *    norms in place, instead of copies on the stream.
  *    The context owns only its workspace (gradient partials, reduction
  *    scratch, the status word), sized once at ofrl_create.  No call after
  *    ofrl_create allocates.
@@ -375,8 +377,9 @@ int32_t ofrl_vnet_path(const ofrl_ctx* ctx, int32_t n_nets);
  * captured CUDA graph.  ofrl_step_graph_create captures one ofrl_train_step
  * with these arguments (all of them checked as ofrl_train_step checks them;
  * nothing runs) and instantiates it.  ofrl_step_graph_launch replays it on
- * `stream` as the step `step`: the relabel uses `step`; q (device [B, A], or
- * NULL to keep the previous one) and aux_src (host array of n_nets * n_aux
+ * `stream` as the step `step`: the relabel uses `step`; q ([B, A], device
+ * or, as for ofrl_train_step, page-locked host memory; NULL keeps the
+ * previous one) and aux_src (host array of n_nets * n_aux
  * device pointers, or NULL to keep the previous ones) replace the captured
  * pointers; each network's t advances by one in the caller's `nets` array
  * (which must outlive the graph), exactly as ofrl_train_step would.  Every

@@ -415,8 +415,10 @@ class StepGraph:
     def __init__(self, ctx: Context, replay: Replay, her: HerConfig, batch: Batch, nets: List[VNet], opt: Opt, q,
                  aux=None, v_out=None, pi_out=None, argmax_out=None, loss_out=None, norms_out=None, grad_out=None,
                  q_host=None, loss_host=None, norms_host=None):
-        """q_host / loss_host / norms_host (pinned CPU tensors): the graph also copies Q in from q_host and the
-        loss and norms out to loss_host / norms_host; replay it with launch_io."""
+        """q, loss_out and norms_out may be pinned CPU tensors, as for train_step (Q staged by the relabel,
+        loss and norms written in place).  q_host / loss_host / norms_host (pinned CPU tensors, with device
+        q, loss_out, norms_out): the graph also copies Q in from q_host and the loss and norms out to
+        loss_host / norms_host; replay it with launch_io."""
         self.ctx, self.nets = ctx, nets
         self._keep = [replay, batch, nets, q, aux, v_out, pi_out, argmax_out, loss_out, norms_out, grad_out,
                       q_host, loss_host, norms_host]
@@ -429,10 +431,11 @@ class StepGraph:
             for i, t in enumerate(t for per in aux for t in per):
                 self.aux_arr[i] = _ptr(t, F32, "aux").value
         handle = C.c_void_p()
-        args = (ctx.handle, C.byref(self.r), C.byref(self.h), C.byref(self.b), _ptr(q, F32, "q"), self.cn,
+        args = (ctx.handle, C.byref(self.r), C.byref(self.h), C.byref(self.b), _ptr(q, F32, "q", host_ok=True), self.cn,
                 self.n_nets, C.byref(self.o), self.aux_arr if self.n_aux else None, self.n_aux,
                 _ptr(v_out, F32, "v_out"), _ptr(pi_out, F32, "pi_out"), _ptr(argmax_out, I32, "argmax_out"),
-                _ptr(loss_out, F32, "loss_out"), _ptr(norms_out, F32, "norms_out"), _ptr(grad_out, F32, "grad_out"))
+                _ptr(loss_out, F32, "loss_out", host_ok=True), _ptr(norms_out, F32, "norms_out", host_ok=True),
+                _ptr(grad_out, F32, "grad_out"))
         self.io = q_host is not None or loss_host is not None or norms_host is not None
         if self.io:
             _abi.check("ofrl_step_graph_create_io", ctx._lib.ofrl_step_graph_create_io(

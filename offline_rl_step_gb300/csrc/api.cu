@@ -38,7 +38,7 @@ bool hidden_supported(int h) { return h == 64 || h == 128 || h == 256; }
 
 struct Layout {
     int64_t off_partials, off_tile_loss, off_g0, off_gram, off_scalars, off_counter, off_status, off_img, off_ximg,
-        off_act[3], off_tvec, off_barrier, total;
+        off_act[3], off_tvec, off_qbuf, off_barrier, total;
     int32_t max_tiles;
     int32_t tiles128;        // 128-row tiles of the tensor-core paths
     bool layered;            // the layered tensor-core path has its buffers
@@ -77,12 +77,23 @@ Layout layout_of(const ofrl_vshape* s, int32_t max_batch, int32_t max_nets) {
         L.off_act[k] = take(L.layered ? (int64_t)max_nets * L.tiles128 * vnet_wide_act_bytes(s->hidden, planes_of(s))
                                       : 0);
     L.off_tvec = take(L.layered ? (int64_t)max_nets * L.tiles128 * vnet_wide_tvec_stride(s->hidden) * 4 : 0);
+    L.off_qbuf = take((int64_t)max_batch * kMaxActions * 4);
     L.off_barrier = take(8);
     L.total = o;
     return L;
 }
 
 inline ofrl_status cuda_status(cudaError_t e) { return e == cudaSuccess ? OFRL_OK : OFRL_ECUDA; }
+
+// Page-locked host memory (cudaHostAlloc / cudaHostRegister).
+bool host_memory(const void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeHost;
+}
 
 ofrl_status check_ctx(const ofrl_ctx* ctx) {
     if (ctx == nullptr) return OFRL_EINVAL;
@@ -295,6 +306,7 @@ ofrl_status ofrl_create(const ofrl_vshape* shape, int32_t max_batch, int32_t max
     ctx->ws.ximg = reinterpret_cast<uint8_t*>(b + L.off_ximg);
     for (int k = 0; k < 3; ++k) ctx->ws.act[k] = L.layered ? reinterpret_cast<uint8_t*>(b + L.off_act[k]) : nullptr;
     ctx->ws.tvec = L.layered ? reinterpret_cast<float*>(b + L.off_tvec) : nullptr;
+    ctx->ws.qbuf = reinterpret_cast<float*>(b + L.off_qbuf);
     ctx->ws.barrier = reinterpret_cast<unsigned long long*>(b + L.off_barrier);
     ctx->barrier_arrivals = 0;
     ctx->vnet_path = PATH_AUTO;
@@ -755,6 +767,15 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
         ha.pack_nets = n_nets;
         for (int k = 0; k < n_nets; ++k) ha.pack_params[k] = nets[k].params;
         v.ximg = ctx->ws.ximg;
+    }
+    // Q in page-locked host memory: the relabel's row blocks, which run beside
+    // the previous step's optimizer kernel, copy it into the workspace, and the
+    // V kernel reads it there instead of across the host link
+    if (host_memory(q)) {
+        ha.q_src = q;
+        ha.q_dst = ctx->ws.qbuf;
+        ha.q_cols = sh.num_actions;
+        v.q = ctx->ws.qbuf;
     }
     cudaError_t e = launch_her_relabel(ha, st);
     if (e != cudaSuccess) return OFRL_ECUDA;

@@ -43,6 +43,7 @@ struct Workspace {
     uint8_t* ximg;        // [128-row tiles] bf16 images of the relabelled state tiles
     uint8_t* act[3];      // layered tensor-core path: h1, dz2, dz1 images [max_nets][128-row tiles]
     float* tvec;          // layered path: per-tile dW3, db2 column sums and db3 [max_nets][tiles][tvec_stride]
+    float* qbuf;          // [max_batch][A] Q staged from host memory by the relabel (train step)
     unsigned long long* barrier;  // grid-barrier arrival counter of the fused reduce + Adam (only grows)
 };
 
@@ -307,6 +308,11 @@ struct HerLaunch {
     const int32_t* src_in;  // [batch] or null: sources drawn here
     const float* isw_in;    // [batch] or null: weight 1 for every row
     float* isw_out;         // [batch] or null
+    // optional: Q [batch][q_cols] in host memory, copied to q_dst by the row
+    // blocks (the train step's V kernel then reads device memory)
+    const float* q_src;
+    float* q_dst;
+    int32_t q_cols;
 };
 cudaError_t launch_episode_ends_append(const float* dones, int64_t first_index, int32_t n, int32_t* episode_ends,
                                        int32_t* num_episodes, int32_t max_episodes, int32_t* status,

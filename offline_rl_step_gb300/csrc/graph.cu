@@ -234,12 +234,14 @@ ofrl_status launch_graph(ofrl_step_graph* g, uint64_t step, const float* q, cons
             if (aux_src[i] == nullptr) return OFRL_EINVAL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     g->ctx->early_ok = 0;
-    // 1. relabel: the step index
+    // 1. relabel: the step index (and the Q pointer when the relabel stages Q
+    // from host memory)
     g->her.step = step;
+    if (q != nullptr && g->her.q_src != nullptr) g->her.q_src = q;
     void* a0[] = {&g->her};
     cudaError_t e = set_args(g, 0, a0);
     // 2. V: the Q pointer
-    if (e == cudaSuccess && q != nullptr && q != g->vnet.q) {
+    if (e == cudaSuccess && q != nullptr && g->her.q_src == nullptr && q != g->vnet.q) {
         g->vnet.q = q;
         void* a1[] = {&g->vnet, &g->vnet_wimg, g->vnet_maps};
         e = set_args(g, 1, a1);

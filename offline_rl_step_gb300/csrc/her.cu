@@ -85,6 +85,7 @@ __device__ void pack_weights(const HerLaunch& a) {
     }
 }
 
+template <bool STAGE_Q>
 __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerLaunch a) {
     pdl_trigger();
     // The weight packing reads what the previous kernel (Adam) wrote.  The
@@ -99,6 +100,32 @@ __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerL
     if ((int)blockIdx.x >= rb) {
         pack_weights(a);
         return;
+    }
+    // this block's rows of Q (one contiguous run of at most 16 x 16 floats)
+    // from host memory: loaded here, stored into the device copy the V
+    // kernel reads once the rows' own loads are done, so the host link's
+    // latency overlaps them; 16-byte copies when the run is aligned
+    float4 qv = make_float4(0.f, 0.f, 0.f, 0.f);
+    float* q_to = nullptr;
+    bool q_vec = false;
+    if (STAGE_Q) {
+        const int r0 = (rb - 1 - (int)blockIdx.x) * kRowsPerBlock;
+        const int nr = min(kRowsPerBlock, a.batch - r0);
+        if (nr > 0) {
+            const int64_t e0 = (int64_t)r0 * a.q_cols;
+            const int n = nr * a.q_cols;
+            const float* qs = a.q_src + e0;
+            float* qd = a.q_dst + e0;
+            q_vec = ((reinterpret_cast<uintptr_t>(qs) | reinterpret_cast<uintptr_t>(qd)) & 15u) == 0 && (n & 3) == 0;
+            const int i = (int)threadIdx.x;
+            if (q_vec && i < n / 4) {
+                qv = reinterpret_cast<const float4*>(qs)[i];
+                q_to = qd + 4 * i;
+            } else if (!q_vec && i < n) {
+                qv.x = qs[i];
+                q_to = qd + i;
+            }
+        }
     }
     const int sub = threadIdx.x & (kLanesPerRow - 1);
     // blocks in reverse row order: the HER rows (the last rows, with the
@@ -206,6 +233,10 @@ __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerL
         if (base + 2 < a.goal_dim) { sv.z = gv.z; nv.z = gv.z; }
         if (base + 3 < a.goal_dim) { sv.w = gv.w; nv.w = gv.w; }
     }
+    if (STAGE_Q && q_to != nullptr) {
+        if (q_vec) *reinterpret_cast<float4*>(q_to) = qv;
+        else *q_to = qv.x;
+    }
     if (!live) return;
     if (a.ximg != nullptr) {
         // the relabelled state, columns 4 sub .. 4 sub + 3, into this row's tile image
@@ -300,11 +331,15 @@ cudaError_t launch_her_relabel(const HerLaunch& a_in, cudaStream_t st) {
     a.pack_blocks = a.wimg != nullptr ? (a.pack_width > 128 ? 160 : 48) : 0;
     static bool configured = false;
     if (!configured) {
-        const cudaError_t e = set_max_shared_carveout(her_relabel_kernel);
+        cudaError_t e = set_max_shared_carveout(her_relabel_kernel<false>);
+        if (e == cudaSuccess) e = set_max_shared_carveout(her_relabel_kernel<true>);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    return launch_pdl(her_relabel_kernel, dim3(a.relabel_blocks + a.pack_blocks), dim3(kRelabelThreads), 0, st, a);
+    // Q staged from host memory: its own instance (the copy's registers
+    // would lower the occupancy of the plain one)
+    return launch_pdl(a.q_src != nullptr ? her_relabel_kernel<true> : her_relabel_kernel<false>,
+                      dim3(a.relabel_blocks + a.pack_blocks), dim3(kRelabelThreads), 0, st, a);
 }
 
 }  // namespace ofrl

@@ -323,9 +323,19 @@ def test_step_graph_host_io_matches_oracle(w):
 
 @pytest.mark.parametrize("w", [dataclasses.replace(synth.PROD, steps=4),
                                dataclasses.replace(synth.BUDGETED, batch=1000, capacity=1 << 14, steps=3),
-                               dataclasses.replace(synth.TINY, steps=3)],
-                         ids=["prod_host_buffers", "budgeted_host_buffers", "tiny_host_buffers"])
+                               dataclasses.replace(synth.TINY, steps=3),
+                               dataclasses.replace(synth.PROD, batch=1001, capacity=1 << 14, steps=3)],
+                         ids=["prod_host_buffers", "budgeted_host_buffers", "tiny_host_buffers",
+                              "ragged_host_buffers"])
 def test_train_step_with_host_buffers_matches_oracle(w):
-    # Q read in place from pinned host memory, loss and norms written in
-    # place into pinned host memory by the kernels
+    # Q in pinned host memory (staged into the workspace by the relabel's row
+    # blocks; 1001 rows of 5 actions end in a run copied element by element),
+    # loss and norms written in place into pinned host memory by the kernels
     test_train_step_matches_oracle(w, host_io=True)
+
+
+def test_step_graph_with_host_q_matches_oracle():
+    # a graph captured with Q in pinned host memory: each replay points the
+    # relabel's staging copy at that step's host Q
+    w = dataclasses.replace(synth.PROD, batch=2000, capacity=1 << 16, steps=3)
+    test_train_step_matches_oracle(w, graph=True, host_io=True)
