@@ -328,11 +328,12 @@ ofrl_status ofrl_target_ema(const float* params, float* target, int64_t n, float
  * gradient g0).  Increments nets[k].t on the host.
  * When the previous launch of this context on `stream` was a train step, the
  * relabel of this step's batch starts while that step's optimizer kernel
- * still runs (it reads only the replay buffer and writes only the batch;
- * the V kernel still waits for both).  Writes to the replay buffer in
- * between by ordinary kernels or copies are ordered as usual; a kernel of
- * the caller's that lets its dependents launch early (programmatic
- * dependent launch) must not write the replay buffer right before a step. */
+ * still runs (it reads only the replay buffer and, when q is in host memory,
+ * q, and writes only the batch and the context's copy of q; the V kernel
+ * still waits for both).  Writes to the replay buffer or q in between by
+ * ordinary kernels or copies are ordered as usual; a kernel of the caller's
+ * that lets its dependents launch early (programmatic dependent launch)
+ * must not write them right before a step. */
 ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl_her_cfg* her,
                             uint64_t step, const ofrl_batch* batch, const float* q,
                             ofrl_vnet* nets, int32_t n_nets, const ofrl_opt* opt,
