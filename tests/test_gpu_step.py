@@ -324,9 +324,10 @@ def test_step_graph_host_io_matches_oracle(w):
 @pytest.mark.parametrize("w", [dataclasses.replace(synth.PROD, steps=4),
                                dataclasses.replace(synth.BUDGETED, batch=1000, capacity=1 << 14, steps=3),
                                dataclasses.replace(synth.TINY, steps=3),
-                               dataclasses.replace(synth.PROD, batch=1001, capacity=1 << 14, steps=3)],
+                               dataclasses.replace(synth.PROD, batch=1001, capacity=1 << 14, steps=3),
+                               dataclasses.replace(synth.TWIN, steps=3)],
                          ids=["prod_host_buffers", "budgeted_host_buffers", "tiny_host_buffers",
-                              "ragged_host_buffers"])
+                              "ragged_host_buffers", "twin_host_buffers"])
 def test_train_step_with_host_buffers_matches_oracle(w):
     # Q in pinned host memory (staged into the workspace by the relabel's row
     # blocks; 1001 rows of 5 actions end in a run copied element by element),
