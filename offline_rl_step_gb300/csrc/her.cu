@@ -55,6 +55,51 @@ __device__ __forceinline__ int episode_search(const int32_t* __restrict__ ends, 
     return f < len ? lo + f : lo + len;
 }
 
+// The source rows are gathered, and the relabelled rows written, once a step
+// and read by no later kernel of the step: evict_first in L2, so they do not
+// push out the state-tile images and gradient partials that the next
+// kernels read.
+__device__ __forceinline__ float4 ldg4_first(const float* p) {
+    float4 v;
+    asm volatile(
+        "{\n\t.reg .b64 pol;\n\tcreatepolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+        "ld.global.nc.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], pol;\n\t}"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st4_first(float* p, const float4& v) {
+    asm volatile(
+        "{\n\t.reg .b64 pol;\n\tcreatepolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+        "st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, pol;\n\t}" ::"l"(p),
+        "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+        : "memory");
+}
+
+// put4 with the state-tile image kept in L2 (evict_last): the V kernel reads
+// it next.
+__device__ __forceinline__ void st8_keep(uint8_t* p, uint32_t lo, uint32_t hi) {
+    asm volatile(
+        "{\n\t.reg .b64 pol;\n\tcreatepolicy.fractional.L2::evict_last.b64 pol, 1.0;\n\t"
+        "st.global.L2::cache_hint.v2.b32 [%0], {%1, %2}, pol;\n\t}" ::"l"(p),
+        "r"(lo), "r"(hi)
+        : "memory");
+}
+__device__ __forceinline__ void put4_keep(uint8_t* img, uint32_t plane, int np, int C, int r, int c,
+                                          const float (&x)[4]) {
+    const uint32_t o = tc::img_off(r, c, C);
+    if (np == 3) {
+        uint32_t a0, a1, a2, b0, b1, b2;
+        tc::split3x2(x[0], x[1], a0, a1, a2);
+        tc::split3x2(x[2], x[3], b0, b1, b2);
+        st8_keep(img + o, a0, b0);
+        st8_keep(img + plane + o, a1, b1);
+        st8_keep(img + 2 * plane + o, a2, b2);
+    } else {
+        st8_keep(img + o, tc::pack_bf16x2(x[0], x[1]), tc::pack_bf16x2(x[2], x[3]));
+    }
+}
+
 // Extra blocks of the relabel grid: W1 [H][S] -> [W x 64] image and
 // W2 [H][H] -> [W x W] image of every network (W = pack_width >= H: units
 // past H zero), img_planes planes.
@@ -136,8 +181,8 @@ __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerL
     if (a.ximg != nullptr && row_raw >= a.batch && row_raw < a.img_rows) {
         // the last tile's rows past the batch: zero image rows
         const float z[4] = {0.f, 0.f, 0.f, 0.f};
-        tc::put4(a.ximg + (int64_t)(row_raw / tc::TM) * a.img_planes * tc::kPlaneX, tc::kPlaneX, a.img_planes,
-                 tc::KX, row_raw % tc::TM, 4 * sub, z);
+        put4_keep(a.ximg + (int64_t)(row_raw / tc::TM) * a.img_planes * tc::kPlaneX, tc::kPlaneX, a.img_planes,
+                  tc::KX, row_raw % tc::TM, 4 * sub, z);
     }
     const int row = live ? row_raw : a.batch - 1;   // dead half-warps shadow the last row, write nothing
     const uint64_t ctr = (a.step << 32) | ((uint64_t)row << 1);
@@ -161,8 +206,8 @@ __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerL
     const bool has = sub < chunks;
     float4 sv = make_float4(0.f, 0.f, 0.f, 0.f), nv = sv;
     if (has) {
-        sv = __ldg(reinterpret_cast<const float4*>(a.states + (int64_t)src * a.in_stride) + sub);
-        nv = __ldg(reinterpret_cast<const float4*>(a.next_states + (int64_t)src * a.in_stride) + sub);
+        sv = ldg4_first(a.states + (int64_t)src * a.in_stride + 4 * sub);
+        nv = ldg4_first(a.next_states + (int64_t)src * a.in_stride + 4 * sub);
     }
     int act = 0;
     float done = 0.0f, rew = 0.0f;
@@ -245,12 +290,12 @@ __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerL
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             if (!has || 4 * sub + j >= a.state_dim) x[j] = tc::ones_column(4 * sub + j, a.state_dim) ? 1.0f : 0.0f;
-        tc::put4(a.ximg + (int64_t)(row / tc::TM) * a.img_planes * tc::kPlaneX, tc::kPlaneX, a.img_planes, tc::KX,
-                 row % tc::TM, 4 * sub, x);
+        put4_keep(a.ximg + (int64_t)(row / tc::TM) * a.img_planes * tc::kPlaneX, tc::kPlaneX, a.img_planes, tc::KX,
+                  row % tc::TM, 4 * sub, x);
     }
     if (has) {
-        reinterpret_cast<float4*>(a.out_states + (int64_t)row * a.out_stride)[sub] = sv;
-        reinterpret_cast<float4*>(a.out_next_states + (int64_t)row * a.out_stride)[sub] = nv;
+        st4_first(a.out_states + (int64_t)row * a.out_stride + 4 * sub, sv);
+        st4_first(a.out_next_states + (int64_t)row * a.out_stride + 4 * sub, nv);
     }
     if (sub == 0) {
         a.out_actions[row] = act;
