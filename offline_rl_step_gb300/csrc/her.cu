@@ -55,10 +55,10 @@ __device__ __forceinline__ int episode_search(const int32_t* __restrict__ ends, 
     return f < len ? lo + f : lo + len;
 }
 
-// The source rows are gathered, and the relabelled rows written, once a step
-// and read by no later kernel of the step: evict_first in L2, so they do not
-// push out the state-tile images and gradient partials that the next
-// kernels read.
+// The relabelled rows are written, and (with random donors) the source rows
+// gathered, once a step and read by no later kernel of the step:
+// evict_first in L2, so they do not push out the state-tile images and
+// gradient partials that the next kernels read.
 __device__ __forceinline__ float4 ldg4_first(const float* p) {
     float4 v;
     asm volatile(
@@ -131,7 +131,7 @@ __device__ void pack_weights(const HerLaunch& a) {
     }
 }
 
-template <bool STAGE_Q>
+template <bool STAGE_Q, bool RANDOM_DONORS>
 __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerLaunch a) {
     pdl_trigger();
     // The weight packing reads what the previous kernel (Adam) wrote.  The
@@ -206,8 +206,18 @@ __global__ void __launch_bounds__(kRelabelThreads) her_relabel_kernel(const HerL
     const bool has = sub < chunks;
     float4 sv = make_float4(0.f, 0.f, 0.f, 0.f), nv = sv;
     if (has) {
-        sv = ldg4_first(a.states + (int64_t)src * a.in_stride + 4 * sub);
-        nv = ldg4_first(a.next_states + (int64_t)src * a.in_stride + 4 * sub);
+        const float* sr = a.states + (int64_t)src * a.in_stride + 4 * sub;
+        const float* nr = a.next_states + (int64_t)src * a.in_stride + 4 * sub;
+        // evict_first on the gathers pays with 'random' donors (65,536 rows:
+        // 96.3 -> 93.4 us a step) and costs with 'future' ones (two networks:
+        // +0.9 us), so only the random strategy's instance marks them
+        if constexpr (RANDOM_DONORS) {
+            sv = ldg4_first(sr);
+            nv = ldg4_first(nr);
+        } else {
+            sv = __ldg(reinterpret_cast<const float4*>(sr));
+            nv = __ldg(reinterpret_cast<const float4*>(nr));
+        }
     }
     int act = 0;
     float done = 0.0f, rew = 0.0f;
@@ -389,15 +399,15 @@ cudaError_t launch_her_relabel(const HerLaunch& a_in, cudaStream_t st) {
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
-        if (e == cudaSuccess) e = set_max_shared_carveout(her_relabel_kernel<false>);
-        if (e == cudaSuccess) e = set_max_shared_carveout(her_relabel_kernel<true>);
         const int cap_bytes = smem_sm / kCappedBlocks - reserved;
+        for (auto k : {her_relabel_kernel<false, false>, her_relabel_kernel<true, false>,
+                       her_relabel_kernel<false, true>, her_relabel_kernel<true, true>}) {
+            if (e == cudaSuccess) e = set_max_shared_carveout(k);
+            if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, cap_bytes);
+        }
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(her_relabel_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, cap_bytes);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(her_relabel_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, cap_bytes);
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&full, her_relabel_kernel<false>, kRelabelThreads, 0);
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&full, her_relabel_kernel<false, false>, kRelabelThreads,
+                                                              0);
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -405,8 +415,10 @@ cudaError_t launch_her_relabel(const HerLaunch& a_in, cudaStream_t st) {
     const size_t smem = a.early && blocks <= full * sms ? (size_t)(smem_sm / kCappedBlocks - reserved) : 0;
     // Q staged from host memory: its own instance (the copy's registers
     // would lower the occupancy of the plain one)
-    return launch_pdl(a.q_src != nullptr ? her_relabel_kernel<true> : her_relabel_kernel<false>, dim3(blocks),
-                      dim3(kRelabelThreads), smem, st, a);
+    const bool rnd = a.strategy == OFRL_HER_RANDOM;
+    const auto kern = a.q_src != nullptr ? (rnd ? her_relabel_kernel<true, true> : her_relabel_kernel<true, false>)
+                                         : (rnd ? her_relabel_kernel<false, true> : her_relabel_kernel<false, false>);
+    return launch_pdl(kern, dim3(blocks), dim3(kRelabelThreads), smem, st, a);
 }
 
 }  // namespace ofrl
