@@ -32,6 +32,23 @@ enum { OFRL_SELFTEST_TF32 = 0, OFRL_SELFTEST_TF32X3 = 1, OFRL_SELFTEST_BF16 = 2 
 ofrl_status ofrl_selftest_umma(const float* a, const float* b, float* d, int32_t n, int32_t k, int32_t kind,
                                int32_t a_mn, int32_t b_mn, int32_t mn_swap, int32_t* flag, void* stream);
 
+/* Self-test of the bounded grid barrier of the fused reduce + Adam launch
+ * (the train step's optimizer kernel when its grid fits on the device at
+ * once; "DQN Backward-Path NaN Audit", Phase E: device anomalies become
+ * sticky status flags the host reads, never a fault or a hang).
+ * For the train steps of ctx that follow:
+ *   wait_ns      how long each CTA waits at the barrier before it gives up
+ *                (1000 .. 1e10 ns; 0 restores the default, 1 s);
+ *   unreachable  1: the launch's barrier target is one above the arrivals
+ *                its grid can make, so every CTA waits wait_ns and gives up;
+ *                0: the normal target.
+ * A CTA that gives up writes no norms, loss, weights, moments or target and
+ * adds 1 to the status word's timeout count (ofrl_poll_status); the reduced
+ * primary gradient (written before the barrier) is complete.  The arrival
+ * count stays consistent, so the next normal step runs as usual.  Returns
+ * OFRL_EINVAL for a null ctx or values out of range; launches nothing. */
+ofrl_status ofrl_selftest_barrier(ofrl_ctx* ctx, uint64_t wait_ns, int32_t unreachable);
+
 #ifdef __cplusplus
 }
 #endif

@@ -86,6 +86,7 @@ SIGNATURES = {
                                                    vp, vp, vp, vp]),
     "ofrl_selftest_umma": (C.c_int32, [vp, vp, vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
                                        C.c_int32, vp, vp]),
+    "ofrl_selftest_barrier": (C.c_int32, [vp, C.c_uint64, C.c_int32]),
     "ofrl_profile_begin": (C.c_int32, [vp, C.c_int32]),
     "ofrl_profile_end": (C.c_int32, [vp, C.POINTER(C.c_float), C.POINTER(C.c_int32)]),
 }

@@ -21,7 +21,7 @@ using namespace ofrl;
 
 namespace {
 
-constexpr int kMaxGramBlocksWs = 2048;
+constexpr uint64_t kBarrierWaitNs = 1000000000ull;   // a CTA gives up at the grid barrier after 1 s
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
@@ -65,7 +65,7 @@ Layout layout_of(const ofrl_vshape* s, int32_t max_batch, int32_t max_nets) {
     L.off_partials = take((int64_t)max_nets * L.max_tiles * part_stride_of(L.P) * 4);
     L.off_tile_loss = take((int64_t)max_nets * L.max_tiles * 4);
     L.off_g0 = take((int64_t)max_nets * L.P * 4);
-    L.off_gram = take((int64_t)max_nets * kMaxGramBlocksWs * kGramStride * 4);
+    L.off_gram = take((int64_t)max_nets * kMaxGramBlocks * kGramStride * 4);
     L.off_scalars = take((int64_t)max_nets * kScalars * 4);
     L.off_counter = take((int64_t)max_nets * 4);
     L.off_status = take((int64_t)OFRL_STAT_WORDS * 4);
@@ -286,7 +286,7 @@ ofrl_status ofrl_create(const ofrl_vshape* shape, int32_t max_batch, int32_t max
     ctx->max_batch = max_batch;
     ctx->max_nets = max_nets;
     ctx->max_tiles = L.max_tiles;
-    ctx->max_gram_blocks = kMaxGramBlocksWs;
+    ctx->max_gram_blocks = kMaxGramBlocks;
     ctx->n_params = L.P;
     ctx->bytes = L.total;
     if (cudaMalloc(&ctx->base, (size_t)L.total) != cudaSuccess) {
@@ -309,6 +309,8 @@ ofrl_status ofrl_create(const ofrl_vshape* shape, int32_t max_batch, int32_t max
     ctx->ws.qbuf = reinterpret_cast<float*>(b + L.off_qbuf);
     ctx->ws.barrier = reinterpret_cast<unsigned long long*>(b + L.off_barrier);
     ctx->barrier_arrivals = 0;
+    ctx->barrier_wait_ns = kBarrierWaitNs;
+    ctx->barrier_unreachable = 0;
     ctx->vnet_path = PATH_AUTO;
     ctx->early_ok = 0;
     ctx->early_stream = nullptr;
@@ -845,10 +847,12 @@ ofrl_status ofrl_train_step(ofrl_ctx* ctx, const ofrl_replay* replay, const ofrl
     a.weight_decay = opt->weight_decay;
     a.max_grad_norm = opt->max_grad_norm;
     a.status = ctx->ws.status;
+    a.wait_ns = ctx->barrier_wait_ns;
     // 3 + 4 in one cooperative launch when its grid fits on the device
     // (a grid barrier between the reduce and Adam), else two launches
     if (reduce_adam_fusable(r)) {
-        e = launch_reduce_adam(r, a, ctx->ws.barrier, ctx->barrier_arrivals, st);
+        e = launch_reduce_adam(r, a, ctx->ws.barrier, ctx->barrier_arrivals + (ctx->barrier_unreachable ? 1u : 0u),
+                               st);
         if (e != cudaSuccess) return OFRL_ECUDA;
         ctx->barrier_arrivals += (uint64_t)reduce_adam_blocks(r);
         prof_mark(ctx, 3, st);

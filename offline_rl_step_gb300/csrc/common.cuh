@@ -14,6 +14,7 @@ constexpr int kMaxNets = 2;
 constexpr int kMaxSrc = 4;        // primary + up to three auxiliary sources
 constexpr int kGramPairs = 10;    // upper triangle of a 4x4 Gram matrix
 constexpr int kGramStride = 16;   // floats per block's Gram partial (padded: four 16-byte loads)
+constexpr int kMaxGramBlocks = 2048;   // cap of the reduce grid: Gram partials any scratch must hold per network
 constexpr int kScalars = 32;      // per-network scalar slots (see Scalar)
 constexpr int kMaxActions = 16;
 constexpr int kMaxStateDim = 64;
@@ -92,6 +93,11 @@ struct ofrl_ctx {
     int32_t tvec_stride;
     ofrl::WideMaps* maps;       // tensor maps of the layered path (null: not available)
     uint64_t barrier_arrivals;  // arrivals the launched fused kernels add to ws.barrier
+    // self-test of the bounded grid barrier (ofrl_selftest_barrier): its wait
+    // limit, and 1 to give the next fused reduce + Adam launches a target one
+    // above the arrivals their grid can make
+    uint64_t barrier_wait_ns;
+    int32_t barrier_unreachable;
     // measurement hooks: events[step][OFRL_PHASES + 1] while profiling
     cudaEvent_t* prof_events;
     int32_t prof_max;
@@ -426,6 +432,7 @@ struct AdamLaunch {
     float clamp;                 // > 0: |p| <= clamp after the update
     float* target[kMaxNets];     // Polyak target per network, or null
     float polyak[kMaxNets];
+    uint64_t wait_ns;            // fused reduce + Adam: how long a CTA waits at the grid barrier
 };
 cudaError_t launch_target_ema(const float* p, float* target, int64_t n, float polyak, cudaStream_t st);
 cudaError_t launch_adam(const AdamLaunch& a, cudaStream_t st);

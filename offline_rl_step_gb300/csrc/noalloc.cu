@@ -24,7 +24,6 @@ namespace {
 
 constexpr size_t kScratchBytes = (size_t)4 << 20;   // OFRL_NOALLOC_SCRATCH_BYTES
 constexpr int kMaxDevices = 64;
-constexpr int kGramBlocks = 2048;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
@@ -42,7 +41,7 @@ ScratchLayout scratch_layout(int64_t part_stride, int n_tiles) {
     size_t o = 0;
     L.partials = o; o = up256(o + (size_t)n_tiles * part_stride * sizeof(float));
     L.tile_loss = o; o = up256(o + (size_t)n_tiles * sizeof(float));
-    L.gram = o; o = up256(o + (size_t)kGramBlocks * ofrl::kGramStride * sizeof(float));
+    L.gram = o; o = up256(o + (size_t)ofrl::kMaxGramBlocks * ofrl::kGramStride * sizeof(float));
     L.scalars = o; o = up256(o + (size_t)ofrl::kScalars * sizeof(float));
     L.counter = o; o = up256(o + sizeof(unsigned int));
     L.status = o; o = up256(o + OFRL_STAT_WORDS * sizeof(int32_t));

@@ -34,7 +34,6 @@ namespace {
 constexpr int kRedThreads = 256;
 constexpr int kManyParts = 64;     // more partials than this: EL = 32 or 64 (fused), else 8
 constexpr int kRedUnroll = 8;      // partial loads in flight per thread
-constexpr int kMaxGramBlocks = 2048;
 
 __device__ __forceinline__ void add4(float4& s, const float4& v) {
     s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
@@ -126,7 +125,13 @@ __device__ __forceinline__ void fused_norms_adam(const ReduceLaunch& a, const Ad
             gp[tid] = s;
         }
     }
-    const bool ok = grid_barrier(bar, bar_target, 1000000000ull);
+    // A CTA that gave up waiting cannot know the other CTAs' Gram partials:
+    // it writes nothing more (no norms, no p / m / v / target) and only
+    // counts the timeout.  ok is the same for every thread of the CTA.
+    if (!grid_barrier(bar, bar_target, d.wait_ns)) {
+        if (tid == 0) atomicAdd(d.status + OFRL_STAT_TIMEOUT, 1);
+        return;
+    }
 
     // totals of the Gram entries present and of the loss, in the same fixed
     // order in every block.  Every block reads all G Gram partials.  With one
@@ -260,7 +265,6 @@ __device__ __forceinline__ void fused_norms_adam(const ReduceLaunch& a, const Ad
     }
     bad = __syncthreads_count(bad);
     if (bad && tid == 0) atomicAdd(d.status + OFRL_STAT_NONFINITE_GRAD, bad);
-    if (!ok && tid == 0) atomicAdd(d.status + OFRL_STAT_TIMEOUT, 1);
 }
 
 // ADAM: one cooperative launch does the reduce and Adam.  One pass of the

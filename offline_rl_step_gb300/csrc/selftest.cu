@@ -161,3 +161,11 @@ extern "C" ofrl_status ofrl_selftest_umma(const float* a, const float* b, float*
     kern<<<1, ofrl::kSelfThreads, smem, static_cast<cudaStream_t>(stream)>>>(a, b, d, n, k, kind, a_mn, b_mn, mn_swap, flag);
     return cudaGetLastError() == cudaSuccess ? OFRL_OK : OFRL_ECUDA;
 }
+
+extern "C" ofrl_status ofrl_selftest_barrier(ofrl_ctx* ctx, uint64_t wait_ns, int32_t unreachable) {
+    if (ctx == nullptr || (unreachable != 0 && unreachable != 1)) return OFRL_EINVAL;
+    if (wait_ns != 0 && (wait_ns < 1000ull || wait_ns > 10000000000ull)) return OFRL_EINVAL;
+    ctx->barrier_wait_ns = wait_ns != 0 ? wait_ns : 1000000000ull;
+    ctx->barrier_unreachable = unreachable;
+    return OFRL_OK;
+}

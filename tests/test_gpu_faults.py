@@ -122,3 +122,58 @@ def test_two_runs_are_bit_identical():
     for key in ("v", "pi", "loss", "norms", "grad"):
         assert np.array_equal(outs[0][key].view(np.uint32), outs[1][key].view(np.uint32)), key
     assert np.array_equal(outs[0]["params"][0].view(np.uint32), outs[1]["params"][0].view(np.uint32))
+
+
+def test_grid_barrier_timeout_writes_nothing_and_context_stays_usable():
+    # The fused reduce + Adam launch is given a grid-barrier target one above
+    # what its grid can reach and a 2 ms wait limit (a test-only setting of
+    # the context): every CTA gives up, writes no weights, moments or norms,
+    # and counts a timeout.  Nothing faults or hangs: the wait is bounded.
+    # Afterwards the same step runs normally, bit for bit as on a fresh context.
+    need_gpu()
+    from offline_rl_step_gb300 import _abi
+    lib = _abi.load()
+    w = dataclasses.replace(synth.PROD, batch=4096, capacity=1 << 16, steps=1)
+    q0 = synth.make_q(w, 0)
+    g = GpuStep(w)
+    try:
+        assert g.kernels() == 3   # relabel, V, and the cooperative reduce + Adam
+        net = g.nets[0]
+        before = [t.cpu().numpy().copy() for t in (net.params, net.m, net.v)]
+        assert lib.ofrl_selftest_barrier(g.ctx.handle, 2_000_000, 1) == _abi.OK
+        g.step(0, q0)
+        st = g.ctx.poll_status()
+        assert st["timeout"] > 0, st
+        after = [t.cpu().numpy() for t in (net.params, net.m, net.v)]
+        for name, b, a in zip(("params", "m", "v"), before, after):
+            assert np.array_equal(b.view(np.uint32), a.view(np.uint32)), f"{name} written after the timeout"
+        # back to the normal barrier; the step again from t = 0
+        assert lib.ofrl_selftest_barrier(g.ctx.handle, 0, 0) == _abi.OK
+        net.t = 0
+        got = g.step(0, q0)
+        st = g.ctx.poll_status()
+        assert st["timeout"] == 0, st
+    finally:
+        g.close()
+    fresh = GpuStep(w)
+    try:
+        want = fresh.step(0, q0)
+    finally:
+        fresh.close()
+    for key in ("v", "pi", "loss", "norms", "grad"):
+        assert np.array_equal(got[key].view(np.uint32), want[key].view(np.uint32)), key
+    assert np.array_equal(got["params"][0].view(np.uint32), want["params"][0].view(np.uint32))
+
+
+def test_barrier_selftest_arguments():
+    need_gpu()
+    from offline_rl_step_gb300 import _abi
+    lib = _abi.load()
+    g = GpuStep(synth.TINY)
+    try:
+        assert lib.ofrl_selftest_barrier(None, 0, 0) == _abi.EINVAL
+        assert lib.ofrl_selftest_barrier(g.ctx.handle, 10, 0) == _abi.EINVAL          # below 1 us
+        assert lib.ofrl_selftest_barrier(g.ctx.handle, 0, 2) == _abi.EINVAL
+        assert lib.ofrl_selftest_barrier(g.ctx.handle, 1_000_000, 0) == _abi.OK
+    finally:
+        g.close()

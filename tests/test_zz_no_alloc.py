@@ -6,15 +6,19 @@ latency-critical loop), ofrl_iql_value_fwd_bwd_noalloc runs the same
 computation as ofrl_iql_value_fwd_bwd out of the library's fixed scratch
 array.  This test calls both through the C ABI on the same inputs, twice in a
 row (the scratch keeps the previous call's contents), and requires the same
-results within the parity tolerance; it also checks the size limit.  It sits
-in a file of its own that pytest collects last.
+results within the parity tolerance, and the allocation-free results to match
+the oracle (V, loss and gradient within 1e-4 / 1e-5 or the fp32 error bound);
+it also checks the size limit.  It sits in a file of its own that pytest
+collects last.
 """
 import numpy as np
 import pytest
 import torch
 
 import synth
+from _errmodel import grad_ok, value_uncertainty, within
 from _gpu import ATOL, RTOL, assert_close, dev, need_gpu
+from oracle import iql
 
 pytestmark = pytest.mark.gpu
 
@@ -45,6 +49,14 @@ def test_noalloc_matches_context_entry_point_twice(s, h, b):
         torch.cuda.synchronize()
         for name, g, r in zip(("V", "loss", "gradient"), got, want):
             assert_close(g.cpu().numpy(), r.cpu().numpy(), rtol=RTOL, atol=ATOL, what=f"call {call} {name}")
+        # against the oracle (fp64), on the same inputs
+        v_ref, loss_ref, g_ref = iql.value_fwd_bwd(params, x, q, 0.7, s, h)
+        _, _, vu, gu = value_uncertainty(params, x, q, 0.7, s, h)
+        v_got, loss_got, g_got = (t.cpu().numpy() for t in got)
+        assert within(v_got, v_ref, vu, RTOL, ATOL).all(), f"call {call}: V against the oracle"
+        assert_close(loss_got[0], loss_ref, what=f"call {call}: loss against the oracle")
+        ok, _, rel = grad_ok(g_got, g_ref, gu)
+        assert ok, f"call {call}: gradient against the oracle (norm rel {rel:.3g})"
     ctx.close()
 
 
