@@ -18,4 +18,4 @@ Sources (web pages describing the method):
 Every function states the passage it follows.  Pins for every function live
 in tests/test_oracle_*.py.
 """
-from . import her, iql, optim, rng, step  # noqa: F401
+from . import her, iql, optim, precision, rng, step  # noqa: F401

@@ -14,8 +14,18 @@ Follows "GPU IQL + HER Porting Plan":
 All arithmetic in fp64.  Linear layers are y = x W^T + b with W[out, in]
 row-major.  The ReLU derivative is 1[z > 0]; the expectile weight is a
 constant in the derivative, so dL/dV_b = -2 w_b d_b / B.
+
+bf16-operand mode (forward / backward with gemm_operand=precision.bf16):
+the operands of the five matrix products are rounded before the product
+("Phase 2: Multi-Stream Graph Parallelism", "2C. Grouped GEMM for IQL":
+bf16 GEMM inputs, fp32 accumulation); see oracle/precision.py for which
+values that covers.  With gemm_operand=None the products are exact.
 """
 import numpy as np
+
+
+def _same(a):
+    return a
 
 
 def unflatten(flat, state_dim: int, hidden: int):
@@ -37,13 +47,18 @@ def flatten(w1, b1, w2, b2, w3, b3):
     return np.concatenate([w1.ravel(), b1.ravel(), w2.ravel(), b2.ravel(), w3.ravel(), b3.ravel()])
 
 
-def forward(flat, states, state_dim: int, hidden: int):
-    """V forward.  Returns V[B] and the activations the backward needs."""
+def forward(flat, states, state_dim: int, hidden: int, gemm_operand=None):
+    """V forward.  Returns V[B] and the activations the backward needs.
+
+    gemm_operand: None, or the rounding applied to each operand of the two
+    matrix products (X and W1; h1 and W2) before the product.
+    """
+    r = _same if gemm_operand is None else gemm_operand
     w1, b1, w2, b2, w3, b3 = unflatten(flat, state_dim, hidden)
     x = np.asarray(states, dtype=np.float64)[:, :state_dim]
-    z1 = x @ w1.T + b1
+    z1 = r(x) @ r(w1).T + b1
     h1 = np.maximum(z1, 0.0)
-    z2 = h1 @ w2.T + b2
+    z2 = r(h1) @ r(w2).T + b2
     h2 = np.maximum(z2, 0.0)
     v = (h2 @ w3.T + b3)[:, 0]
     return v, dict(x=x, z1=z1, h1=h1, z2=z2, h2=h2)
@@ -99,8 +114,16 @@ def policy(q, v, beta: float):
     return pi, np.argmax(pi, axis=1).astype(np.int32)
 
 
-def backward(flat, act: dict, dv, state_dim: int, hidden: int):
-    """Gradient of the loss w.r.t. the flat parameters, given dL/dV[B]."""
+def backward(flat, act: dict, dv, state_dim: int, hidden: int, gemm_operand=None):
+    """Gradient of the loss w.r.t. the flat parameters, given dL/dV[B].
+
+    gemm_operand: None, or the rounding applied to each operand of the three
+    matrix products (dz2 and h1 for dW2; dz2 and W2 for dh1; dz1 and X for
+    dW1) before the product.  The bias gradients (batch sums of dz1, dz2,
+    dV) and dW3 (the N = 1 output layer) are not matrix products and stay
+    exact.
+    """
+    r = _same if gemm_operand is None else gemm_operand
     w1, b1, w2, b2, w3, b3 = unflatten(flat, state_dim, hidden)
     dv = np.asarray(dv, dtype=np.float64)
     x, z1, h1, z2, h2 = act["x"], act["z1"], act["h1"], act["z2"], act["h2"]
@@ -108,11 +131,11 @@ def backward(flat, act: dict, dv, state_dim: int, hidden: int):
     dz2 = dh2 * (z2 > 0.0)
     dw3 = (dv[None, :] @ h2)          # [1, H]
     db3 = np.array([dv.sum()])
-    dw2 = dz2.T @ h1                  # [H, H]
+    dw2 = r(dz2).T @ r(h1)            # [H, H]
     db2 = dz2.sum(axis=0)
-    dh1 = dz2 @ w2                    # [B, H]
+    dh1 = r(dz2) @ r(w2)              # [B, H]
     dz1 = dh1 * (z1 > 0.0)
-    dw1 = dz1.T @ x                   # [H, S]
+    dw1 = r(dz1).T @ r(x)             # [H, S]
     db1 = dz1.sum(axis=0)
     return flatten(dw1, db1, dw2, db2, dw3, db3)
 
@@ -140,9 +163,9 @@ def backward_abs(flat, act: dict, dv, state_dim: int, hidden: int):
     return flatten(adw1, adb1, adw2, adb2, adw3, adb3)
 
 
-def value_fwd_bwd(flat, states, qt, tau: float, state_dim: int, hidden: int):
-    """V forward + expectile loss + backward, as one call (fp64)."""
-    v, act = forward(flat, states, state_dim, hidden)
+def value_fwd_bwd(flat, states, qt, tau: float, state_dim: int, hidden: int, gemm_operand=None):
+    """V forward + expectile loss + backward, as one call (fp64 sums)."""
+    v, act = forward(flat, states, state_dim, hidden, gemm_operand)
     loss, dv = expectile_loss(qt, v, tau)
-    grad = backward(flat, act, dv, state_dim, hidden)
+    grad = backward(flat, act, dv, state_dim, hidden, gemm_operand)
     return v, loss, grad

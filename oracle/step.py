@@ -24,7 +24,7 @@ from typing import Optional
 
 import numpy as np
 
-from . import her, iql, optim
+from . import her, iql, optim, precision
 
 
 @dataclass
@@ -66,6 +66,10 @@ class StepConfig:
     alpha: tuple = (1.0, 1.0, 1.0, 1.0)
     weight_clamp_max_abs: float = 0.0
     sanitize_sources: bool = False
+    prec: str = "fp32"          # 'bf16': GEMM operands rounded to bf16 (oracle/precision.py)
+
+    def gemm_operand(self):
+        return precision.bf16 if self.prec == "bf16" else None
 
 
 def config_from_workload(w) -> StepConfig:
@@ -75,7 +79,7 @@ def config_from_workload(w) -> StepConfig:
         strategy=her.STRATEGY[w.strategy], goal_threshold=w.goal_threshold, seed=w.seed,
         beta=w.beta, lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps,
         weight_decay=w.weight_decay, max_grad_norm=w.max_grad_norm,
-        budget=tuple(w.budget))
+        budget=tuple(w.budget), prec=w.prec)
 
 
 def train_step(cfg: StepConfig, replay: dict, step: int, q, nets, aux=None):
@@ -91,10 +95,11 @@ def train_step(cfg: StepConfig, replay: dict, step: int, q, nets, aux=None):
     out = dict(batch=batch, v=[], loss=[], pi=[], argmax=[], grad=[], combined=[],
                combined_abs=[], norms=[], skipped=[])
     for k, net in enumerate(nets):
-        v, act = iql.forward(net.params, batch["states"], cfg.state_dim, cfg.hidden)
+        rnd = cfg.gemm_operand()
+        v, act = iql.forward(net.params, batch["states"], cfg.state_dim, cfg.hidden, rnd)
         loss, dv = iql.expectile_loss(qt, v, net.tau)
         pi, am = iql.policy(q, v, cfg.beta)
-        g0 = iql.backward(net.params, act, dv, cfg.state_dim, cfg.hidden)
+        g0 = iql.backward(net.params, act, dv, cfg.state_dim, cfg.hidden, rnd)
         g0_abs = iql.backward_abs(net.params, act, dv, cfg.state_dim, cfg.hidden)
         sources = [g0]
         if aux is not None and aux[k] is not None:
