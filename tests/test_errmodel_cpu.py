@@ -8,7 +8,8 @@ import numpy as np
 import pytest
 
 import synth
-from _errmodel import grad_ok, value_uncertainty, within
+from _errmodel import bf16_uncertainty, bf16_value_uncertainty, grad_ok, value_uncertainty, within
+from oracle.precision import bf16
 from oracle import iql
 
 
@@ -99,3 +100,91 @@ def test_weight_difference_widens_the_bound():
     vp, _, gp = iql.value_fwd_bwd(flat + dp * np.sign(rng.standard_normal(len(flat))), x, qt, 0.7, s, h)
     assert (np.abs(vp - v) <= vu2).all()
     assert (np.abs(gp - g) <= gu2).all()
+
+
+def _bf16_fp32_fwd_bwd(flat, x, qt, tau, s, h):
+    """V and the gradient with bf16 GEMM operands, products summed in fp32
+    (numpy float32, its own order), h1, dz2 and dz1 rounded to bf16 from
+    their fp32 values, db1 summed from the rounded dz1 (as a ones column of
+    the dW1 contraction would)."""
+    f = np.float32
+    w1, b1, w2, b2, w3, b3 = [a.astype(f) for a in iql.unflatten(flat, s, h)]
+    r32 = lambda a: bf16(np.asarray(a, dtype=np.float64)).astype(f)
+    xr = r32(x[:, :s])
+    z1 = xr @ r32(w1).T + b1
+    h1 = r32(np.maximum(z1, f(0)))
+    z2 = h1 @ r32(w2).T + b2
+    h2 = np.maximum(z2, f(0))
+    v = (h2 @ w3.T + b3)[:, 0]
+    n = x.shape[0]
+    d = qt.astype(f) - v
+    wgt = np.where(d >= 0, f(tau), f(1 - tau)).astype(f)
+    dv = (f(-2) * wgt * d / f(n)).astype(f)
+    dz2 = (dv[:, None] * w3) * (z2 > 0)
+    dz2r = r32(dz2)
+    dz1 = (dz2r @ r32(w2)) * (z1 > 0)
+    dz1r = r32(dz1)
+    g = np.concatenate([(dz1r.T @ xr).ravel(), dz1r.sum(0), (dz2r.T @ h1).ravel(), dz2.sum(0),
+                        (dv[None, :] @ h2).ravel(), [dv.sum()]])
+    return v.astype(np.float64), g.astype(np.float64)
+
+
+@pytest.mark.parametrize("h,b,seed", [(128, 16384, 0), (64, 4096, 1), (256, 4096, 2)])
+def test_bf16_fp32_evaluation_inside_bound(h, b, seed):
+    # an fp32 evaluation of the bf16-operand network stays inside the bf16
+    # bound on every element; some V rows are off the exact-rounding oracle by
+    # more than 1e-5 (h1 roundings that go the other way: the bound is
+    # needed).  On the median element the bound is well below the workload's
+    # 2e-2 relative tolerance for V, W2, b2, w3 and b3.  For W1 and b1 it is
+    # looser (a few percent: every ReLU mask of z2 that a possible h1 flip
+    # reaches counts in full, over every row), which the per-tensor norm-wise
+    # check of the GPU tests (tests/_gpu.py bf16_grad_check) makes up for
+    w = dataclasses.replace(synth.PROD, state_dim=50, hidden=h, net_seeds=(seed + 3,))
+    flat = synth.make_params(w).astype(np.float64)
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((b, 50)).astype(np.float32).astype(np.float64)
+    qt = (rng.standard_normal(b) * 2).astype(np.float32).astype(np.float64)
+    v, act = iql.forward(flat, x, 50, h, gemm_operand=bf16)
+    g = iql.backward(flat, act, iql.expectile_loss(qt, v, 0.7)[1], 50, h, gemm_operand=bf16)
+    v32, g32 = _bf16_fp32_fwd_bwd(flat, x, qt, 0.7, 50, h)
+    vu, gu = bf16_uncertainty(flat, x, qt, 0.7, 50, h)
+    assert np.array_equal(vu, bf16_value_uncertainty(flat, x, 50, h))
+    assert (np.abs(v32 - v) <= vu).all()
+    assert (np.abs(g32 - g) <= gu).all()
+    if b >= 16384:
+        assert (np.abs(v32 - v) > 1e-5).sum() >= 1
+    assert np.median(vu / np.abs(v)) < (2e-3 if h <= 128 else 1e-2)
+    seg = iql.flatten(*[np.full(np.shape(a), i) for i, a in enumerate(iql.unflatten(np.zeros(len(flat)), 50, h))])
+    big = np.abs(g) > 1e-6
+    for t in range(2, 6):
+        m = big & (seg == t)
+        assert np.median(gu[m] / np.abs(g[m])) < 2e-3, t
+
+
+def test_bf16_bound_rejects_planted_mistakes():
+    # a plausible kernel bug in one gradient tensor (wrong sign, shifted
+    # index, 10% scale) fails the bf16 gradient check: norm-wise always, and
+    # element-wise on most of the tensor's elements
+    from _gpu import bf16_grad_check
+    s, h, b = 50, 128, 4096
+    w = dataclasses.replace(synth.PROD, state_dim=s, hidden=h)
+    flat = synth.make_params(w).astype(np.float64)
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal((b, s))
+    qt = rng.standard_normal(b) * 2
+    v, act = iql.forward(flat, x, s, h, gemm_operand=bf16)
+    g = iql.backward(flat, act, iql.expectile_loss(qt, v, 0.7)[1], s, h, gemm_operand=bf16)
+    _, gu = bf16_uncertainty(flat, x, qt, 0.7, s, h)
+    assert bf16_grad_check(g, g, gu, s, h)[0]
+    seg = iql.flatten(*[np.full(np.shape(a), i) for i, a in enumerate(iql.unflatten(np.zeros(len(flat)), s, h))])
+    for t in range(6):
+        m = seg == t
+        for mistake in ("sign", "shift", "scale"):
+            if m.sum() == 1 and mistake == "shift":
+                continue
+            bad = g.copy()
+            bad[m] = -bad[m] if mistake == "sign" else (np.roll(bad[m], 1) if mistake == "shift" else bad[m] * 1.1)
+            assert not bf16_grad_check(bad, g, gu, s, h)[0], (t, mistake)
+            if m.sum() > 1 and mistake != "scale":
+                caught = ~within(bad[m], g[m], gu[m], 2e-2, 1e-5)
+                assert caught.mean() > 0.5, (t, mistake, caught.mean())
