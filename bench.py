@@ -31,13 +31,19 @@ UNIT = "samples/s"
 SMS = 152
 FP32_LANES_PER_SM = 128
 PROFILE_NOTE = "profiles/ (ncu launch list and per-kernel summaries)"
+# The sources each dominant kernel is compiled from: their hash keys the ncu
+# traffic figure below, so a changed kernel reports null until captured again.
+KERNEL_SOURCES = {
+    "vnet_tc (tcgen05)": ("vnet_tc.cu", "common.cuh", "tc_image.cuh", "umma.cuh"),
+    "vnet_wide fwd + wgrad (tcgen05, TMA)": ("vnet_wide.cu", "common.cuh", "tc_image.cuh", "umma.cuh"),
+}
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
-# kernel, from the ncu --set full capture summarised under profiles/ (taken
-# on the kernel as it stands; a changed kernel drops its entry until it is
-# captured again)
-NCU_TRAFFIC = {("vnet_tc (tcgen05)", "prod_fp32_B16384_S50_H128_A5"): 6934784,
-               # both layered kernels of one step, cold-cache capture
-               ("vnet_wide fwd + wgrad (tcgen05, TMA)", "budgeted_fp32_B16384_S50_H256_A9"): 95681536}
+# kernel from the ncu capture summarised under profiles/, with the hash of
+# the kernel sources the capture ran (source_hash)
+NCU_TRAFFIC = {
+    # profiles/vnet_tc_prod_fp32_B16384_H128.md (ncu --set full, one launch)
+    ("vnet_tc (tcgen05)", "prod_fp32_B16384_S50_H128_A5"): ("ddecdde7b6214ef9", 6934272),
+}
 
 
 def parse():
@@ -50,6 +56,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="bounded oracle sample (CPU baseline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--repeats", type=int, default=5, help="timed regions of --steps steps; the median is reported")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the per-workload table of the other configs")
     return ap.parse_args()
 
 
@@ -194,177 +202,137 @@ def whole_job_rate(world, steps, rows_per_rank, ms_max):
     return world * steps * rows_per_rank / (ms_max / 1e3)
 
 
-def run_ours(args, w):
-    import torch
-    import torch.distributed as dist
+def source_hash(files):
+    """First 16 hex digits of the sha256 of the given package sources (a kernel and the headers it includes)."""
+    import hashlib
+    hsh = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "offline_rl_step_gb300", "csrc", f), "rb") as fh:
+            hsh.update(fh.read())
+    return hsh.hexdigest()[:16]
 
-    import offline_rl_step_gb300 as ofrl
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+class Run:
+    """One workload set up on the GPU: replay buffer, context, networks, a pre-marshalled step, and every
+    step's Q (device and pinned host) and auxiliary sources resident before any timing."""
 
-    rep = synth.make_replay(w)
-    replay = ofrl.Replay(dev(rep["states"]), dev(rep["next_states"]), dev(rep["actions"]), dev(rep["rewards"]),
-                         dev(rep["dones"]), w.state_dim, w.goal_dim, dev(rep["episode_ends"]))
-    replay_bytes = sum(t.numel() * t.element_size() for t in (replay.states, replay.next_states))
-    del rep
-    her = ofrl.HerConfig(w.batch, w.her_count, w.strategy, w.goal_threshold, w.seed + rank)
-    ctx = ofrl.Context(w.state_dim, w.hidden, w.num_actions, w.prec, max_batch=w.batch, max_nets=w.n_nets)
-    nets = [ofrl.VNet.from_params(torch.from_numpy(synth.make_params(w, k)), w.taus[k]) for k in range(w.n_nets)]
-    opt = ofrl.Opt(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
-                   max_grad_norm=w.max_grad_norm, beta=w.beta, budget=w.budget)
-    batch = ofrl.Batch.empty(w.batch, w.state_stride)
-    n, b, a = w.n_nets, w.batch, w.num_actions
-    v_out = torch.empty(n, b, device="cuda")
-    pi_out = torch.empty(n, b, a, device="cuda")
-    am_out = torch.empty(n, b, dtype=torch.int32, device="cuda")
-    loss_out = torch.empty(n, device="cuda")
-    norms_out = torch.empty(n, 5, device="cuda")
-    total = args.warmup + args.steps
-    q_host = np.stack([synth.make_q(w, k) for k in range(total)])
-    q_dev = dev(q_host)
-    aux_dev = None
-    if w.n_aux:
-        aux_dev = [[dev(x) for x in synth.make_aux(w, k, 0)] for k in range(total)]
-    plan = ofrl.StepPlan(ctx, replay, her, batch, nets, opt, n_aux=w.n_aux, v_out=v_out, pi_out=pi_out,
-                         argmax_out=am_out, loss_out=loss_out, norms_out=norms_out)
+    def __init__(self, w, rank, steps, warmup):
+        import torch
 
-    def step(k):
-        plan.run(k, q_dev[k], [aux_dev[k]] if aux_dev is not None else None)
+        import offline_rl_step_gb300 as ofrl
+        self.torch, self.ofrl, self.w = torch, ofrl, w
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        rep = synth.make_replay(w)
+        self.replay = ofrl.Replay(dev(rep["states"]), dev(rep["next_states"]), dev(rep["actions"]),
+                                  dev(rep["rewards"]), dev(rep["dones"]), w.state_dim, w.goal_dim,
+                                  dev(rep["episode_ends"]))
+        self.replay_bytes = sum(t.numel() * t.element_size() for t in (self.replay.states, self.replay.next_states))
+        del rep
+        self.her = ofrl.HerConfig(w.batch, w.her_count, w.strategy, w.goal_threshold, w.seed + rank)
+        self.ctx = ofrl.Context(w.state_dim, w.hidden, w.num_actions, w.prec, max_batch=w.batch, max_nets=w.n_nets)
+        self.nets = [ofrl.VNet.from_params(torch.from_numpy(synth.make_params(w, k)), w.taus[k])
+                     for k in range(w.n_nets)]
+        self.opt = ofrl.Opt(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
+                            max_grad_norm=w.max_grad_norm, beta=w.beta, budget=w.budget)
+        self.batch = ofrl.Batch.empty(w.batch, w.state_stride)
+        n, b, a = w.n_nets, w.batch, w.num_actions
+        self.v_out = torch.empty(n, b, device="cuda")
+        self.pi_out = torch.empty(n, b, a, device="cuda")
+        self.am_out = torch.empty(n, b, dtype=torch.int32, device="cuda")
+        self.loss_out = torch.empty(n, device="cuda")
+        self.norms_out = torch.empty(n, 5, device="cuda")
+        self.total = warmup + steps
+        self.warmup, self.steps = warmup, steps
+        self.q_host = np.stack([synth.make_q(w, k) for k in range(self.total)])
+        self.q_dev = dev(self.q_host)
+        self.aux_dev = None
+        if w.n_aux:
+            self.aux_dev = [[dev(x) for x in synth.make_aux(w, k, 0)] for k in range(self.total)]
+        self.plan = ofrl.StepPlan(self.ctx, self.replay, self.her, self.batch, self.nets, self.opt, n_aux=w.n_aux,
+                                  v_out=self.v_out, pi_out=self.pi_out, argmax_out=self.am_out,
+                                  loss_out=self.loss_out, norms_out=self.norms_out)
+        self.qh = self.loss_h = self.norms_h = self.hplan = None
 
-    for k in range(args.warmup):
-        step(k)
-    torch.cuda.synchronize()
+    def auxk(self, k):
+        return [self.aux_dev[k]] if self.aux_dev is not None else None
 
-    # ---- timed region: K steps, device time by CUDA events ----
-    clocks = Clocks(local)
-    clocks.start()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for k in range(args.warmup, total):
-        step(k)
-    e1.record()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    clk = clocks.stop()
-    ms = max_over_ranks(e0.elapsed_time(e1), "cuda")
-    ms_per_step = ms / args.steps
-    value = whole_job_rate(world, args.steps, w.batch, ms)
+    def warm(self):
+        for k in range(self.warmup):
+            self.plan.run(k, self.q_dev[k], self.auxk(k))
+        self.torch.cuda.synchronize()
 
-    # ---- per-phase device time (CUDA events inside the step, same stream) ----
-    ofrl.profile_begin(ctx, args.steps)
-    for k in range(args.warmup, total):
-        step(k)
-    phase_ms, nprof = ofrl.profile_end(ctx)
-    phase_avg = {p: v / max(nprof, 1) for p, v in phase_ms.items()}
+    def host_io(self):
+        """The end-to-end form: Q read in place from pinned host memory, loss and norms written in place to
+        pinned host memory (the public train_step call with host buffers)."""
+        torch = self.torch
+        if self.hplan is None:
+            self.qh = torch.from_numpy(self.q_host).pin_memory()
+            self.loss_h = torch.empty(self.w.n_nets, pin_memory=True)
+            self.norms_h = torch.empty(self.w.n_nets, 5, pin_memory=True)
+            self.plan.sync_t()
+            self.hplan = self.ofrl.StepPlan(self.ctx, self.replay, self.her, self.batch, self.nets, self.opt,
+                                            n_aux=self.w.n_aux, v_out=self.v_out, pi_out=self.pi_out,
+                                            argmax_out=self.am_out, loss_out=self.loss_h, norms_out=self.norms_h)
+            for k in range(self.warmup):
+                self.hplan.run(k, self.qh[k], self.auxk(k))
+            torch.cuda.synchronize()
+            self.hplan.sync_t()
+            self.plan.reload_t()
 
-    # ---- end to end through the public API with host buffers ----
-    # (a) train_step reading each step's Q in place from pinned host memory
-    # and writing loss and norms in place into pinned host memory (the bytes
-    # cross NVLink-C2C inside the kernels); (b) the step graph with its host
-    # I/O: one graph launch per step copies this step's pinned host Q in,
-    # runs the step and copies loss and norms out; (c) direct calls with
-    # copies: a torch copy of Q in, train_step, two copies out
-    e2e = None
-    if not args.no_e2e:
-        qh = torch.from_numpy(q_host).pin_memory()
-        q_stage = torch.empty_like(q_dev[0])
-        loss_h = torch.empty(n, pin_memory=True)
-        norms_h = torch.empty(n, 5, pin_memory=True)
-        io_bytes = {"h2d_bytes_per_step": int(b * a * 4), "d2h_bytes_per_step": int(n * 4 + n * 5 * 4)}
-        auxk = lambda k: [aux_dev[k]] if aux_dev is not None else None
-        # (b') the step graph captured with the pinned host Q and the pinned
-        # loss / norms buffers themselves: Q staged by the relabel, the loss
-        # and norms written in place, no copy nodes
+    def region(self, e2e=False, world=1):
+        """One timed region of `steps` steps (CUDA events on the launching stream, a barrier and a
+        synchronize on both sides); returns the milliseconds, max over ranks."""
+        torch = self.torch
+        import torch.distributed as dist
+        if e2e:
+            self.host_io()
+            self.hplan.reload_t()
+            plan, q = self.hplan, self.qh
+        else:
+            plan, q = self.plan, self.q_dev
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for k in range(self.warmup, self.total):
+            plan.run(k, q[k], self.auxk(k))
+        e1.record()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
         plan.sync_t()
-        sgh = ofrl.StepGraph(ctx, replay, her, batch, nets, opt, qh[0], aux=auxk(0), v_out=v_out, pi_out=pi_out,
-                             argmax_out=am_out, loss_out=loss_h, norms_out=norms_h)
-        for k in range(args.warmup):
-            sgh.launch(k, qh[k], auxk(k))
-        torch.cuda.synchronize()
-        e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e2.record()
-        for k in range(args.warmup, total):
-            sgh.launch(k, qh[k], auxk(k))
-        e3.record()
-        torch.cuda.synchronize()
-        sgh.sync_t()
-        sgh.close()
-        gms = max_over_ranks(e2.elapsed_time(e3), "cuda")
-        plan.reload_t()
-        sg = ofrl.StepGraph(ctx, replay, her, batch, nets, opt, q_stage, aux=auxk(0), v_out=v_out, pi_out=pi_out,
-                            argmax_out=am_out, loss_out=loss_out, norms_out=norms_out, q_host=qh[0],
-                            loss_host=loss_h, norms_host=norms_h)
-        for k in range(args.warmup):
-            sg.launch_io(k, qh[k], auxk(k), loss_h, norms_h)
-        torch.cuda.synchronize()
-        e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e2.record()
-        for k in range(args.warmup, total):
-            sg.launch_io(k, qh[k], auxk(k), loss_h, norms_h)
-        e3.record()
-        torch.cuda.synchronize()
-        sg.sync_t()
-        sg.close()
-        ems = max_over_ranks(e2.elapsed_time(e3), "cuda")
-        plan.reload_t()
-        e2.record()
-        for k in range(args.warmup, total):
-            q_stage.copy_(qh[k], non_blocking=True)
-            plan.run(k, q_stage, auxk(k))
-            loss_h.copy_(loss_out, non_blocking=True)
-            norms_h.copy_(norms_out, non_blocking=True)
-        e3.record()
-        torch.cuda.synchronize()
-        dms = max_over_ranks(e2.elapsed_time(e3), "cuda")
-        plan.sync_t()
-        hplan = ofrl.StepPlan(ctx, replay, her, batch, nets, opt, n_aux=w.n_aux, v_out=v_out, pi_out=pi_out,
-                              argmax_out=am_out, loss_out=loss_h, norms_out=norms_h)
-        for k in range(args.warmup):
-            hplan.run(k, qh[k], auxk(k))
-        torch.cuda.synchronize()
-        e2.record()
-        for k in range(args.warmup, total):
-            hplan.run(k, qh[k], auxk(k))
-        e3.record()
-        torch.cuda.synchronize()
-        zms = max_over_ranks(e2.elapsed_time(e3), "cuda")
-        hplan.sync_t()
-        e2e = {"value": whole_job_rate(world, args.steps, w.batch, zms), "unit": UNIT, **io_bytes,
-               "path": "train_step with Q read in place from pinned host memory and loss / norms written in place "
-                       "to pinned host memory (NVLink-C2C)",
-               "graph_value": whole_job_rate(world, args.steps, w.batch, gms),
-               "graph_path": "StepGraph captured with the pinned host Q and loss / norms buffers: one graph launch "
-                             "per step, Q staged by the relabel, loss / norms written in place",
-               "graph_copy_value": whole_job_rate(world, args.steps, w.batch, ems),
-               "graph_copy_path": "StepGraph.launch_io: one graph launch per step (Q copy-in node, step, loss / norms "
-                                  "copy-out nodes)",
-               "copy_value": whole_job_rate(world, args.steps, w.batch, dms),
-               "copy_path": "torch copy of Q in, train_step (three kernel launches), two copies out"}
-    plan.sync_t()
-    status = ctx.poll_status()
+        if e2e:
+            self.plan.reload_t()
+        return max_over_ranks(e0.elapsed_time(e1), "cuda")
 
-    # ---- roofline of the dominant kernel ----
-    pk, pk_kind = peaks()
+    def phases(self):
+        """Per-phase device milliseconds per step (one event pair per phase on the step's stream)."""
+        self.ofrl.profile_begin(self.ctx, self.steps)
+        for k in range(self.warmup, self.total):
+            self.plan.run(k, self.q_dev[k], self.auxk(k))
+        phase_ms, nprof = self.ofrl.profile_end(self.ctx)
+        self.plan.sync_t()
+        return {p: v / max(nprof, 1) for p, v in phase_ms.items()}
+
+    def close(self):
+        self.ctx.close()
+
+
+def roofline(w, phase_avg, path, region_s, pk, pk_kind):
+    """The dominant kernel against its roof, and every phase against its own."""
     alg = algorithmic(w)
     dominant = max(phase_avg, key=phase_avg.get)
     dur_s = phase_avg[dominant] / 1e3
     sm_mhz = pk.get("sm_max_mhz", 2070.0)
-    path = ctx.vnet_path(w.n_nets)
+    # a kernel inside a timed region under a second long runs at the burst
+    # rate; the sustained figure is for kernels inside seconds-long loops
+    burst = region_s < 1.0
+    tpk = pk["bf16_tflops"] if burst or "bf16_tflops_sustained" not in pk else pk["bf16_tflops_sustained"]
+    tpk_name = "bf16_tflops" if burst or "bf16_tflops_sustained" not in pk else "bf16_tflops_sustained"
     if dominant == "vnet" and path in ("tc_fused", "tc_layered"):
         # tensor-core kernels: bf16 MMAs (three-term split, six products per
-        # K-step, for fp32 workloads); algorithmic flops over the measured
-        # sustained bf16 peak (the kernels run inside a long step)
-        peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+        # K-step, for fp32 workloads); algorithmic flops over the bf16 peak
         ach = alg["vnet_flops"] / dur_s / 1e12
         # MMA work as executed: 128-row tiles, S padded to 64, five GEMMs,
         # one product per K-step (bf16) or six (fp32 through the split)
@@ -373,11 +341,15 @@ def run_ours(args, w):
         hp = max(w.hidden, 128)   # hidden 64 runs zero-padded to 128 units on the fused kernel
         mma = w.n_nets * tiles * prods * 2 * 128 * (2 * hp * 64 + 3 * hp ** 2)
         kname = "vnet_tc (tcgen05)" if path == "tc_fused" else "vnet_wide fwd + wgrad (tcgen05, TMA)"
-        roof = {"kernel": kname, "bound": "tensor", "achieved": ach, "peak": peak,
-                "unit": "TFLOP/s", "frac": ach / peak,
-                "traffic": NCU_TRAFFIC.get((kname, w.name)),
-                "peak_source": f"bf16_tflops_sustained ({pk_kind})",
-                "mma_tflops_executed": mma / dur_s / 1e12, "mma_frac_executed": mma / dur_s / 1e12 / peak}
+        entry = NCU_TRAFFIC.get((kname, w.name))
+        traffic = None
+        if entry is not None and entry[0] == source_hash(KERNEL_SOURCES[kname]):
+            traffic = entry[1]
+        roof = {"kernel": kname, "bound": "tensor", "achieved": ach, "peak": tpk,
+                "unit": "TFLOP/s", "frac": ach / tpk, "traffic": traffic,
+                "peak_source": f"{tpk_name} ({pk_kind}; timed region {region_s * 1e3:.1f} ms)",
+                "kernel_source_sha16": source_hash(KERNEL_SOURCES[kname]),
+                "mma_tflops_executed": mma / dur_s / 1e12, "mma_frac_executed": mma / dur_s / 1e12 / tpk}
     elif dominant == "vnet":
         fp32_peak = SMS * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
         ach = alg["vnet_flops"] / dur_s / 1e12
@@ -393,12 +365,11 @@ def run_ours(args, w):
     roof["relabel_hbm_frac"] = alg["relabel_bytes"] / (phase_avg["relabel"] / 1e3) / 1e9 / pk["hbm_gbs"]
     # every phase against its own roof, algorithmic work over the phase's
     # event-timed duration: relabel and the optimizer (reduce, norms, Adam)
-    # against measured HBM, the V forward / backward against the measured
-    # sustained bf16 peak (the fp32 workloads reach it through the split)
+    # against measured HBM, the V forward / backward against the bf16 peak
+    # (the fp32 workloads reach it through the split)
     t_rl = phase_avg["relabel"] / 1e3
     t_v = phase_avg["vnet"] / 1e3
     t_opt = (phase_avg["reduce"] + phase_avg.get("adam", 0.0)) / 1e3
-    tpk = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
     roof["phases"] = {
         "relabel": {"bound": "hbm", "bytes": alg["relabel_bytes"], "achieved_gbs": alg["relabel_bytes"] / t_rl / 1e9,
                     "frac": alg["relabel_bytes"] / t_rl / 1e9 / pk["hbm_gbs"]},
@@ -409,6 +380,83 @@ def run_ours(args, w):
                               "frac": alg["optim_bytes"] / t_opt / 1e9 / pk["hbm_gbs"],
                               "note": "parameter buffers (<= 2.2 MB) are L2-resident"},
     }
+    return roof
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import offline_rl_step_gb300 as ofrl  # noqa: F401
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    pk, pk_kind = peaks()
+
+    run = Run(w, rank, args.steps, args.warmup)
+    run.warm()
+
+    # ---- timed regions: R regions of K steps each (device Q), each followed
+    # by one region of the end-to-end form (host Q in, loss / norms out in
+    # place), interleaved so both see the same box state; medians reported ----
+    clocks = Clocks(local)
+    clocks.start()
+    dev_ms, e2e_ms = [], []
+    for _ in range(args.repeats):
+        dev_ms.append(run.region(world=world))
+        if not args.no_e2e:
+            e2e_ms.append(run.region(e2e=True, world=world))
+    clk = clocks.stop()
+    ms = statistics.median(dev_ms)
+    ms_per_step = ms / args.steps
+    value = whole_job_rate(world, args.steps, w.batch, ms)
+
+    phase_avg = run.phases()
+    path = run.ctx.vnet_path(w.n_nets)
+    roof = roofline(w, phase_avg, path, ms / 1e3, pk, pk_kind)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = {"value": whole_job_rate(world, args.steps, w.batch, statistics.median(e2e_ms)), "unit": UNIT,
+               "h2d_bytes_per_step": int(w.batch * w.num_actions * 4),
+               "d2h_bytes_per_step": int(w.n_nets * 4 + w.n_nets * 5 * 4),
+               "ms_per_step_regions": [round(x / args.steps, 5) for x in e2e_ms],
+               "path": "train_step with Q read in place from pinned host memory and loss / norms written in place "
+                       "to pinned host memory (NVLink-C2C); median of the regions interleaved with the device ones"}
+        e2e.update(other_e2e_forms(run, world))
+    status = run.ctx.poll_status()
+    launches = run.plan.kernels() * args.steps
+    replay_bytes = run.replay_bytes
+    run.close()
+    del run
+    torch.cuda.empty_cache()
+
+    workloads = None
+    if rank == 0 and world == 1 and not args.no_workloads:
+        workloads = {}
+        for ow in synth.ALL:
+            r2 = Run(ow, rank, args.steps, args.warmup)
+            r2.warm()
+            regions = [r2.region() for _ in range(args.repeats)]
+            m = statistics.median(regions)
+            ph = r2.phases()
+            rf = roofline(ow, ph, r2.ctx.vnet_path(ow.n_nets), m / 1e3, pk, pk_kind)
+            workloads[ow.name] = {
+                "value": ow.batch * args.steps / (m / 1e3), "unit": UNIT, "ms_per_step": m / args.steps,
+                "ms_per_step_regions": [round(x / args.steps, 5) for x in regions],
+                "vnet_path": r2.ctx.vnet_path(ow.n_nets), "dominant_kernel": rf["kernel"],
+                "dominant_frac": rf["frac"], "vnet_frac": rf["phases"]["vnet"]["frac"],
+                "vnet_mma_frac_executed": rf.get("mma_frac_executed"),
+                "relabel_hbm_frac": rf["relabel_hbm_frac"],
+                "reduce_norms_adam_hbm_frac": rf["phases"]["reduce_norms_adam"]["frac"],
+                "phase_ms": rf["phase_ms"]}
+            r2.close()
+            del r2
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -420,6 +468,9 @@ def run_ours(args, w):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "steps_per_s": 1e3 / ms_per_step * world,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if w.prec == "bf16" else "f32", "data": "synthetic",
+            "repeats": {"n": args.repeats, "statistic": "median",
+                        "ms_per_step_regions": [round(x / args.steps, 5) for x in dev_ms],
+                        "spread": (max(dev_ms) - min(dev_ms)) / ms},
             "config": {"workload": w.name, "batch": w.batch, "state_dim": w.state_dim, "hidden": w.hidden,
                        "num_actions": w.num_actions, "n_nets": w.n_nets, "her": f"{w.strategy} {w.her_ratio}",
                        "capacity": w.capacity, "parallelism": f"replicas{world}",
@@ -427,13 +478,71 @@ def run_ours(args, w):
                        "vnet_path": path,
                        "l2": f"inputs larger than L2: replay buffer {replay_bytes / 2**20:.0f} MiB read at "
                              f"random rows every step"},
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": plan.kernels() * args.steps, "clocks": clk, "status": status,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "workloads": workloads,
+            "gpu_launches": launches, "clocks": clk, "status": status,
         }
         print(json.dumps(line))
-    ctx.close()
     if world > 1:
         dist.destroy_process_group()
+
+
+def other_e2e_forms(run, world):
+    """Other end-to-end forms, one region each: (a) the step graph captured with the pinned host Q and
+    loss / norms buffers themselves; (b) the step graph with a Q copy-in node and loss / norms copy-out
+    nodes; (c) direct calls with a torch copy of Q in and two copies out."""
+    torch, ofrl = run.torch, run.ofrl
+    run.host_io()
+    qh, loss_h, norms_h, auxk = run.qh, run.loss_h, run.norms_h, run.auxk
+    b = run.w.batch
+    out = {}
+
+    def timed(fn):
+        e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2.record()
+        for k in range(run.warmup, run.total):
+            fn(k)
+        e3.record()
+        torch.cuda.synchronize()
+        return max_over_ranks(e2.elapsed_time(e3), "cuda")
+
+    kw = dict(v_out=run.v_out, pi_out=run.pi_out, argmax_out=run.am_out)
+    sgh = ofrl.StepGraph(run.ctx, run.replay, run.her, run.batch, run.nets, run.opt, qh[0], aux=auxk(0),
+                         loss_out=loss_h, norms_out=norms_h, **kw)
+    for k in range(run.warmup):
+        sgh.launch(k, qh[k], auxk(k))
+    torch.cuda.synchronize()
+    gms = timed(lambda k: sgh.launch(k, qh[k], auxk(k)))
+    sgh.sync_t()
+    sgh.close()
+    q_stage = torch.empty_like(run.q_dev[0])
+    sg = ofrl.StepGraph(run.ctx, run.replay, run.her, run.batch, run.nets, run.opt, q_stage, aux=auxk(0),
+                        loss_out=run.loss_out, norms_out=run.norms_out, q_host=qh[0], loss_host=loss_h,
+                        norms_host=norms_h, **kw)
+    for k in range(run.warmup):
+        sg.launch_io(k, qh[k], auxk(k), loss_h, norms_h)
+    torch.cuda.synchronize()
+    ems = timed(lambda k: sg.launch_io(k, qh[k], auxk(k), loss_h, norms_h))
+    sg.sync_t()
+    sg.close()
+    run.plan.reload_t()
+
+    def copy_step(k):
+        q_stage.copy_(qh[k], non_blocking=True)
+        run.plan.run(k, q_stage, auxk(k))
+        loss_h.copy_(run.loss_out, non_blocking=True)
+        norms_h.copy_(run.norms_out, non_blocking=True)
+    dms = timed(copy_step)
+    run.plan.sync_t()
+    rate = lambda m: whole_job_rate(world, run.steps, b, m)
+    out["graph_value"] = rate(gms)
+    out["graph_path"] = ("StepGraph captured with the pinned host Q and loss / norms buffers: one graph launch per "
+                         "step, Q staged by the relabel, loss / norms written in place")
+    out["graph_copy_value"] = rate(ems)
+    out["graph_copy_path"] = ("StepGraph.launch_io: one graph launch per step (Q copy-in node, step, loss / norms "
+                              "copy-out nodes)")
+    out["copy_value"] = rate(dms)
+    out["copy_path"] = "torch copy of Q in, train_step (three kernel launches), two copies out"
+    return out
 
 
 def main():
