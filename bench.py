@@ -58,6 +58,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--repeats", type=int, default=5, help="timed regions of --steps steps; the median is reported")
     ap.add_argument("--no-workloads", action="store_true", help="skip the per-workload table of the other configs")
+    ap.add_argument("--no-forward", action="store_true", help="skip the IQL-target (V forward) measurement")
     return ap.parse_args()
 
 
@@ -103,6 +104,15 @@ class Clocks:
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        # nvidia-smi's start-up queries the driver for a while and slows
+        # kernel launches meanwhile: begin timing once it has printed a sample
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.05)
+        time.sleep(0.05)
 
     def stop(self):
         if self.proc is None:
@@ -428,6 +438,7 @@ def run_ours(args, w):
                "path": "train_step with Q read in place from pinned host memory and loss / norms written in place "
                        "to pinned host memory (NVLink-C2C); median of the regions interleaved with the device ones"}
         e2e.update(other_e2e_forms(run, world))
+    fwd = None if args.no_forward else forward_bench(run, args.steps, args.repeats, pk, pk_kind, world)
     status = run.ctx.poll_status()
     launches = run.plan.kernels() * args.steps
     replay_bytes = run.replay_bytes
@@ -478,12 +489,45 @@ def run_ours(args, w):
                        "vnet_path": path,
                        "l2": f"inputs larger than L2: replay buffer {replay_bytes / 2**20:.0f} MiB read at "
                              f"random rows every step"},
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "workloads": workloads,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "workloads": workloads, "iql_target": fwd,
             "gpu_launches": launches, "clocks": clk, "status": status,
         }
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+def forward_bench(run, steps, repeats, pk, pk_kind, world):
+    """The IQL bootstrap target r + gamma (1 - done) V(s') of the relabelled batch (ofrl_iql_target: V
+    forward on the next states, tensor cores where the step's V kernel is the fused one): median of
+    `repeats` regions of `steps` calls, rows/s and the forward's flops against the bf16 peak."""
+    torch, ofrl, w = run.torch, run.ofrl, run.w
+    b = w.batch
+    tgt = torch.empty(b, device="cuda")
+    vn = torch.empty(b, device="cuda")
+    prm = run.nets[0].params
+    call = lambda: ofrl.iql_target(run.ctx, prm, run.batch.next_states, run.batch.rewards, run.batch.dones, 0.99,
+                                   tgt, v_next_out=vn)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    regions = []
+    for _ in range(repeats):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        regions.append(max_over_ranks(e0.elapsed_time(e1), "cuda"))
+    ms = statistics.median(regions) / steps
+    flops = 2 * b * (w.state_dim * w.hidden + w.hidden ** 2 + w.hidden)
+    tpk = pk["bf16_tflops"]
+    return {"rows_per_s": whole_job_rate(world, 1, b, ms), "us_per_call": ms * 1e3, "batch": b,
+            "vnet_path": run.ctx.vnet_path(1),
+            "tflops": flops / (ms / 1e3) / 1e12, "frac_of_bf16_burst_peak": flops / (ms / 1e3) / 1e12 / tpk,
+            "peak_source": f"bf16_tflops ({pk_kind})",
+            "note": "one call = weight pack + forward kernel; median of regions of back-to-back calls"}
 
 
 def other_e2e_forms(run, world):

@@ -254,7 +254,12 @@ ofrl_status ofrl_iql_value_fwd_bwd(ofrl_ctx* ctx, const float* params, const flo
  * a forward-only pass of the V network, result kept on the device).
  * params: device [P] (the online or the target network); states: device
  * [batch, state_stride] (columns >= S ignored).  v_out: device [batch].
- * 1 <= batch <= max_batch; asynchronous on `stream`. */
+ * 1 <= batch <= max_batch; asynchronous on `stream`.  Runs on the tensor
+ * cores (a weight-pack launch, then one CTA per 128-row tile: G1, h1, G2,
+ * V) when ofrl_vnet_path(ctx, 1) is OFRL_VNET_TC_FUSED and the states are
+ * 16-byte aligned with state_stride a multiple of 4; else on the CUDA
+ * cores.  Uses the context's weight-image workspace, so calls on one
+ * context must not overlap. */
 ofrl_status ofrl_forward_values(ofrl_ctx* ctx, const float* params, const float* states,
                                 int32_t state_stride, int32_t batch, float* v_out, void* stream);
 
@@ -263,7 +268,8 @@ ofrl_status ofrl_forward_values(ofrl_ctx* ctx, const float* params, const float*
  * max-over-actions target): target_out[b] = rewards[b] + gamma (1 - dones[b])
  * V(next_states[b]) with V from `params` (terminal rows bootstrap nothing).
  * rewards, dones: device [batch] (e.g. the relabelled batch's); v_next_out:
- * device [batch] or NULL, receives V(s').  gamma in [0, 1]. */
+ * device [batch] or NULL, receives V(s').  gamma in [0, 1].  Same
+ * implementation choice as ofrl_forward_values. */
 ofrl_status ofrl_iql_target(ofrl_ctx* ctx, const float* params, const float* next_states,
                             int32_t state_stride, const float* rewards, const float* dones,
                             int32_t batch, float gamma, float* v_next_out, float* target_out,

@@ -439,7 +439,12 @@ ofrl_status value_forward(ofrl_ctx* ctx, const float* params, const float* state
     v.gamma = gamma;
     v.target_out = target_out;
     v.status = ctx->ws.status;
-    return cuda_status(launch_vnet_forward(v, static_cast<cudaStream_t>(stream)));
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the tensor cores where the context's step takes the fused kernel (and
+    // the states meet its alignment), else the CUDA cores
+    if (choose_path(ctx, v) == PATH_FUSED && ctx->ws.img != nullptr)
+        return cuda_status(launch_vnet_tc_forward(v, ctx->ws.img, st));
+    return cuda_status(launch_vnet_forward(v, st));
 }
 
 }  // namespace

@@ -366,6 +366,10 @@ cudaError_t launch_vnet_fwd_bwd(const VnetLaunch& a, cudaStream_t st);
 // V forward only (CUDA cores, every hidden size): v_out and, with target_out,
 // rewards + gamma (1 - dones) V.
 cudaError_t launch_vnet_forward(const VnetLaunch& a, cudaStream_t st);
+// V forward only on the tensor cores (hidden 64 or 128, S <= 64; one
+// network): packs the weight images into img, then one launch; v_out and,
+// with target_out, rewards + gamma (1 - dones) V.
+cudaError_t launch_vnet_tc_forward(const VnetLaunch& a, uint8_t* img, cudaStream_t st);
 // tensor-core kernel (hidden 128): packed weight images per network
 int64_t vnet_tc_image_bytes();
 bool vnet_tc_supported(const VnetLaunch& a);

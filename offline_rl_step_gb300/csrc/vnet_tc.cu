@@ -537,6 +537,146 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     if (warp == 0) umma::tmem_dealloc(tmem, kTmemCols);
 }
 
+// V forward only on the tensor cores ("GPU IQL + HER Porting Plan", "Rust
+// Integration: gpu_iql_trainer.rs", forward_values, and "IQL modifies the
+// target computation"): per 128-row tile G1 z1 = X W1^T, h1 = relu(z1 + b1)
+// as the image G2 reads, G2 z2 = h1 W2^T, V = relu(z2 + b2) . w3 + b3; with
+// target_out also r + gamma (1 - done) V.  The state tile is built here from
+// the caller's fp32 states (the fused step's relabel is not involved), the
+// weight images come from pack_weights_kernel.  Same warp roles, regions and
+// bounded waits as vnet_tc_kernel; 256 TMEM columns (z1, z2).
+template <int NP>
+__global__ void __launch_bounds__(kThreads, 1) vnet_tc_forward_kernel(const VnetLaunch a,
+                                                                      const uint8_t* __restrict__ wimg) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    TcSmem& sm = *reinterpret_cast<TcSmem*>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool epi = warp != 0;
+    const int q = warp & 3, cg = (warp - 1) >> 2;
+    const int row = 32 * q + lane;
+    const int S = a.state_dim, B = a.batch;
+    const int n_tiles = (B + TM - 1) / TM;
+    const int Hn = a.hidden;
+    const Offsets off = offsets_of(S, Hn);
+    const float* __restrict__ prm = a.params[0];
+    const uint8_t* w1i = wimg;
+    const uint8_t* w2i = w1i + tc::w2_image_offset();
+    constexpr uint32_t kXBytes = (uint32_t)NP * kPlaneX, kW2Bytes = (uint32_t)NP * kPlaneH;
+    constexpr uint32_t kCols = 256;
+
+    if (tid == 0) {
+        umma::mbar_init(&sm.bar_mma, 1);
+        umma::mbar_init(&sm.bar_load, 1);
+        umma::fence_mbar_init();
+    }
+    if (warp == 0) umma::tmem_alloc(&sm.tmem_slot, kCols);
+    pdl_trigger();
+    pdl_wait();
+    for (int i = tid; i < HH; i += kThreads) {
+        const bool u = i < Hn;
+        sm.b1[i] = u ? __ldg(prm + off.b1 + i) : 0.0f;
+        sm.b2[i] = u ? __ldg(prm + off.b2 + i) : 0.0f;
+        sm.w3[i] = u ? __ldg(prm + off.w3 + i) : 0.0f;
+    }
+    const float b3 = __ldg(prm + off.b3);
+    uint32_t ph_mma = 0, ph_load = 0;
+    bool ok = true;
+    auto wait_mma = [&]() {
+        ok &= umma::mbar_wait(&sm.bar_mma, ph_mma, kWaitNs);
+        ph_mma ^= 1u;
+        umma::fence_after_sync();
+    };
+    auto wait_load = [&]() {
+        ok &= umma::mbar_wait(&sm.bar_load, ph_load, kWaitNs);
+        ph_load ^= 1u;
+    };
+
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        const int row0 = tile * TM;
+        // W1 image -> R1 (the previous tile's G2 has finished reading R1)
+        if (tid == 0) {
+            umma::mbar_expect_tx(&sm.bar_load, kXBytes);
+            umma::bulk_g2s(sm.r1, w1i, kXBytes, &sm.bar_load);
+        }
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
+        const uint32_t tmem = sm.tmem_slot;
+        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
+        build_x(sm.r0, NP, a.states, a.stride, row0, B, S);
+        umma::fence_smem_to_async();
+        __syncthreads();
+        wait_load();
+        // ---- G1: z1 = X . W1^T ----
+        if (tid == 0) {
+            umma::fence_after_sync();
+            gemm<NP>(tmem + TM_Z1, sm.r0, kPlaneX, KX, false, sm.r1, kPlaneX, KX, false, KX / 16, HH);
+            umma::commit(&sm.bar_mma);
+        }
+        wait_mma();
+        if (tid == 0) {
+            umma::mbar_expect_tx(&sm.bar_load, kW2Bytes);
+            umma::bulk_g2s(sm.r1, w2i, kW2Bytes, &sm.bar_load);
+        }
+        // ---- epilogue 1: h1 = relu(z1 + b1) -> R0 ----
+        if (epi) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c0 = cg * 32 + cc * 16;
+                float v[16];
+                umma::tmem_ld16(tq + TM_Z1 + (uint32_t)c0, v);
+                umma::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float z = v[j] + sm.b1[c0 + j];
+                    v[j] = z < 0.0f ? 0.0f : z;
+                }
+                store16<NP>(sm.r0, row, c0, v);
+            }
+        }
+        umma::fence_smem_to_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        wait_load();
+        // ---- G2: z2 = h1 . W2^T ----
+        if (tid == 0) {
+            umma::fence_after_sync();
+            gemm<NP>(tmem + TM_Z2, sm.r0, kPlaneH, HH, false, sm.r1, kPlaneH, HH, false, HH / 16, HH);
+            umma::commit(&sm.bar_mma);
+        }
+        wait_mma();
+        // ---- epilogue 2: V (and the target) ----
+        if (epi) {
+            float vp = 0.0f;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c0 = cg * 32 + cc * 16;
+                float v[16];
+                umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, v);
+                umma::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float z = v[j] + sm.b2[c0 + j];
+                    vp = fmaf(z < 0.0f ? 0.0f : z, sm.w3[c0 + j], vp);
+                }
+            }
+            sm.vsum[cg][row] = vp;
+        }
+        __syncthreads();
+        const int b = row0 + row;
+        if (epi && cg == 0 && b < B) {
+            const float V = ((sm.vsum[0][row] + sm.vsum[1][row]) + (sm.vsum[2][row] + sm.vsum[3][row])) + b3;
+            if (a.v_out != nullptr) a.v_out[b] = V;
+            if (a.target_out != nullptr)
+                a.target_out[b] = __ldg(a.rewards + b) + a.gamma * (1.0f - __ldg(a.dones + b)) * V;
+        }
+    }
+    if (!ok && tid == 0) atomicAdd(a.status + OFRL_STAT_TIMEOUT, 1);
+    umma::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) umma::tmem_dealloc(sm.tmem_slot, kCols);
+}
+
 // Pack W1 ([H][S] -> [128 x 64] image) and W2 ([H][H] -> [128 x 128] image)
 // of every network into NP bf16 planes each, units past H zero (standalone V
 // forward/backward; the fused step packs inside the relabel launch).
@@ -597,6 +737,20 @@ cudaError_t launch_np(const VnetLaunch& a, const uint8_t* wimg, cudaStream_t st)
     return launch_pdl(vnet_tc_kernel<NP>, grid, dim3(kThreads), sizeof(TcSmem), st, a, wimg);
 }
 
+template <int NP>
+cudaError_t launch_forward_np(const VnetLaunch& a, const uint8_t* wimg, cudaStream_t st) {
+    static cudaError_t state = cudaErrorNotReady;
+    if (state == cudaErrorNotReady) {
+        auto kern = vnet_tc_forward_kernel<NP>;
+        state = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(TcSmem));
+        if (state == cudaSuccess) state = set_max_shared_carveout(kern);
+    }
+    if (state != cudaSuccess) return state;
+    const int n_tiles = (a.batch + TM - 1) / TM;
+    const dim3 grid((unsigned)vnet_tc_ctas(n_tiles, 1));
+    return launch_pdl(vnet_tc_forward_kernel<NP>, grid, dim3(kThreads), sizeof(TcSmem), st, a, wimg);
+}
+
 }  // namespace
 
 int64_t vnet_tc_image_bytes() { return tc::weight_image_bytes(); }
@@ -623,6 +777,15 @@ cudaError_t launch_vnet_tc_pack(const VnetLaunch& a, uint8_t* img, cudaStream_t 
 cudaError_t launch_vnet_tc(const VnetLaunch& a, const uint8_t* img, cudaStream_t st) {
     if (a.batch <= 0) return cudaSuccess;
     return a.prec == OFRL_PREC_BF16 ? launch_np<1>(a, img, st) : launch_np<3>(a, img, st);
+}
+
+cudaError_t launch_vnet_tc_forward(const VnetLaunch& a, uint8_t* img, cudaStream_t st) {
+    if (a.batch <= 0) return cudaSuccess;
+    VnetLaunch one = a;
+    one.n_nets = 1;
+    cudaError_t e = launch_vnet_tc_pack(one, img, st);
+    if (e != cudaSuccess) return e;
+    return a.prec == OFRL_PREC_BF16 ? launch_forward_np<1>(one, img, st) : launch_forward_np<3>(one, img, st);
 }
 
 }  // namespace ofrl

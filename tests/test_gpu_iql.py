@@ -118,7 +118,7 @@ def test_policy(b, a):
     ctx.close()
 
 
-def _forward_case(s, h, b, prec="fp32", seed=0):
+def _forward_case(s, h, b, prec="fp32", seed=0, path=None):
     import offline_rl_step_gb300 as ofrl
     need_gpu()
     w = dataclasses.replace(synth.PROD, state_dim=s, hidden=h, net_seeds=(seed + 11,))
@@ -130,12 +130,20 @@ def _forward_case(s, h, b, prec="fp32", seed=0):
     r = rng.standard_normal(b).astype(np.float32)
     d = (rng.random(b) < 0.1).astype(np.float32)
     ctx = ofrl.Context(s, h, 5, prec, max_batch=b)
+    if path is not None:
+        ctx.select_vnet_path(path)
+    # forward_values and iql_target run on the tensor cores wherever the
+    # step takes the fused kernel (hidden 64 / 128), else on the CUDA cores
+    want = path or ("tc_fused" if h <= 128 else "tc_layered")
+    assert ctx.vnet_path(1) == want, (h, path)
     return ofrl, ctx, w, params, x, r, d
 
 
-@pytest.mark.parametrize("s,h,b", [(50, 128, 16384), (48, 64, 256), (50, 256, 333), (7, 64, 1), (64, 128, 129)])
-def test_forward_values_fp32(s, h, b):
-    ofrl, ctx, w, params, x, _, _ = _forward_case(s, h, b, seed=s + b)
+@pytest.mark.parametrize("path", [None, "cuda_cores"], ids=["default", "cuda_cores"])
+@pytest.mark.parametrize("s,h,b", [(50, 128, 16384), (50, 128, 65536), (48, 64, 256), (50, 256, 333), (7, 64, 1),
+                                   (64, 128, 129), (50, 128, 1000)])
+def test_forward_values_fp32(s, h, b, path):
+    ofrl, ctx, w, params, x, _, _ = _forward_case(s, h, b, seed=s + b, path=path)
     v = torch.empty(b, device="cuda")
     ofrl.forward_values(ctx, dev(params), dev(x), v)
     torch.cuda.synchronize()
@@ -144,9 +152,10 @@ def test_forward_values_fp32(s, h, b):
     assert within(v.cpu().numpy(), rv, vu, RTOL, ATOL).all(), "V outside tolerance and fp32 bound"
 
 
-@pytest.mark.parametrize("s,h,b", [(50, 128, 16384), (50, 256, 1000)])
-def test_iql_target_fp32(s, h, b):
-    ofrl, ctx, w, params, x, r, d = _forward_case(s, h, b, seed=3 * b)
+@pytest.mark.parametrize("path", [None, "cuda_cores"], ids=["default", "cuda_cores"])
+@pytest.mark.parametrize("s,h,b", [(50, 128, 16384), (50, 256, 1000), (48, 64, 777)])
+def test_iql_target_fp32(s, h, b, path):
+    ofrl, ctx, w, params, x, r, d = _forward_case(s, h, b, seed=3 * b, path=path)
     gamma = 0.99
     t = torch.empty(b, device="cuda")
     vn = torch.empty(b, device="cuda")
@@ -165,8 +174,9 @@ def test_iql_target_fp32(s, h, b):
     assert np.array_equal(tg[term], r[term])
 
 
-def test_forward_values_bf16():
-    ofrl, ctx, w, params, x, _, _ = _forward_case(50, 128, 4096, prec="bf16", seed=5)
+@pytest.mark.parametrize("path", [None, "cuda_cores"], ids=["default", "cuda_cores"])
+def test_forward_values_bf16(path):
+    ofrl, ctx, w, params, x, _, _ = _forward_case(50, 128, 4096, prec="bf16", seed=5, path=path)
     v = torch.empty(4096, device="cuda")
     ofrl.forward_values(ctx, dev(params), dev(x), v)
     torch.cuda.synchronize()
