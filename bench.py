@@ -137,35 +137,72 @@ class Clocks:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def cpu_baseline(w, seconds):
-    """The oracle as it stands, on this host, on a bounded sample of the workload."""
+def _oracle_steps(w, n_steps, seconds, batch=None):
+    """Time up to n_steps oracle steps (stopping after `seconds`) of workload w, or of a row sample of
+    its batch; returns (steps, seconds)."""
     from oracle import step as ostep
+    ws = w if batch is None or batch >= w.batch else synth.scaled(w, batch=batch)
     rep = synth.make_replay(w)
-    cfg = ostep.config_from_workload(w)
+    cfg = ostep.config_from_workload(ws)
     nets = [ostep.NetState.fresh(synth.make_params(w, k), w.taus[k]) for k in range(w.n_nets)]
     k = 0
     t0 = time.perf_counter()
-    while True:
-        q = synth.make_q(w, k)
+    while k < n_steps:
+        q = synth.make_q(ws, k)
         aux = [synth.make_aux(w, k, n) for n in range(w.n_nets)] if w.n_aux else None
         ostep.train_step(cfg, rep, k, q, nets, aux)
         k += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or k >= 50:
+        if time.perf_counter() - t0 >= seconds:
             break
-    return {"value": k * w.batch / el, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{k} full steps (B={w.batch}) of {w.name} in {el:.1f} s, numpy fp64 with its default "
-                      f"BLAS threading; index sampling in single-threaded Python"}
+    return k, time.perf_counter() - t0
+
+
+_SINGLE_CORE = """
+import json, sys
+sys.path.insert(0, {root!r})
+import synth, bench
+w = synth.BY_NAME[{name!r}]
+bench._oracle_steps(w, 1, 1e9)                      # warm-up (imports, first-touch)
+k, el = bench._oracle_steps(w, {steps}, {seconds})
+print(json.dumps([k, el]))
+"""
+
+
+def cpu_baseline(w, seconds):
+    """The oracle as it stands, on this host, on a bounded sample of the workload: whole steps with numpy's
+    default BLAS threading, and (a separate process, one BLAS thread) the first few steps on one core."""
+    k, el = _oracle_steps(w, 50, seconds)
+    out = {"value": k * w.batch / el, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+           "sample": f"{k} full steps (B={w.batch}) of {w.name} in {el:.1f} s, numpy fp64 with its default "
+                     f"BLAS threading; index sampling in single-threaded Python"}
+    env = dict(os.environ)
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = "1"
+    try:
+        r = subprocess.run([sys.executable, "-c", _SINGLE_CORE.format(root=ROOT, name=w.name, steps=5,
+                                                                      seconds=seconds)],
+                           capture_output=True, text=True, env=env, timeout=300)
+        k1, el1 = json.loads(r.stdout.strip().splitlines()[-1])
+        out["single_core"] = {"value": k1 * w.batch / el1, "unit": UNIT, "cores": 1,
+                              "sample": f"{k1} full steps after one warm-up step, one BLAS thread"}
+    except (subprocess.SubprocessError, ValueError, IndexError, OSError):
+        out["single_core"] = None
+    return out
 
 
 def run_reference(args, w):
-    """--impl reference: the CPU oracle (the slow definition) timed on this host."""
+    """--impl reference: the CPU oracle (the slow definition) timed on this host, whole steps of the
+    workload (a row sample of each step's batch only if whole steps would not finish in a few minutes)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     from oracle import step as ostep
-    sample_rows = 2048
-    ws = synth.scaled(w, batch=sample_rows)
+    # one step's cost decides the sample: whole batches when K + W of them fit in about two minutes
+    k1, t1 = _oracle_steps(w, 1, 1e9)
+    rows = w.batch
+    if (args.steps + args.warmup) * t1 > 120.0:
+        rows = max(256, int(w.batch * 120.0 / ((args.steps + args.warmup) * t1)) // 256 * 256)
+    ws = synth.scaled(w, batch=rows) if rows < w.batch else w
     rep = synth.make_replay(w)
     cfg = ostep.config_from_workload(ws)
     nets = [ostep.NetState.fresh(synth.make_params(w, k), w.taus[k]) for k in range(w.n_nets)]
@@ -181,14 +218,14 @@ def run_reference(args, w):
     for k in range(args.steps):
         one(args.warmup + k)
     el = time.perf_counter() - t0
-    value = args.steps * sample_rows / el
-    sample = (f"each step: {sample_rows} rows of the {w.name} batch (full-size replay buffer and V network), "
-              f"numpy fp64 oracle")
+    value = args.steps * rows / el
+    sample = (f"each step: {'the whole' if rows == w.batch else f'{rows} rows of the'} {w.name} batch "
+              f"(B={w.batch}; full-size replay buffer and V network), numpy fp64 oracle")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "batch": sample_rows, "hidden": w.hidden, "state_dim": w.state_dim},
+        "config": {"workload": w.name, "batch": rows, "hidden": w.hidden, "state_dim": w.state_dim},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
