@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--repeats", type=int, default=5, help="timed regions of --steps steps; the median is reported")
     ap.add_argument("--no-workloads", action="store_true", help="skip the per-workload table of the other configs")
     ap.add_argument("--no-forward", action="store_true", help="skip the IQL-target (V forward) measurement")
+    ap.add_argument("--vnet-path", default=None, choices=("tc_fused", "tc_layered", "cuda_cores"),
+                    help="V forward/backward implementation (default: the library's choice for the shape)")
     return ap.parse_args()
 
 
@@ -263,7 +265,7 @@ class Run:
     """One workload set up on the GPU: replay buffer, context, networks, a pre-marshalled step, and every
     step's Q (device and pinned host) and auxiliary sources resident before any timing."""
 
-    def __init__(self, w, rank, steps, warmup):
+    def __init__(self, w, rank, steps, warmup, vnet_path=None):
         import torch
 
         import offline_rl_step_gb300 as ofrl
@@ -277,6 +279,8 @@ class Run:
         del rep
         self.her = ofrl.HerConfig(w.batch, w.her_count, w.strategy, w.goal_threshold, w.seed + rank)
         self.ctx = ofrl.Context(w.state_dim, w.hidden, w.num_actions, w.prec, max_batch=w.batch, max_nets=w.n_nets)
+        if vnet_path is not None:
+            self.ctx.select_vnet_path(vnet_path)
         self.nets = [ofrl.VNet.from_params(torch.from_numpy(synth.make_params(w, k)), w.taus[k])
                      for k in range(w.n_nets)]
         self.opt = ofrl.Opt(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
@@ -444,7 +448,7 @@ def run_ours(args, w):
     torch.cuda.set_device(local)
     pk, pk_kind = peaks()
 
-    run = Run(w, rank, args.steps, args.warmup)
+    run = Run(w, rank, args.steps, args.warmup, args.vnet_path)
     run.warm()
 
     # ---- timed regions: R regions of K steps each (device Q), each followed

@@ -113,18 +113,36 @@ __device__ __forceinline__ void store16(uint8_t* img, int r, int c0, const float
 
 // Build the X image ([128 x 64]) of a tile from the fp32 batch (used when the
 // relabel kernel did not write images): rows past the batch, columns past S
-// are zero.
+// are zero.  PREFETCH: every thread's loads are issued before any of them is
+// split and stored, so the tile costs one round of memory latency (the
+// forward-only kernel; the training kernel keeps the loop, whose registers
+// it cannot spare).
+template <bool PREFETCH = false>
 __device__ __forceinline__ void build_x(uint8_t* img, int np, const float* __restrict__ states, int stride, int row0,
                                         int B, int S) {
-    for (int e = threadIdx.x; e < TM * (KX / 4); e += kThreads) {
-        const int r = e / (KX / 4), c = 4 * (e % (KX / 4));
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (row0 + r < B && c < S) v = __ldg(reinterpret_cast<const float4*>(states + (int64_t)(row0 + r) * stride + c));
-        float x[4] = {v.x, v.y, v.z, v.w};
+    constexpr int kChunks = TM * (KX / 4);                      // float4 chunks of the tile
+    constexpr int kPer = PREFETCH ? (kChunks + kThreads - 1) / kThreads : 1;
+    for (int e0 = threadIdx.x; e0 < kChunks; e0 += kPer * kThreads) {
+        float4 v[kPer];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (c + j >= S) x[j] = row0 + r < B && tc::ones_column(c + j, S) ? 1.0f : 0.0f;
-        tc::put4(img, kPlaneX, np, KX, r, c, x);
+        for (int i = 0; i < kPer; ++i) {
+            const int e = e0 + i * kThreads;
+            const int r = e / (KX / 4), c = 4 * (e % (KX / 4));
+            v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e < kChunks && row0 + r < B && c < S)
+                v[i] = __ldg(reinterpret_cast<const float4*>(states + (int64_t)(row0 + r) * stride + c));
+        }
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int e = e0 + i * kThreads;
+            if (e >= kChunks) break;
+            const int r = e / (KX / 4), c = 4 * (e % (KX / 4));
+            float x[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (c + j >= S) x[j] = row0 + r < B && tc::ones_column(c + j, S) ? 1.0f : 0.0f;
+            tc::put4(img, kPlaneX, np, KX, r, c, x);
+        }
     }
 }
 
@@ -603,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_forward_kernel(const Vnet
         umma::fence_after_sync();
         const uint32_t tmem = sm.tmem_slot;
         const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
-        build_x(sm.r0, NP, a.states, a.stride, row0, B, S);
+        build_x<true>(sm.r0, NP, a.states, a.stride, row0, B, S);
         umma::fence_smem_to_async();
         __syncthreads();
         wait_load();
