@@ -42,7 +42,7 @@ KERNEL_SOURCES = {
 # the kernel sources the capture ran (source_hash)
 NCU_TRAFFIC = {
     # profiles/vnet_tc_prod_fp32_B16384_H128.md (ncu --set full, one launch)
-    ("vnet_tc (tcgen05)", "prod_fp32_B16384_S50_H128_A5"): ("ddecdde7b6214ef9", 6934272),
+    ("vnet_tc (tcgen05)", "prod_fp32_B16384_S50_H128_A5"): ("17deacc019223ee6", 6934528),
 }
 
 
