@@ -42,7 +42,7 @@ KERNEL_SOURCES = {
 # the kernel sources the capture ran (source_hash)
 NCU_TRAFFIC = {
     # profiles/vnet_tc_prod_fp32_B16384_H128.md (ncu --set full, one launch)
-    ("vnet_tc (tcgen05)", "prod_fp32_B16384_S50_H128_A5"): ("17deacc019223ee6", 6934528),
+    ("vnet_tc (tcgen05)", "prod_fp32_B16384_S50_H128_A5"): ("4d1e1cbc730aaf80", 6932992),
 }
 
 
@@ -385,12 +385,16 @@ def roofline(w, phase_avg, path, region_s, pk, pk_kind):
         # tensor-core kernels: bf16 MMAs (three-term split, six products per
         # K-step, for fp32 workloads); algorithmic flops over the bf16 peak
         ach = alg["vnet_flops"] / dur_s / 1e12
-        # MMA work as executed: 128-row tiles, S padded to 64, five GEMMs,
-        # one product per K-step (bf16) or six (fp32 through the split)
-        prods = 1 if w.prec == "bf16" else 6
+        # MMA work as executed: 128-row tiles, S padded to 64, five GEMMs;
+        # one product per K-step (bf16), or through the fp32 split six for
+        # z1, z2, dh1 (K = S, H) and three for the weight gradients dW1, dW2
+        # (K = batch rows)
         tiles = -(-w.batch // 128)
         hp = max(w.hidden, 128)   # hidden 64 runs zero-padded to 128 units on the fused kernel
-        mma = w.n_nets * tiles * prods * 2 * 128 * (2 * hp * 64 + 3 * hp ** 2)
+        fwd = hp * 64 + 2 * hp ** 2          # z1, z2, dh1 per row
+        wgr = hp * 64 + hp ** 2              # dW1, dW2 per row
+        per_row = fwd + wgr if w.prec == "bf16" else 6 * fwd + 3 * wgr
+        mma = w.n_nets * tiles * 128 * 2 * per_row
         kname = "vnet_tc (tcgen05)" if path == "tc_fused" else "vnet_wide fwd + wgrad (tcgen05, TMA)"
         entry = NCU_TRAFFIC.get((kname, w.name))
         traffic = None

@@ -19,10 +19,17 @@
 // operand of one GEMM and the MN-major operand of another.
 //
 // Precision: for fp32 results every operand is split into three bf16 terms
-// x = x0 + x1 + x2 (24 significand bits) and each K-step issues the six
-// products down to 2^-16 of the leading one (x2 y0, x1 y1, x0 y2, x1 y0,
-// x0 y1, x0 y0); the rest lie below fp32 rounding.  The bf16 workload has one
-// term and one product.
+// x = x0 + x1 + x2 (24 significand bits).  The GEMMs whose K is a hidden or
+// state dimension (G1, G2, G4) issue per K-step the six products down to
+// 2^-16 of the leading one (x2 y0, x1 y1, x0 y2, x1 y0, x0 y1, x0 y0); the
+// rest lie below fp32 rounding.  The weight-gradient GEMMs (G3, G5), whose K
+// runs over the batch rows, issue the three leading ones (x1 y0, x0 y1,
+// x0 y0): with |x2| <= 2^-18 |x| each product is then off by at most 3.1 *
+// 2^-18 of itself, at random, which over a sum of n rows adds about sqrt(n)
+// 3.1 2^-18 rms(terms), against an fp32 summation error of order sqrt(n)
+// 2^-24 times the sum of |terms|, about n / 200 times larger (comparable
+// within one 128-row tile, 80 times larger over a 16,384-row batch).  The
+// bf16 workload has one term and one product.
 //
 // Shared memory: two 96 KB regions reused through the step:
 //   R0: X image -> h1 -> W2 image (for G4) -> dz1
@@ -72,18 +79,21 @@ __device__ __forceinline__ uint64_t desc_mn(const uint8_t* plane, int C, int ks)
 
 // Issue one GEMM (all K-steps, all split terms) from one thread.
 // accumulate: add to what D holds (else the first product overwrites it).
-template <int NP>
+// LEADING: only the three leading products of the split (the batch-row
+// weight-gradient GEMMs; see the precision note above).
+template <int NP, bool LEADING = false>
 __device__ __forceinline__ void gemm(uint32_t d_tmem, const uint8_t* a, uint32_t a_plane, int a_cols, bool a_mn,
                                      const uint8_t* b, uint32_t b_plane, int b_cols, bool b_mn, int ksteps, int n,
                                      bool accumulate = false) {
     const uint32_t idesc = umma::instr_desc(umma::kTypeBF16, a_mn, b_mn, TM, n);
+    constexpr int t0 = NP == 3 && LEADING ? 3 : 0;
     constexpr int nt = NP == 3 ? 6 : 1;
     constexpr int ta[6] = {2, 1, 0, 1, 0, 0};   // smallest products first
     constexpr int tb[6] = {0, 1, 2, 0, 1, 0};
     uint32_t acc = accumulate ? 1u : 0u;
     for (int ks = 0; ks < ksteps; ++ks) {
 #pragma unroll
-        for (int t = 0; t < nt; ++t) {
+        for (int t = t0; t < nt; ++t) {
             const uint8_t* ap = a + (uint32_t)(NP == 3 ? ta[t] : 0) * a_plane;
             const uint8_t* bp = b + (uint32_t)(NP == 3 ? tb[t] : 0) * b_plane;
             const uint64_t ad = a_mn ? desc_mn(ap, a_cols, ks) : desc_k(ap, a_cols, ks);
@@ -355,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         // ---- G3: dW2 = dz2^T . h1 ----
         if (tid == 0) {
             umma::fence_after_sync();
-            gemm<NP>(tmem + TM_DW2, sm.r1, kPlaneH, HH, true, sm.r0, kPlaneH, HH, true, TM / 16, HH, it > 0);
+            gemm<NP, true>(tmem + TM_DW2, sm.r1, kPlaneH, HH, true, sm.r0, kPlaneH, HH, true, TM / 16, HH, it > 0);
             umma::commit(&sm.bar_mma);
         }
         if (epi && cg == 0) {
@@ -477,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         // ---- G5: dW1 = dz1^T . X ----
         if (tid == 0) {
             umma::fence_after_sync();
-            gemm<NP>(tmem + TM_DW1, sm.r0, kPlaneH, HH, true, sm.r1, kPlaneX, KX, true, TM / 16, KX, it > 0);
+            gemm<NP, true>(tmem + TM_DW1, sm.r0, kPlaneH, HH, true, sm.r1, kPlaneX, KX, true, TM / 16, KX, it > 0);
             umma::commit(&sm.bar_mma);
         }
         // db1: with S < 64 G5 yields it in its last column (the ones column of

@@ -29,7 +29,8 @@
 // K-major chunks (all 128 rows x 16 columns) or MN-major chunks (16 rows x
 // some or all columns), so the image written once serves both kinds of GEMM.
 // fp32 precision as in the fused kernel: three bf16 planes per operand and
-// six products per K-step; the bf16 workload has one plane and one product.
+// six products per K-step (the weight-gradient kernel, whose K is the batch,
+// the three leading ones); the bf16 workload has one plane and one product.
 
 #include <cuda.h>
 
@@ -562,6 +563,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
 
     if (tid == 0) {
+        // weight gradients (K = batch rows): the three leading products of
+        // the split (terms 3..5; the fused kernel's G3 / G5 note has why)
+        constexpr int t0_ = NP == 3 ? 3 : 0;
         constexpr int nt_ = NP == 3 ? 6 : 1;
         const uint32_t id2 = umma::instr_desc(umma::kTypeBF16, true, true, TM, H);
         const uint32_t id1 = umma::instr_desc(umma::kTypeBF16, true, true, TM, KX);
@@ -572,9 +576,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::fence_after_sync();
             const uint8_t* st = sm.ring + s * G::kStageB;
 #pragma unroll
-            for (int t = 0; t < nt_; ++t) {
+            for (int t = t0_; t < nt_; ++t) {
                 const int ta = NP == 3 ? term_a(t) : 0, tb = NP == 3 ? term_b(t) : 0;
-                const uint32_t acc = (i > 0 || t > 0) ? 1u : 0u;
+                const uint32_t acc = (i > 0 || t > t0_) ? 1u : 0u;
                 // MN-major chunks: [plane][2 row groups][chunks]: LBO = one row group, SBO = 128
                 const uint64_t a2 = desc(st + (uint32_t)ta * G::kPlaneHalf, 16u * 128u, 128u);
                 const uint64_t b2 = desc(st + G::kOffB2 + (uint32_t)tb * G::kPlaneN, (uint32_t)(H / 8) * 128u, 128u);

@@ -16,7 +16,13 @@ difference between the two sides' weights (zero on the first step):
     is inside it;
   * ReLU masks: where |z| is inside z's own uncertainty, 1[z > 0] = 0 and 1
     are both fp32-correct; the contribution of every such entry is added in
-    full.
+    full;
+  * split products: the tensor-core kernels form fp32 products from a
+    three-term bf16 split (x = x0 + x1 + x2 with |x - x0| <= 2^-9 |x|, so
+    |x1| <= 2^-9 |x| and |x2| <= 2^-18 |x|), and their weight-gradient GEMMs
+    (K = batch rows) take only the three leading products x1 y0 + x0 y1 +
+    x0 y0: the dropped x2 y0 + x1 y1 + x0 y2 (and smaller) are within
+    SPLIT_REL = 3.1 * 2^-18 of |x y|, added linearly to dW1, db1 and dW2.
 
 The tests accept a CUDA value inside the benchmark spec's tolerance or inside
 this bound; a CPU test checks that an independent fp32 evaluation stays
@@ -29,6 +35,7 @@ from oracle.precision import bf16
 
 U = 2.0 ** -24
 LAM = 8.0
+SPLIT_REL = 3.1 * 2.0 ** -18
 
 
 def _rnd(abs_sum, n):
@@ -123,9 +130,9 @@ def value_uncertainty(flat, x, qt, tau, state_dim, hidden, batch=None, dparams=N
     one = np.ones((x.shape[0], 1))
     zero1 = np.zeros((x.shape[0], 1))
     zx = np.zeros_like(ax)
-    u_w1 = bsum(adz1, dz1r, dz1s, ax, zx, zx)
-    u_b1 = bsum(adz1, dz1r, dz1s, one, zero1, zero1)[:, 0]
-    u_w2 = bsum(adz2, dz2r, dz2s, np.abs(h1), h1r, h1s)
+    u_w1 = bsum(adz1, dz1r, dz1s, ax, zx, zx) + SPLIT_REL * (adz1.T @ ax)
+    u_b1 = bsum(adz1, dz1r, dz1s, one, zero1, zero1)[:, 0] + SPLIT_REL * adz1.sum(axis=0)
+    u_w2 = bsum(adz2, dz2r, dz2s, np.abs(h1), h1r, h1s) + SPLIT_REL * (adz2.T @ np.abs(h1))
     u_b2 = bsum(adz2, dz2r, dz2s, one, zero1, zero1)[:, 0]
     u_w3 = bsum(adv[:, None], dvr[:, None], dvs[:, None], np.abs(h2), h2r, h2s)
     u_b3 = bsum(adv[:, None], dvr[:, None], dvs[:, None], one, zero1, zero1)[:, 0]
