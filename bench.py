@@ -42,7 +42,7 @@ KERNEL_SOURCES = {
 # the kernel sources the capture ran (source_hash)
 NCU_TRAFFIC = {
     # profiles/vnet_tc_prod_fp32_B16384_H128.md (ncu --set full, one launch)
-    ("vnet_tc (tcgen05)", "prod_fp32_B16384_S50_H128_A5"): ("4d1e1cbc730aaf80", 6932992),
+    ("vnet_tc (tcgen05)", "prod_fp32_B16384_S50_H128_A5"): ("826d7c19df437fb9", 6921728),
 }
 
 
@@ -387,13 +387,19 @@ def roofline(w, phase_avg, path, region_s, pk, pk_kind):
         ach = alg["vnet_flops"] / dur_s / 1e12
         # MMA work as executed: 128-row tiles, S padded to 64, five GEMMs;
         # one product per K-step (bf16), or through the fp32 split six for
-        # z1, z2, dh1 (K = S, H) and three for the weight gradients dW1, dW2
-        # (K = batch rows)
+        # the forward z1, z2 and three for the backward GEMMs (fused: dh1,
+        # dW2, dW1; layered: dW2, dW1, its dh1 six)
         tiles = -(-w.batch // 128)
         hp = max(w.hidden, 128)   # hidden 64 runs zero-padded to 128 units on the fused kernel
-        fwd = hp * 64 + 2 * hp ** 2          # z1, z2, dh1 per row
+        fwd = hp * 64 + hp ** 2              # z1, z2 per row
+        dh1 = hp ** 2
         wgr = hp * 64 + hp ** 2              # dW1, dW2 per row
-        per_row = fwd + wgr if w.prec == "bf16" else 6 * fwd + 3 * wgr
+        if w.prec == "bf16":
+            per_row = fwd + dh1 + wgr
+        elif path == "tc_fused":
+            per_row = 6 * fwd + 3 * (dh1 + wgr)
+        else:
+            per_row = 6 * (fwd + dh1) + 3 * wgr
         mma = w.n_nets * tiles * 128 * 2 * per_row
         kname = "vnet_tc (tcgen05)" if path == "tc_fused" else "vnet_wide fwd + wgrad (tcgen05, TMA)"
         entry = NCU_TRAFFIC.get((kname, w.name))

@@ -62,6 +62,15 @@ __device__ __forceinline__ void split3x2(float a, float b, uint32_t& p0, uint32_
     p2 = pack_bf16x2(a, b);
 }
 
+// The first two of those terms only (x0 + x1: 16 significand bits), for
+// operands that only the three leading products read.
+__device__ __forceinline__ void split2x2(float a, float b, uint32_t& p0, uint32_t& p1) {
+    p0 = pack_bf16x2(a, b);
+    a -= bf16_lo(p0);
+    b -= bf16_hi(p0);
+    p1 = pack_bf16x2(a, b);
+}
+
 // Write 4 consecutive values of row r, columns c..c+3 (c a multiple of 4)
 // into an image with C columns and np planes of `plane` bytes.
 __device__ __forceinline__ void put4(uint8_t* img, uint32_t plane, int np, int C, int r, int c, const float (&x)[4]) {

@@ -19,17 +19,19 @@
 // operand of one GEMM and the MN-major operand of another.
 //
 // Precision: for fp32 results every operand is split into three bf16 terms
-// x = x0 + x1 + x2 (24 significand bits).  The GEMMs whose K is a hidden or
-// state dimension (G1, G2, G4) issue per K-step the six products down to
-// 2^-16 of the leading one (x2 y0, x1 y1, x0 y2, x1 y0, x0 y1, x0 y0); the
-// rest lie below fp32 rounding.  The weight-gradient GEMMs (G3, G5), whose K
-// runs over the batch rows, issue the three leading ones (x1 y0, x0 y1,
-// x0 y0): with |x2| <= 2^-18 |x| each product is then off by at most 3.1 *
-// 2^-18 of itself, at random, which over a sum of n rows adds about sqrt(n)
-// 3.1 2^-18 rms(terms), against an fp32 summation error of order sqrt(n)
-// 2^-24 times the sum of |terms|, about n / 200 times larger (comparable
-// within one 128-row tile, 80 times larger over a 16,384-row batch).  The
-// bf16 workload has one term and one product.
+// x = x0 + x1 + x2 (24 significand bits).  The forward GEMMs (G1, G2) issue
+// per K-step the six products down to 2^-16 of the leading one (x2 y0,
+// x1 y1, x0 y2, x1 y0, x0 y1, x0 y0); the rest lie below fp32 rounding.  The
+// backward GEMMs issue the three leading ones (x1 y0, x0 y1, x0 y0): with
+// |x2| <= 2^-18 |x| each product is then off by at most 3.1 * 2^-18 of
+// itself, at random.  In the weight-gradient GEMMs (G3, G5), whose K runs
+// over the batch rows, that adds about sqrt(n) 3.1 2^-18 rms(terms) to a sum
+// of n rows, against an fp32 summation error of order sqrt(n) 2^-24 times
+// the sum of |terms|, about n / 200 times larger (comparable within one
+// 128-row tile, 80 times larger over a 16,384-row batch).  G4's dh1 feeds
+// only those sums (its ReLU mask comes from the forward z1, which keeps full
+// precision, so no mask decision moves).  The bf16 workload has one term and
+// one product.
 //
 // Shared memory: two 96 KB regions reused through the step:
 //   R0: X image -> h1 -> W2 image (for G4) -> dz1
@@ -105,17 +107,21 @@ __device__ __forceinline__ void gemm(uint32_t d_tmem, const uint8_t* a, uint32_t
 }
 
 // Store 16 fp32 values of row r, columns c0..c0+15 into a [128 x 128] image.
-template <int NP>
+// LEADING: only the two planes the three leading products read (dz2, dz1:
+// operands of the backward GEMMs alone); plane 2 is left as it was.
+template <int NP, bool LEADING = false>
 __device__ __forceinline__ void store16(uint8_t* img, int r, int c0, const float (&v)[16]) {
+    constexpr int NW = NP == 3 && LEADING ? 2 : NP;   // planes written
     uint32_t t[NP][8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        if constexpr (NP == 3) tc::split3x2(v[2 * j], v[2 * j + 1], t[0][j], t[1][j], t[2][j]);
+        if constexpr (NP == 3 && LEADING) tc::split2x2(v[2 * j], v[2 * j + 1], t[0][j], t[1][j]);
+        else if constexpr (NP == 3) tc::split3x2(v[2 * j], v[2 * j + 1], t[0][j], t[1][j], t[2][j]);
         else t[0][j] = tc::pack_bf16x2(v[2 * j], v[2 * j + 1]);
     }
     const uint32_t o0 = tc::img_off(r, c0, HH), o1 = tc::img_off(r, c0 + 8, HH);
 #pragma unroll
-    for (int p = 0; p < NP; ++p) {
+    for (int p = 0; p < NW; ++p) {
         *reinterpret_cast<uint4*>(img + (uint32_t)p * kPlaneH + o0) = make_uint4(t[p][0], t[p][1], t[p][2], t[p][3]);
         *reinterpret_cast<uint4*>(img + (uint32_t)p * kPlaneH + o1) = make_uint4(t[p][4], t[p][5], t[p][6], t[p][7]);
     }
@@ -356,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
                     const float z = g[j] + sm.b2[c0 + j];
                     g[j] = z > 0.0f ? dv * sm.w3[c0 + j] : 0.0f;
                 }
-                store16<NP>(sm.r1, row, c0, g);
+                store16<NP, true>(sm.r1, row, c0, g);
             }
         }
         umma::fence_smem_to_async();
@@ -420,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         // ---- G4: dh1 = dz2 . W2 ----
         if (tid == 0) {
             umma::fence_after_sync();
-            gemm<NP>(tmem + TM_Z1, sm.r1, kPlaneH, HH, false, sm.r0, kPlaneH, HH, true, HH / 16, HH);
+            gemm<NP, true>(tmem + TM_Z1, sm.r1, kPlaneH, HH, false, sm.r0, kPlaneH, HH, true, HH / 16, HH);
             umma::commit(&sm.bar_mma);
         }
         // the policy while G4 runs: four threads per row (lanes 4r .. 4r + 3 of
@@ -476,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
                 umma::tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] = ((mask1 >> (cc * 16 + j)) & 1u) ? v[j] : 0.0f;
-                store16<NP>(sm.r0, row, c0, v);
+                store16<NP, true>(sm.r0, row, c0, v);
             }
         }
         if (!xi) build_x(sm.r1, NP, a.states, a.stride, row0, B, S);
