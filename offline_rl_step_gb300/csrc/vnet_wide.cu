@@ -29,8 +29,10 @@
 // K-major chunks (all 128 rows x 16 columns) or MN-major chunks (16 rows x
 // some or all columns), so the image written once serves both kinds of GEMM.
 // fp32 precision as in the fused kernel: three bf16 planes per operand and
-// six products per K-step (the weight-gradient kernel, whose K is the batch,
-// the three leading ones); the bf16 workload has one plane and one product.
+// six products per K-step; the weight-gradient kernel, whose K is the batch,
+// issues the three leading ones, so it loads the two planes they read, and
+// the dz1 image, which only that kernel reads, is written in two; the bf16
+// workload has one plane and one product.
 
 #include <cuda.h>
 
@@ -68,10 +70,13 @@ struct Geo {
     static constexpr uint32_t kStageA = kBytesA + kBytesB;
     static constexpr uint32_t kPlaneX = TM * KX * 2, kPlaneW1 = H * KX * 2;
     static constexpr uint32_t kXBytes = NP * kPlaneX, kW1Bytes = NP * kPlaneW1;
-    // kernel B: dz2 half, h1, dz1 half, X (16 rows each)
+    // kernel B: dz2 half, h1, dz1 half, X (16 rows each), the planes its
+    // three leading products read (two of three)
+    static constexpr int kNPB = NP == 3 ? 2 : 1;
     static constexpr uint32_t kPlaneHalf = 16 * 128 * 2, kPlaneN = 16 * H * 2, kPlaneXK = 16 * KX * 2;
-    static constexpr uint32_t kOffB2 = NP * kPlaneHalf, kOffA1 = kOffB2 + NP * kPlaneN, kOffB1 = kOffA1 + NP * kPlaneHalf;
-    static constexpr uint32_t kStageB = kOffB1 + NP * kPlaneXK;
+    static constexpr uint32_t kOffB2 = kNPB * kPlaneHalf, kOffA1 = kOffB2 + kNPB * kPlaneN,
+                              kOffB1 = kOffA1 + kNPB * kPlaneHalf;
+    static constexpr uint32_t kStageB = kOffB1 + kNPB * kPlaneXK;
     static constexpr uint32_t kActPlane = TM * H * 2;        // one plane of a tile image
     static constexpr int kStride2 = H + 4;                   // staged dW2 rows (floats)
     // the stage rings, also holding kernel A's X and W1 images at the start
@@ -136,18 +141,20 @@ __host__ __device__ constexpr int term_b(int t) { return t == 2 ? 2 : (t == 1 ||
 
 // Store 16 fp32 values of row r, columns c0..c0+15 into a global tile image
 // with C columns (NP planes of `plane` bytes).
-template <int NP>
+template <int NP, bool LEADING = false>
 __device__ __forceinline__ void store16_global(uint8_t* img, uint32_t plane, int C, int r, int c0,
                                                const float (&v)[16], uint64_t pol) {
+    constexpr int NW = NP == 3 && LEADING ? 2 : NP;
     uint32_t t[NP][8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        if constexpr (NP == 3) tc::split3x2(v[2 * j], v[2 * j + 1], t[0][j], t[1][j], t[2][j]);
+        if constexpr (NP == 3 && LEADING) tc::split2x2(v[2 * j], v[2 * j + 1], t[0][j], t[1][j]);
+        else if constexpr (NP == 3) tc::split3x2(v[2 * j], v[2 * j + 1], t[0][j], t[1][j], t[2][j]);
         else t[0][j] = tc::pack_bf16x2(v[2 * j], v[2 * j + 1]);
     }
     const uint32_t o0 = tc::img_off(r, c0, C), o1 = tc::img_off(r, c0 + 8, C);
 #pragma unroll
-    for (int p = 0; p < NP; ++p) {
+    for (int p = 0; p < NW; ++p) {
         umma::st16_hint(img + (uint32_t)p * plane + o0, make_uint4(t[p][0], t[p][1], t[p][2], t[p][3]), pol);
         umma::st16_hint(img + (uint32_t)p * plane + o1, make_uint4(t[p][4], t[p][5], t[p][6], t[p][7]), pol);
     }
@@ -498,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = ((mask1 >> (16 * p + j)) & 1ull) ? v[j] : 0.0f;
-            store16_global<NP>(dz1g, G::kActPlane, H, row, c0, v, keep);
+            store16_global<NP, true>(dz1g, G::kActPlane, H, row, c0, v, keep);
         }
         umma::fence_global_to_async();
     }
@@ -795,8 +802,10 @@ cudaError_t vnet_wide_maps(WideMaps* m, int hidden, int planes, int n_nets, int 
     const cuuint64_t adim[5] = {64, H / 8, TM / 8, NP, (cuuint64_t)n_nets * act_tiles};
     const cuuint64_t astr[4] = {128, 16 * H, plane, NP * plane};
     const cuuint32_t kbox[5] = {64, 2, TM / 8, (cuuint32_t)NP, 1};
-    const cuuint32_t hbox[5] = {64, 16, 2, (cuuint32_t)NP, 1};
-    const cuuint32_t nbox[5] = {64, (cuuint32_t)(H / 8), 2, (cuuint32_t)NP, 1};
+    // kernel B's boxes take the planes its three leading products read
+    const cuuint32_t npb = NP == 3 ? 2 : (cuuint32_t)NP;
+    const cuuint32_t hbox[5] = {64, 16, 2, npb, 1};
+    const cuuint32_t nbox[5] = {64, (cuuint32_t)(H / 8), 2, npb, 1};
     cudaError_t e = encode5(&m->h1k, act[0], adim, astr, kbox);
     if (e == cudaSuccess) e = encode5(&m->dz2k, act[1], adim, astr, kbox);
     if (e == cudaSuccess) e = encode5(&m->dz2h, act[1], adim, astr, hbox);
@@ -805,7 +814,7 @@ cudaError_t vnet_wide_maps(WideMaps* m, int hidden, int planes, int n_nets, int 
     // state-tile images: [tile][plane][128 x 64]
     const cuuint64_t xdim[5] = {64, KX / 8, TM / 8, NP, (cuuint64_t)x_tiles};
     const cuuint64_t xstr[4] = {128, (KX / 8) * 128, tc::kPlaneX, NP * tc::kPlaneX};
-    const cuuint32_t xbox[5] = {64, KX / 8, 2, (cuuint32_t)NP, 1};
+    const cuuint32_t xbox[5] = {64, KX / 8, 2, npb, 1};
     if (e == cudaSuccess) e = encode5(&m->xk, ximg, xdim, xstr, xbox);
     // W2 images: (core matrix, chunk, row group, plane, network)
     const cuuint64_t wdim[5] = {64, H / 8, H / 8, NP, (cuuint64_t)n_nets};
