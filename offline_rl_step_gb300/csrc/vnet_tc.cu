@@ -43,6 +43,8 @@
 // reads TMEM lane quarter w % 4 (tile rows, or hidden units for the weight
 // gradients) and column group (w - 1) / 4 (32 columns).
 
+#include <cstddef>
+
 #include "common.cuh"
 #include "tc_image.cuh"
 #include "umma.cuh"
@@ -165,19 +167,22 @@ __device__ __forceinline__ void build_x(uint8_t* img, int np, const float* __res
 struct TcSmem {
     uint8_t r0[kRegion];
     uint8_t r1[kRegion];
-    float b1[HH], b2[HH], w3[HH];
+    __align__(16) float b1[HH];
+    __align__(16) float b2[HH];
+    float w3[HH];                     // right after b2: one copy brings both
     float vsum[4][TM];
     float red[3][kEpiWarps][32];   // per epilogue warp column sums: dW3, db2, db1
     float lred[2][4];           // per lane-quarter warp of column group 0: loss, db3
     __align__(16) float vec[3][HH];   // this CTA's dW3, db2, db1 over its tiles
-    float qt[TM * kMaxActions];       // the tile's Q rows [row][action] (or q_taken [row])
-    int32_t act[TM];                  // the tile's actions
+    __align__(16) float qt[TM * kMaxActions];   // the tile's Q rows [row][action] (or q_taken [row])
+    __align__(16) int32_t act[TM];              // the tile's actions
     float vrow[TM];                   // V of each row
     float vb3;                  // this CTA's db3 over its tiles
     uint64_t bar_mma, bar_load;
     uint32_t tmem_slot;
 };
 static_assert(sizeof(TcSmem) <= 227 * 1024, "tensor-core kernel shared memory above the per-CTA limit");
+static_assert(offsetof(TcSmem, w3) == offsetof(TcSmem, b2) + HH * sizeof(float), "w3 follows b2");
 
 template <int NP>
 __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a, const uint8_t* __restrict__ wimg) {
@@ -207,11 +212,17 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     if (warp == 0) umma::tmem_alloc(&sm.tmem_slot, kTmemCols);
     pdl_trigger();
     pdl_wait();
+    // b1, b2 and w3 arrive by bulk copies with the first tile's images (one
+    // round of latency for everything the tile needs) when H = 128 and the
+    // parameters are 16-byte aligned; else (zero-padded units) loaded here
+    const bool bulk_bias = Hn == HH && (reinterpret_cast<uintptr_t>(prm) & 15) == 0;
     for (int i = tid; i < HH; i += kThreads) {
-        const bool u = i < Hn;   // padded units: zero bias and output weight, so they stay zero
-        sm.b1[i] = u ? __ldg(prm + off.b1 + i) : 0.0f;
-        sm.b2[i] = u ? __ldg(prm + off.b2 + i) : 0.0f;
-        sm.w3[i] = u ? __ldg(prm + off.w3 + i) : 0.0f;
+        if (!bulk_bias) {
+            const bool u = i < Hn;   // padded units: zero bias and output weight, so they stay zero
+            sm.b1[i] = u ? __ldg(prm + off.b1 + i) : 0.0f;
+            sm.b2[i] = u ? __ldg(prm + off.b2 + i) : 0.0f;
+            sm.w3[i] = u ? __ldg(prm + off.w3 + i) : 0.0f;
+        }
         sm.vec[0][i] = sm.vec[1][i] = sm.vec[2][i] = 0.0f;
     }
     if (tid == 0) sm.vb3 = 0.0f;
@@ -235,22 +246,38 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     for (int tile = blockIdx.x, it = 0; tile < n_tiles; tile += gridDim.x, ++it) {
         const int row0 = tile * TM;
         const uint8_t* xi = a.ximg != nullptr ? a.ximg + (int64_t)tile * NP * kPlaneX : nullptr;
-        // ---- stage 1: X image -> R0, W1 image -> R1 (issued first; the loads
-        // below overlap it; the previous tile's G5 has finished reading them) ----
+        // ---- stage 1: X image -> R0, W1 image -> R1, and the tile's Q rows
+        // and actions (one contiguous block each) for the loss and the policy,
+        // all by bulk copies on one barrier (the previous tile's G5 has
+        // finished reading R0 and R1); Q and the actions by loads where a
+        // copy's address or size is not a multiple of 16 bytes ----
+        const int nrow = B - row0 < TM ? B - row0 : TM;
+        const float* qsrc = a.q != nullptr ? a.q + (int64_t)row0 * NA : a.q_taken + row0;
+        const uint32_t qbytes = (uint32_t)(nrow * (a.q != nullptr ? NA : 1)) * 4u;
+        const bool bulk_q = (nrow & 3) == 0 && (reinterpret_cast<uintptr_t>(qsrc) & 15) == 0 &&
+                            (a.q == nullptr || (reinterpret_cast<uintptr_t>(a.actions + row0) & 15) == 0);
         if (tid == 0) {
-            umma::mbar_expect_tx(&sm.bar_load, (xi ? kXBytes : 0u) + kXBytes);
+            uint32_t bytes = (xi ? kXBytes : 0u) + kXBytes;
+            if (it == 0 && bulk_bias) bytes += 3u * HH * 4u;
+            if (bulk_q) bytes += qbytes + (a.q != nullptr ? (uint32_t)nrow * 4u : 0u);
+            umma::mbar_expect_tx(&sm.bar_load, bytes);
             if (xi) umma::bulk_g2s(sm.r0, xi, kXBytes, &sm.bar_load);
             umma::bulk_g2s(sm.r1, w1i, kXBytes, &sm.bar_load);
+            if (it == 0 && bulk_bias) {
+                umma::bulk_g2s(sm.b1, prm + off.b1, HH * 4u, &sm.bar_load);
+                umma::bulk_g2s(sm.b2, prm + off.b2, 2u * HH * 4u, &sm.bar_load);   // b2, then w3
+            }
+            if (bulk_q) {
+                umma::bulk_g2s(sm.qt, qsrc, qbytes, &sm.bar_load);
+                if (a.q != nullptr) umma::bulk_g2s(sm.act, a.actions + row0, (uint32_t)nrow * 4u, &sm.bar_load);
+            }
         }
-        // the tile's actions and Q rows (one contiguous block) for the loss and
-        // the policy, read long before they are needed
-        {
-            const int nrow = B - row0 < TM ? B - row0 : TM;
+        if (!bulk_q) {
             if (a.q != nullptr) {
-                for (int e = tid; e < nrow * NA; e += kThreads) sm.qt[e] = __ldg(a.q + (int64_t)row0 * NA + e);
+                for (int e = tid; e < nrow * NA; e += kThreads) sm.qt[e] = __ldg(qsrc + e);
                 for (int e = tid; e < nrow; e += kThreads) sm.act[e] = __ldg(a.actions + row0 + e);
             } else {
-                for (int e = tid; e < nrow; e += kThreads) sm.qt[e] = __ldg(a.q_taken + row0 + e);
+                for (int e = tid; e < nrow; e += kThreads) sm.qt[e] = __ldg(qsrc + e);
             }
         }
         umma::fence_before_sync();
