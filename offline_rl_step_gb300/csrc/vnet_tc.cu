@@ -33,9 +33,13 @@
 // precision, so no mask decision moves).  The bf16 workload has one term and
 // one product.
 //
-// Shared memory: two 96 KB regions reused through the step:
-//   R0: X image -> h1 -> W2 image (for G4) -> dz1
-//   R1: W1 image -> W2 image (for G2) -> dz2 -> X image (for G5)
+// Shared memory: two 96 KB regions of three 32 KB plane slots, reused
+// through the step:
+//   R0: X image -> h1 (planes 0-2; G2, then planes 0-1 for G3)
+//       + dz2 plane 0 in slot 2 -> X planes 0-1 (for G5) in slots 0-1
+//   R1: W1 image -> W2 (planes 0-2; G2, then planes 0-1 for G4)
+//       + dz2 plane 1 in slot 2 -> dz1 (planes 0-1, for G5)
+// so W2 is loaded once per tile and G3, G4 run back to back.
 // Images arrive by bulk asynchronous copies (cp.async.bulk) on an mbarrier:
 // the weights from the per-step pack, the state tiles from the relabel
 // kernel (or, without those, are built here from the fp32 batch).
@@ -108,11 +112,13 @@ __device__ __forceinline__ void gemm(uint32_t d_tmem, const uint8_t* a, uint32_t
     }
 }
 
-// Store 16 fp32 values of row r, columns c0..c0+15 into a [128 x 128] image.
+// Store 16 fp32 values of row r, columns c0..c0+15 into a [128 x 128] image
+// whose planes lie `plane` bytes apart.
 // LEADING: only the two planes the three leading products read (dz2, dz1:
 // operands of the backward GEMMs alone); plane 2 is left as it was.
 template <int NP, bool LEADING = false>
-__device__ __forceinline__ void store16(uint8_t* img, int r, int c0, const float (&v)[16]) {
+__device__ __forceinline__ void store16(uint8_t* img, int r, int c0, const float (&v)[16],
+                                        uint32_t plane = kPlaneH) {
     constexpr int NW = NP == 3 && LEADING ? 2 : NP;   // planes written
     uint32_t t[NP][8];
 #pragma unroll
@@ -124,8 +130,8 @@ __device__ __forceinline__ void store16(uint8_t* img, int r, int c0, const float
     const uint32_t o0 = tc::img_off(r, c0, HH), o1 = tc::img_off(r, c0 + 8, HH);
 #pragma unroll
     for (int p = 0; p < NW; ++p) {
-        *reinterpret_cast<uint4*>(img + (uint32_t)p * kPlaneH + o0) = make_uint4(t[p][0], t[p][1], t[p][2], t[p][3]);
-        *reinterpret_cast<uint4*>(img + (uint32_t)p * kPlaneH + o1) = make_uint4(t[p][4], t[p][5], t[p][6], t[p][7]);
+        *reinterpret_cast<uint4*>(img + (uint32_t)p * plane + o0) = make_uint4(t[p][0], t[p][1], t[p][2], t[p][3]);
+        *reinterpret_cast<uint4*>(img + (uint32_t)p * plane + o1) = make_uint4(t[p][4], t[p][5], t[p][6], t[p][7]);
     }
 }
 
@@ -178,11 +184,12 @@ struct TcSmem {
     __align__(16) int32_t act[TM];              // the tile's actions
     float vrow[TM];                   // V of each row
     float vb3;                  // this CTA's db3 over its tiles
-    uint64_t bar_mma, bar_load;
+    uint64_t bar_mma, bar_load, bar_g3;   // bar_g3: dW2's GEMM done (the training kernel)
     uint32_t tmem_slot;
 };
 static_assert(sizeof(TcSmem) <= 227 * 1024, "tensor-core kernel shared memory above the per-CTA limit");
 static_assert(offsetof(TcSmem, w3) == offsetof(TcSmem, b2) + HH * sizeof(float), "w3 follows b2");
+static_assert(kMaxActions % 4 == 0, "the policy gives each of a row's four lanes kMaxActions / 4 actions");
 
 template <int NP>
 __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a, const uint8_t* __restrict__ wimg) {
@@ -203,10 +210,12 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     const uint8_t* w1i = wimg + (int64_t)net * tc::weight_image_bytes();
     const uint8_t* w2i = w1i + tc::w2_image_offset();
     constexpr uint32_t kXBytes = (uint32_t)NP * kPlaneX, kW2Bytes = (uint32_t)NP * kPlaneH;
+    constexpr uint32_t kX2Bytes = (uint32_t)(NP < 2 ? NP : 2) * kPlaneX;   // the planes G5 reads
 
     if (tid == 0) {
         umma::mbar_init(&sm.bar_mma, 1);
         umma::mbar_init(&sm.bar_load, 1);
+        umma::mbar_init(&sm.bar_g3, 1);
         umma::fence_mbar_init();
     }
     if (warp == 0) umma::tmem_alloc(&sm.tmem_slot, kTmemCols);
@@ -228,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     if (tid == 0) sm.vb3 = 0.0f;
     const float b3 = __ldg(prm + off.b3);
     uint32_t tmem = 0, tq = 0;
-    uint32_t ph_mma = 0, ph_load = 0;
+    uint32_t ph_mma = 0, ph_load = 0, ph_g3 = 0;
     bool ok = true;
     auto wait_mma = [&]() {
         ok &= umma::mbar_wait(&sm.bar_mma, ph_mma, kWaitNs);
@@ -333,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         }
         wait_mma();
 
-        // ---- epilogue 2: V, loss, dV, policy, dz2 -> R1, dW3 / db2 / db3 ----
+        // ---- epilogue 2: V, loss, dV, dz2; then dW3 / db2 / db3 beside G3, G4 ----
         // z2 is read from TMEM twice (for V, then for dz2) instead of being kept
         // in registers across the row reduction.
         if (epi) {
@@ -375,8 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
             if (cg == 0 && a.v_out != nullptr) a.v_out[(int64_t)net * B + b] = V;
         }
         if (epi && cg == 0) sm.vrow[row] = V;
-        // dz2 -> R1 (what G3 and G4 need); the column sums and the loss partial
-        // are computed while G3 runs, the policy while G4 runs
+        // dz2 in its two planes -> the plane-2 slots of R0 and R1, which G2 was
+        // the last to read (the backward GEMMs read planes 0 and 1 of h1 and
+        // W2), so W2 stays in R1 for G4 and G3, G4 run back to back
+        uint8_t* const dz2 = sm.r0 + 2u * kPlaneH;   // plane 1 at dz2 + kRegion
         if (epi) {
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
@@ -389,30 +400,35 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
                     const float z = g[j] + sm.b2[c0 + j];
                     g[j] = z > 0.0f ? dv * sm.w3[c0 + j] : 0.0f;
                 }
-                store16<NP, true>(sm.r1, row, c0, g);
+                store16<NP, true>(dz2, row, c0, g, kRegion);
             }
         }
         umma::fence_smem_to_async();
         umma::fence_before_sync();
         __syncthreads();
-        // ---- G3: dW2 = dz2^T . h1 ----
+        // ---- G3: dW2 = dz2^T . h1, then G4: dh1 = dz2 . W2 (into z1's
+        // columns: the ReLU mask of z1 is in registers) ----
         if (tid == 0) {
             umma::fence_after_sync();
-            gemm<NP, true>(tmem + TM_DW2, sm.r1, kPlaneH, HH, true, sm.r0, kPlaneH, HH, true, TM / 16, HH, it > 0);
+            gemm<NP, true>(tmem + TM_DW2, dz2, kRegion, HH, true, sm.r0, kPlaneH, HH, true, TM / 16, HH, it > 0);
+            umma::commit(&sm.bar_g3);
+            gemm<NP, true>(tmem + TM_Z1, dz2, kRegion, HH, false, sm.r1, kPlaneH, HH, true, HH / 16, HH);
             umma::commit(&sm.bar_mma);
+            // h1 is no longer read once G3 is done: the planes of the X image
+            // that G5 reads stream into R0 while G4 runs
+            ok &= umma::mbar_wait(&sm.bar_g3, ph_g3, kWaitNs);
+            ph_g3 ^= 1u;
+            umma::fence_after_sync();
+            if (xi) {
+                umma::mbar_expect_tx(&sm.bar_load, kX2Bytes);
+                umma::bulk_g2s(sm.r0, xi, kX2Bytes, &sm.bar_load);
+            }
         }
         if (epi && cg == 0) {
             const float ls = warp_sum(lossp), ds = warp_sum(dv);
             if (lane == 0) { sm.lred[0][q] = ls; sm.lred[1][q] = ds; }
         }
-        wait_mma();
-        // ---- stage 3: W2 image -> R0 (h1 is no longer read) ----
-        if (tid == 0) {
-            umma::mbar_expect_tx(&sm.bar_load, kW2Bytes);
-            umma::bulk_g2s(sm.r0, w2i, kW2Bytes, &sm.bar_load);
-        }
-        // column sums for dW3 and db2 while W2 arrives (no MMA runs: TMEM reads
-        // and shuffles beside a running GEMM slow both)
+        // column sums for dW3 and db2 beside the two GEMMs
         if (epi) {
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
@@ -449,57 +465,10 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
             a.tile_loss[(int64_t)net * a.net_tile_stride + tile] = l;
             sm.vb3 += d3;
         }
-        wait_load();
-        // ---- G4: dh1 = dz2 . W2 ----
-        if (tid == 0) {
-            umma::fence_after_sync();
-            gemm<NP, true>(tmem + TM_Z1, sm.r1, kPlaneH, HH, false, sm.r0, kPlaneH, HH, true, HH / 16, HH);
-            umma::commit(&sm.bar_mma);
-        }
-        // the policy while G4 runs: four threads per row (lanes 4r .. 4r + 3 of
-        // a warp), each over actions j, j + 4, ...; max / argmax (lowest index on
-        // ties) and the sum of exponentials combined over the four lanes
-        if (epi && a.pi_out != nullptr) {
-            const int pr = et >> 2, j = et & 3;
-            const int pb = row0 + pr;
-            const bool prow = pb < B;
-            const float Vp = sm.vrow[pr];
-            const float* qr = sm.qt + pr * NA;
-            float zmax = -INFINITY, amax = -INFINITY;
-            int best = NA;
-            if (prow)
-                for (int k = j; k < NA; k += 4) {
-                    const float adv = fminf(fmaxf(qr[k] - Vp, -10.0f), 10.0f);
-                    if (adv > amax) { amax = adv; best = k; }
-                    zmax = fmaxf(zmax, a.beta * adv);
-                }
-#pragma unroll
-            for (int o = 1; o < 4; o <<= 1) {
-                const float oa = __shfl_xor_sync(0xffffffffu, amax, o);
-                const int ob = __shfl_xor_sync(0xffffffffu, best, o);
-                if (oa > amax || (oa == amax && ob < best)) { amax = oa; best = ob; }
-                zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
-            }
-            float sum = 0.0f;
-            if (prow)
-                for (int k = j; k < NA; k += 4) sum += expf(a.beta * fminf(fmaxf(qr[k] - Vp, -10.0f), 10.0f) - zmax);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            if (prow) {
-                float* po = a.pi_out + ((int64_t)net * B + pb) * NA;
-                for (int k = j; k < NA; k += 4)
-                    po[k] = expf(a.beta * fminf(fmaxf(qr[k] - Vp, -10.0f), 10.0f) - zmax) / sum;
-                if (j == 0 && a.argmax_out != nullptr) a.argmax_out[(int64_t)net * B + pb] = best < NA ? best : 0;
-            }
-        }
         wait_mma();
-        // dz2 is no longer read: the X image streams into R1 during epilogue 4
-        if (tid == 0 && xi) {
-            umma::mbar_expect_tx(&sm.bar_load, kXBytes);
-            umma::bulk_g2s(sm.r1, xi, kXBytes, &sm.bar_load);
-        }
 
-        // ---- epilogue 4: dz1 = dh1 * 1[z1 > 0] -> R0; db1 ----
+        // ---- epilogue 4: dz1 = dh1 * 1[z1 > 0] -> R1 (W2 is no longer read);
+        // without relabel images the X image is built in R0 here ----
         if (epi) {
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
@@ -509,10 +478,10 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
                 umma::tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] = ((mask1 >> (cc * 16 + j)) & 1u) ? v[j] : 0.0f;
-                store16<NP, true>(sm.r0, row, c0, v);
+                store16<NP, true>(sm.r1, row, c0, v);
             }
         }
-        if (!xi) build_x(sm.r1, NP, a.states, a.stride, row0, B, S);
+        if (!xi) build_x(sm.r0, NP, a.states, a.stride, row0, B, S);
         umma::fence_smem_to_async();
         umma::fence_before_sync();
         __syncthreads();
@@ -520,8 +489,53 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         // ---- G5: dW1 = dz1^T . X ----
         if (tid == 0) {
             umma::fence_after_sync();
-            gemm<NP, true>(tmem + TM_DW1, sm.r0, kPlaneH, HH, true, sm.r1, kPlaneX, KX, true, TM / 16, KX, it > 0);
+            gemm<NP, true>(tmem + TM_DW1, sm.r1, kPlaneH, HH, true, sm.r0, kPlaneX, KX, true, TM / 16, KX, it > 0);
             umma::commit(&sm.bar_mma);
+        }
+        // the policy while G5 runs (beside G3 and G4 it would share their
+        // window with the column sums): four threads per row (lanes 4r .. 4r + 3
+        // of a warp), each over actions j, j + 4, ... (its exponentials kept in
+        // registers); max / argmax (lowest index on ties) and the sum of
+        // exponentials combined over the four lanes
+        if (epi && a.pi_out != nullptr) {
+            constexpr int kPer = kMaxActions / 4;
+            const int pr = et >> 2, j = et & 3;
+            const int pb = row0 + pr;
+            const bool prow = pb < B;
+            const float Vp = sm.vrow[pr];
+            const float* qr = sm.qt + pr * NA;
+            float adv[kPer];
+            float zmax = -INFINITY, amax = -INFINITY;
+            int best = NA;
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int k = j + 4 * i;
+                adv[i] = prow && k < NA ? fminf(fmaxf(qr[k] - Vp, -10.0f), 10.0f) : -INFINITY;
+                if (adv[i] > amax) { amax = adv[i]; best = k; }
+                if (prow && k < NA) zmax = fmaxf(zmax, a.beta * adv[i]);
+            }
+#pragma unroll
+            for (int o = 1; o < 4; o <<= 1) {
+                const float oa = __shfl_xor_sync(0xffffffffu, amax, o);
+                const int ob = __shfl_xor_sync(0xffffffffu, best, o);
+                if (oa > amax || (oa == amax && ob < best)) { amax = oa; best = ob; }
+                zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
+            }
+            float sum = 0.0f;
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                adv[i] = j + 4 * i < NA ? expf(a.beta * adv[i] - zmax) : 0.0f;
+                sum += adv[i];
+            }
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            if (prow) {
+                float* po = a.pi_out + ((int64_t)net * B + pb) * NA;
+#pragma unroll
+                for (int i = 0; i < kPer; ++i)
+                    if (j + 4 * i < NA) po[j + 4 * i] = adv[i] / sum;
+                if (j == 0 && a.argmax_out != nullptr) a.argmax_out[(int64_t)net * B + pb] = best < NA ? best : 0;
+            }
         }
         // db1: with S < 64 G5 yields it in its last column (the ones column of
         // the state-tile image); else column sums while G5 runs
