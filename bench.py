@@ -42,7 +42,7 @@ KERNEL_SOURCES = {
 # the kernel sources the capture ran (source_hash)
 NCU_TRAFFIC = {
     # profiles/vnet_tc_prod_fp32_B16384_H128.md (ncu --set full, one launch)
-    ("vnet_tc (tcgen05)", "prod_fp32_B16384_S50_H128_A5"): ("826d7c19df437fb9", 6921728),
+    ("vnet_tc (tcgen05)", "prod_fp32_B16384_S50_H128_A5"): ("53640d0829ea53b5", 6917376),
 }
 
 

@@ -83,7 +83,6 @@ __device__ __forceinline__ void fused_norms_adam(const ReduceLaunch& a, const Ad
     const int tid = threadIdx.x, tx = tid % EL, ty = tid / EL, lane = tid & 31, wid = tid >> 5;
     const int net = blockIdx.y, G = gridDim.x, nsrc = a.n_src;
     const int64_t P = a.P;
-    const int64_t i4 = (int64_t)blockIdx.x * kRedElems + 4 * tx;
     // Adam runs one element per thread (threads 0 .. 4 EL - 1): this
     // thread's weight, moments and target, read before the barrier (only
     // this block writes them)
