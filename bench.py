@@ -42,7 +42,7 @@ KERNEL_SOURCES = {
 # the kernel sources the capture ran (source_hash)
 NCU_TRAFFIC = {
     # profiles/vnet_tc_prod_fp32_B16384_H128.md (ncu --set full, one launch)
-    ("vnet_tc (tcgen05)", "prod_fp32_B16384_S50_H128_A5"): ("53640d0829ea53b5", 6917376),
+    ("vnet_tc (tcgen05)", "prod_fp32_B16384_S50_H128_A5"): ("aaaad2ec427965ce", 6917376),
 }
 
 
@@ -551,7 +551,8 @@ def run_ours(args, w):
 def forward_bench(run, steps, repeats, pk, pk_kind, world):
     """The IQL bootstrap target r + gamma (1 - done) V(s') of the relabelled batch (ofrl_iql_target: V
     forward on the next states, tensor cores where the step's V kernel is the fused one): median of
-    `repeats` regions of `steps` calls, rows/s and the forward's flops against the bf16 peak."""
+    `repeats` regions of `steps` calls through the API, and of the same calls replayed from a CUDA graph
+    (the device's time); rows/s, and the forward's flops against the bf16 peak."""
     torch, ofrl, w = run.torch, run.ofrl, run.w
     b = w.batch
     tgt = torch.empty(b, device="cuda")
@@ -572,13 +573,34 @@ def forward_bench(run, steps, repeats, pk, pk_kind, world):
         torch.cuda.synchronize()
         regions.append(max_over_ranks(e0.elapsed_time(e1), "cuda"))
     ms = statistics.median(regions) / steps
+    # the same calls captured once in a CUDA graph and replayed: the device's
+    # time per call, free of the host's per-call argument checks and launches
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(steps):
+            call()
+    graph.replay()
+    torch.cuda.synchronize()
+    gregions = []
+    for _ in range(repeats):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        gregions.append(max_over_ranks(e0.elapsed_time(e1), "cuda"))
+    del graph
+    gms = statistics.median(gregions) / steps
     flops = 2 * b * (w.state_dim * w.hidden + w.hidden ** 2 + w.hidden)
     tpk = pk["bf16_tflops"]
     return {"rows_per_s": whole_job_rate(world, 1, b, ms), "us_per_call": ms * 1e3, "batch": b,
+            "device_rows_per_s": whole_job_rate(world, 1, b, gms), "device_us_per_call": gms * 1e3,
             "vnet_path": run.ctx.vnet_path(1),
-            "tflops": flops / (ms / 1e3) / 1e12, "frac_of_bf16_burst_peak": flops / (ms / 1e3) / 1e12 / tpk,
+            "tflops": flops / (gms / 1e3) / 1e12, "frac_of_bf16_burst_peak": flops / (gms / 1e3) / 1e12 / tpk,
             "peak_source": f"bf16_tflops ({pk_kind})",
-            "note": "one call = weight pack + forward kernel; median of regions of back-to-back calls"}
+            "note": "one call = weight pack + forward kernel; us_per_call: median of regions of back-to-back "
+                    "calls through the API (bound by the host's per-call cost when it exceeds the device's); "
+                    "device_us_per_call and tflops: the same calls replayed from a CUDA graph"}
 
 
 def other_e2e_forms(run, world):

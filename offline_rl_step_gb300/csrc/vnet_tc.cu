@@ -191,6 +191,15 @@ static_assert(sizeof(TcSmem) <= 227 * 1024, "tensor-core kernel shared memory ab
 static_assert(offsetof(TcSmem, w3) == offsetof(TcSmem, b2) + HH * sizeof(float), "w3 follows b2");
 static_assert(kMaxActions % 4 == 0, "the policy gives each of a row's four lanes kMaxActions / 4 actions");
 
+// 16 consecutive floats of shared memory (16-byte aligned) by four 16-byte loads
+__device__ __forceinline__ void lds16(const float* p, float (&o)[16]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 t = reinterpret_cast<const float4*>(p)[i];
+        o[4 * i] = t.x; o[4 * i + 1] = t.y; o[4 * i + 2] = t.z; o[4 * i + 3] = t.w;
+    }
+}
+
 template <int NP>
 __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a, const uint8_t* __restrict__ wimg) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -321,9 +330,11 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
                 float v[16];
                 umma::tmem_ld16(tq + TM_Z1 + (uint32_t)c0, v);
                 umma::tmem_ld_wait();
+                float bb[16];
+                lds16(sm.b1 + c0, bb);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float z = v[j] + sm.b1[c0 + j];
+                    const float z = v[j] + bb[j];
                     v[j] = z < 0.0f ? 0.0f : z;
                     if (v[j] > 0.0f) mask1 |= 1u << (cc * 16 + j);
                 }
@@ -353,10 +364,13 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
                 float v[16];
                 umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, v);
                 umma::tmem_ld_wait();
+                float bb[16], ww[16];
+                lds16(sm.b2 + c0, bb);
+                lds16(sm.w3 + c0, ww);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float z = v[j] + sm.b2[c0 + j];
-                    vp = fmaf(z < 0.0f ? 0.0f : z, sm.w3[c0 + j], vp);
+                    const float z = v[j] + bb[j];
+                    vp = fmaf(z < 0.0f ? 0.0f : z, ww[j], vp);
                 }
             }
             sm.vsum[cg][row] = vp;
@@ -395,10 +409,13 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
                 float g[16];
                 umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, g);
                 umma::tmem_ld_wait();
+                float bb[16], ww[16];
+                lds16(sm.b2 + c0, bb);
+                lds16(sm.w3 + c0, ww);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float z = g[j] + sm.b2[c0 + j];
-                    g[j] = z > 0.0f ? dv * sm.w3[c0 + j] : 0.0f;
+                    const float z = g[j] + bb[j];
+                    g[j] = z > 0.0f ? dv * ww[j] : 0.0f;
                 }
                 store16<NP, true>(dz2, row, c0, g, kRegion);
             }
@@ -436,10 +453,13 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
                 float g[16], hw[16];
                 umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, g);
                 umma::tmem_ld_wait();
+                float bb[16], ww[16];
+                lds16(sm.b2 + c0, bb);
+                lds16(sm.w3 + c0, ww);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float z = g[j] + sm.b2[c0 + j];
-                    g[j] = z > 0.0f ? dv * sm.w3[c0 + j] : 0.0f;
+                    const float z = g[j] + bb[j];
+                    g[j] = z > 0.0f ? dv * ww[j] : 0.0f;
                     hw[j] = dv * (z < 0.0f ? 0.0f : z);
                 }
                 const float s3 = colsum16(hw);
@@ -701,9 +721,11 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_forward_kernel(const Vnet
                 float v[16];
                 umma::tmem_ld16(tq + TM_Z1 + (uint32_t)c0, v);
                 umma::tmem_ld_wait();
+                float bb[16];
+                lds16(sm.b1 + c0, bb);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float z = v[j] + sm.b1[c0 + j];
+                    const float z = v[j] + bb[j];
                     v[j] = z < 0.0f ? 0.0f : z;
                 }
                 store16<NP>(sm.r0, row, c0, v);
@@ -729,10 +751,13 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_forward_kernel(const Vnet
                 float v[16];
                 umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, v);
                 umma::tmem_ld_wait();
+                float bb[16], ww[16];
+                lds16(sm.b2 + c0, bb);
+                lds16(sm.w3 + c0, ww);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float z = v[j] + sm.b2[c0 + j];
-                    vp = fmaf(z < 0.0f ? 0.0f : z, sm.w3[c0 + j], vp);
+                    const float z = v[j] + bb[j];
+                    vp = fmaf(z < 0.0f ? 0.0f : z, ww[j], vp);
                 }
             }
             sm.vsum[cg][row] = vp;

@@ -175,6 +175,36 @@ def test_iql_target_fp32(s, h, b, path):
 
 
 @pytest.mark.parametrize("path", [None, "cuda_cores"], ids=["default", "cuda_cores"])
+def test_iql_target_in_a_cuda_graph(path):
+    # the forward path captured in a CUDA graph (weight pack + forward kernel,
+    # launched on the capturing stream) and replayed gives the direct call's
+    # results bit for bit, on new inputs copied into the captured buffers
+    b = 3000
+    ofrl, ctx, w, params, x, r, d = _forward_case(50, 128, b, seed=11, path=path)
+    p_d, x_d, r_d, d_d = dev(params), dev(x), dev(r), dev(d)
+    t, vn = torch.empty(b, device="cuda"), torch.empty(b, device="cuda")
+    call = lambda: ofrl.iql_target(ctx, p_d, x_d, r_d, d_d, 0.99, t, v_next_out=vn)
+    call()
+    torch.cuda.synchronize()
+    v0 = vn.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    rng = np.random.default_rng(12)
+    x_d.copy_(dev(x + rng.standard_normal(x.shape).astype(np.float32)))
+    p_d.copy_(dev(params * np.float32(0.9)))
+    g.replay()
+    torch.cuda.synchronize()
+    tg, vg = t.clone(), vn.clone()
+    call()
+    torch.cuda.synchronize()
+    ctx.close()
+    assert torch.equal(tg.view(torch.int32), t.view(torch.int32))
+    assert torch.equal(vg.view(torch.int32), vn.view(torch.int32))
+    assert not torch.equal(vg, v0)   # the replay read the new inputs
+
+
+@pytest.mark.parametrize("path", [None, "cuda_cores"], ids=["default", "cuda_cores"])
 def test_forward_values_bf16(path):
     ofrl, ctx, w, params, x, _, _ = _forward_case(50, 128, 4096, prec="bf16", seed=5, path=path)
     v = torch.empty(4096, device="cuda")
