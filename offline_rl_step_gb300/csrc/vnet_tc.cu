@@ -36,7 +36,7 @@
 // Shared memory: two 96 KB regions of three 32 KB plane slots, reused
 // through the step:
 //   R0: X image -> h1 (planes 0-2; G2, then planes 0-1 for G3)
-//       + dz2 plane 0 in slot 2 -> X planes 0-1 (for G5) in slots 0-1
+//       + dz2 plane 0 in slot 2 -> X planes 0-1 (for G5, 32 KB) in slot 0
 //   R1: W1 image -> W2 (planes 0-2; G2, then planes 0-1 for G4)
 //       + dz2 plane 1 in slot 2 -> dz1 (planes 0-1, for G5)
 // so W2 is loaded once per tile and G3, G4 run back to back.
