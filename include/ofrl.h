@@ -51,7 +51,7 @@ typedef int32_t ofrl_status;
 enum {
     OFRL_OK = 0,
     OFRL_EINVAL = -1,        /* bad argument: null pointer, size, stride, alignment */
-    OFRL_EUNSUPPORTED = -2,  /* valid request this build does not implement (e.g. H not in {64,128,256}) */
+    OFRL_EUNSUPPORTED = -2,  /* valid request the library does not implement (e.g. H not in {64,128,256}) */
     OFRL_ECUDA = -3,         /* a CUDA runtime call or launch failed */
     OFRL_ETIMEOUT = -4       /* reserved: a bounded device-side wait gave up */
 };

@@ -25,8 +25,8 @@ difference between the two sides' weights (zero on the first step):
     within SPLIT_REL = 3.1 * 2^-18 of |x y|, added linearly to dh1 (so to
     dz1) and to dW1, db1 and dW2.
 
-The tests accept a CUDA value inside the benchmark spec's tolerance or inside
-this bound; a CPU test checks that an independent fp32 evaluation stays
+The tests accept a CUDA value inside the stated tolerance (1e-4 relative /
+1e-5 absolute) or inside this bound; a CPU test checks that an independent fp32 evaluation stays
 inside it and that it stays tight on the bulk of the elements.
 """
 import numpy as np
@@ -284,7 +284,7 @@ def grad_ok(gpu, ref, unc, rtol=1e-4, atol=1e-5, norm_rtol=1e-4):
 
 
 def within(gpu, ref, unc, rtol, atol):
-    """Element-wise: inside the benchmark spec's tolerance or inside the fp32 bound."""
+    """Element-wise: inside the stated tolerance (rtol / atol) or inside the fp32 bound."""
     gpu = np.asarray(gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     err = np.abs(gpu - ref)
