@@ -1,8 +1,8 @@
 // IQL value network V(s) forward, expectile loss, policy and backward for one
 // 128-row batch tile per CTA on the 5th-generation tensor cores (tcgen05),
-// hidden width 128 (64 runs zero-padded to 128 units: padded units have zero
-// weights, biases and output weight, so their activations and gradients are
-// exactly zero, and only the H x H, H x S and H entries are written out).
+// hidden width 128 (64 runs in the same images zero-padded to 128 units, the
+// GEMMs over the units cut to 64 and the padded columns' epilogue work
+// skipped; only the H x H, H x S and H entries are written out).
 //
 // Method: "GPU IQL + HER Porting Plan", "IQL (CPU)" items 1-3 and "CUDA
 // Kernel: iql_value_kernel.cu"; same results as the CUDA-core kernel
@@ -213,6 +213,12 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
     const int S = a.state_dim, B = a.batch, NA = a.num_actions;
     const int n_tiles = (B + TM - 1) / TM;
     const int Hn = a.hidden;   // 64 or 128: the weights are zero-padded to 128 units
+    // the units computed: at H = 64 the GEMMs take K and N = 64 where they
+    // run over units, and the epilogue warps of columns 64-127 skip their
+    // work (what lies there is never read, or lands only in the padded rows
+    // of dW2 and dW1, which are not written out)
+    const int HN = Hn <= 64 ? 64 : HH;
+    const bool live = cg * 32 < HN;   // this epilogue warp's columns are units
     const Offsets off = offsets_of(S, Hn);
     const float* __restrict__ prm = a.params[net];
     const float tau = a.tau[net];
@@ -311,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         // ---- G1: z1 = X . W1^T ----
         if (tid == 0) {
             umma::fence_after_sync();
-            gemm<NP>(tmem + TM_Z1, sm.r0, kPlaneX, KX, false, sm.r1, kPlaneX, KX, false, KX / 16, HH);
+            gemm<NP>(tmem + TM_Z1, sm.r0, kPlaneX, KX, false, sm.r1, kPlaneX, KX, false, KX / 16, HN);
             umma::commit(&sm.bar_mma);
         }
         wait_mma();
@@ -323,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
 
         // ---- epilogue 1: h1 = relu(z1 + b1) -> R0; ReLU mask bits kept ----
         uint32_t mask1 = 0;
-        if (epi) {
+        if (epi && live) {
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int c0 = cg * 32 + cc * 16;
@@ -348,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         // ---- G2: z2 = h1 . W2^T ----
         if (tid == 0) {
             umma::fence_after_sync();
-            gemm<NP>(tmem + TM_Z2, sm.r0, kPlaneH, HH, false, sm.r1, kPlaneH, HH, false, HH / 16, HH);
+            gemm<NP>(tmem + TM_Z2, sm.r0, kPlaneH, HH, false, sm.r1, kPlaneH, HH, false, HN / 16, HN);
             umma::commit(&sm.bar_mma);
         }
         wait_mma();
@@ -359,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         if (epi) {
             float vp = 0.0f;
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
+            for (int cc = 0; cc < 2 && live; ++cc) {
                 const int c0 = cg * 32 + cc * 16;
                 float v[16];
                 umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, v);
@@ -402,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         // the last to read (the backward GEMMs read planes 0 and 1 of h1 and
         // W2), so W2 stays in R1 for G4 and G3, G4 run back to back
         uint8_t* const dz2 = sm.r0 + 2u * kPlaneH;   // plane 1 at dz2 + kRegion
-        if (epi) {
+        if (epi && live) {
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int c0 = cg * 32 + cc * 16;
@@ -427,9 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         // columns: the ReLU mask of z1 is in registers) ----
         if (tid == 0) {
             umma::fence_after_sync();
-            gemm<NP, true>(tmem + TM_DW2, dz2, kRegion, HH, true, sm.r0, kPlaneH, HH, true, TM / 16, HH, it > 0);
+            gemm<NP, true>(tmem + TM_DW2, dz2, kRegion, HH, true, sm.r0, kPlaneH, HH, true, TM / 16, HN, it > 0);
             umma::commit(&sm.bar_g3);
-            gemm<NP, true>(tmem + TM_Z1, dz2, kRegion, HH, false, sm.r1, kPlaneH, HH, true, HH / 16, HH);
+            gemm<NP, true>(tmem + TM_Z1, dz2, kRegion, HH, false, sm.r1, kPlaneH, HH, true, HN / 16, HN);
             umma::commit(&sm.bar_mma);
             // h1 is no longer read once G3 is done: the planes of the X image
             // that G5 reads stream into R0 while G4 runs
@@ -446,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
             if (lane == 0) { sm.lred[0][q] = ls; sm.lred[1][q] = ds; }
         }
         // column sums for dW3 and db2 beside the two GEMMs
-        if (epi) {
+        if (epi && live) {
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int c0 = cg * 32 + cc * 16;
@@ -489,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
 
         // ---- epilogue 4: dz1 = dh1 * 1[z1 > 0] -> R1 (W2 is no longer read);
         // without relabel images the X image is built in R0 here ----
-        if (epi) {
+        if (epi && live) {
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int c0 = cg * 32 + cc * 16;
@@ -559,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_kernel(const VnetLaunch a
         }
         // db1: with S < 64 G5 yields it in its last column (the ones column of
         // the state-tile image); else column sums while G5 runs
-        if (epi && !tc::ones_column(KX - 1, S)) {
+        if (epi && live && !tc::ones_column(KX - 1, S)) {
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int c0 = cg * 32 + cc * 16;
@@ -653,6 +659,8 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_forward_kernel(const Vnet
     const int n_tiles = (B + TM - 1) / TM;
     const int Hn = a.hidden;
     const Offsets off = offsets_of(S, Hn);
+    const int HN = Hn <= 64 ? 64 : HH;   // the units computed (as in the training kernel)
+    const bool live = cg * 32 < HN;
     const float* __restrict__ prm = a.params[0];
     const uint8_t* w1i = wimg;
     const uint8_t* w2i = w1i + tc::w2_image_offset();
@@ -705,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_forward_kernel(const Vnet
         // ---- G1: z1 = X . W1^T ----
         if (tid == 0) {
             umma::fence_after_sync();
-            gemm<NP>(tmem + TM_Z1, sm.r0, kPlaneX, KX, false, sm.r1, kPlaneX, KX, false, KX / 16, HH);
+            gemm<NP>(tmem + TM_Z1, sm.r0, kPlaneX, KX, false, sm.r1, kPlaneX, KX, false, KX / 16, HN);
             umma::commit(&sm.bar_mma);
         }
         wait_mma();
@@ -714,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_forward_kernel(const Vnet
             umma::bulk_g2s(sm.r1, w2i, kW2Bytes, &sm.bar_load);
         }
         // ---- epilogue 1: h1 = relu(z1 + b1) -> R0 ----
-        if (epi) {
+        if (epi && live) {
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int c0 = cg * 32 + cc * 16;
@@ -738,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_forward_kernel(const Vnet
         // ---- G2: z2 = h1 . W2^T ----
         if (tid == 0) {
             umma::fence_after_sync();
-            gemm<NP>(tmem + TM_Z2, sm.r0, kPlaneH, HH, false, sm.r1, kPlaneH, HH, false, HH / 16, HH);
+            gemm<NP>(tmem + TM_Z2, sm.r0, kPlaneH, HH, false, sm.r1, kPlaneH, HH, false, HN / 16, HN);
             umma::commit(&sm.bar_mma);
         }
         wait_mma();
@@ -746,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1) vnet_tc_forward_kernel(const Vnet
         if (epi) {
             float vp = 0.0f;
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
+            for (int cc = 0; cc < 2 && live; ++cc) {
                 const int c0 = cg * 32 + cc * 16;
                 float v[16];
                 umma::tmem_ld16(tq + TM_Z2 + (uint32_t)c0, v);
