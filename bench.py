@@ -42,7 +42,7 @@ KERNEL_SOURCES = {
 # the kernel sources the capture ran (source_hash)
 NCU_TRAFFIC = {
     # profiles/vnet_tc_prod_fp32_B16384_H128.md (ncu --set full, one launch)
-    ("vnet_tc (tcgen05)", "prod_fp32_B16384_S50_H128_A5"): ("6a199417a184eb57", 6916608),
+    ("vnet_tc (tcgen05)", "prod_fp32_B16384_S50_H128_A5"): ("5f87a55b6e9d31be", 6908928),
 }
 
 
