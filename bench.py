@@ -172,8 +172,9 @@ print(json.dumps([k, el]))
 
 def cpu_baseline(w, seconds):
     """The oracle as it stands, on this host, on a bounded sample of the workload: whole steps with numpy's
-    default BLAS threading, and (a separate process, one BLAS thread) the first few steps on one core."""
-    k, el = _oracle_steps(w, 50, seconds)
+    default BLAS threading for `seconds` of CPU work, and (a separate process, one BLAS thread) the first
+    few steps on one core."""
+    k, el = _oracle_steps(w, 10 ** 6, seconds)
     out = {"value": k * w.batch / el, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
            "sample": f"{k} full steps (B={w.batch}) of {w.name} in {el:.1f} s, numpy fp64 with its default "
                      f"BLAS threading; index sampling in single-threaded Python"}
