@@ -43,12 +43,12 @@ def _fwd_bwd(s, h, b, tau, prec="fp32", seed=0, stride=None, path=None):
 
 @pytest.mark.parametrize("s,h,b", [(48, 64, 256), (50, 128, 16384), (50, 128, 300), (50, 256, 200),
                                    (50, 256, 16384), (7, 64, 1), (64, 128, 129), (63, 128, 1000),
-                                   (50, 128, 40000), (64, 128, 40000)])
+                                   (50, 128, 40000), (64, 128, 40000), (64, 64, 40000)])
 def test_value_fwd_bwd_fp32(s, h, b):
     # B = 40000: 313 tiles, so the fused kernel's CTAs run two or three tiles
     # each and build the state tiles themselves (no relabel images), for G1
     # and again for G5; S = 64 leaves no ones column, so db1 comes from
-    # column sums
+    # column sums (at H = 64 only the warps of the 64 units' columns run)
     (v, loss, g), (rv, rl, rg, vu, gu) = _fwd_bwd(s, h, b, 0.7, seed=s + h + b)
     assert within(v, rv, vu, RTOL, ATOL).all(), "V outside tolerance and fp32 bound"
     assert_close(loss, rl, what="loss")
